@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the GPTQ per-layer path on GB300: ms per layer, weights quantized / s.
+
+One step = the whole path on one layer: Hessian of the calibration activations
+(gptq_hessian_accumulate), dead columns + damping + inverse-Hessian factor (gptq_prepare),
+the blocked column sweep with lazy trailing updates and packing (gptq_quantize_layer).
+
+Default workload: a 4096 x 4096 layer, 262144 fp16 calibration tokens (128 x 2048) with
+8 outlier channels and 41 dead channels, bf16 weights, 4-bit per-row asymmetric grid,
+B = 128, damping 1 % -- synthetic, seeded.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank quantizes its own copy of the layer (independent problems, no
+collective on the data path): weak scaling, value = all ranks' weights / max time.
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a bounded
+sample of the same workload scaled to the full layer.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per layer & weights quantized/sec (4096×4096 int4 GPTQ), % roofline"
+UNIT = "weights/s"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="layer4096_n262144")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--n-tok", type=int, default=None, help="override token count (smaller runs)")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def reduce_max(value, device=None):
+    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(weights_per_rank, world, ms_step):
+    """Weak scaling: every rank quantizes its own layer; all ranks' weights / max time."""
+    return world * weights_per_rank / (ms_step / 1e3)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.th = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [t.strip() for t in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in self.rows:
+            for name, v in zip(self.NAMES, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(self.rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm): bounded sample scaled to the full layer
+# ---------------------------------------------------------------------------------------
+
+def oracle_sample(X_host_f32_rows, W_host, layer, bits, block, damp, tok_sample, row_sample):
+    """Times the oracle on a sample: Hessian over `tok_sample` tokens, the full prepare
+    at this d_in, the sweep of `row_sample` rows.  Returns (est_seconds_full, detail)."""
+    import numpy as np
+    from oracle import gptq_oracle as O
+    n_tok = layer.act.n_tok
+    m = layer.d_out
+    Xs = X_host_f32_rows[:tok_sample]
+    t0 = time.perf_counter()
+    H = O.hessian(Xs)
+    t1 = time.perf_counter()
+    Hd, dead, _ = O.damp_hessian(H, damp)
+    U = O.inverse_cholesky_upper(Hd)
+    t2 = time.perf_counter()
+    Ws = W_host[:row_sample]
+    scale, zero = O.row_grid(Ws, bits)
+    codes, _ = O.gptq_quantize(Ws, U, scale, zero, bits, block=block, dead=dead)
+    O.pack_codes(codes, bits)
+    t3 = time.perf_counter()
+    est = (t1 - t0) * n_tok / tok_sample + (t2 - t1) + (t3 - t2) * m / row_sample
+    detail = {"hessian_s": t1 - t0, "prepare_s": t2 - t1, "sweep_s": t3 - t2,
+              "tok_sample": tok_sample, "row_sample": row_sample}
+    _ = np
+    return est, detail
+
+
+def host_cores():
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            n = min(n, int(os.environ[k]))
+    return n
+
+
+# ---------------------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    from post_weight_quantization_03_gb300 import build_lib, gptq
+    from post_weight_quantization_03_gb300 import synthetic as S
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    build_lib.build()
+    gptq.load()
+
+    wl = S.WORKLOADS[args.workload]
+    layer = wl.layers[0]
+    bits, block, damp = wl.bits[-1], wl.block, wl.damp
+    act = layer.act
+    if args.n_tok:
+        from dataclasses import replace
+        act = replace(act, n_tok=args.n_tok)
+        layer = replace(layer, act=act)
+    m, d, n = layer.d_out, act.d_in, act.n_tok
+
+    # inputs resident in HBM (drawn on the device, seeded; untimed)
+    A = S.mixing_matrix(d, act.seed, dev)
+    X = S.activations(act, device=dev, A=A)
+    del A
+    W = S.layer_weights(layer, dev)
+    torch.cuda.synchronize()
+
+    # outputs and workspaces (allocated once, outside the timed region)
+    H = torch.empty(d, d, dtype=torch.float32, device=dev)
+    U = torch.empty(d, d, dtype=torch.float32, device=dev)
+    dm = torch.empty(d, dtype=torch.uint8, device=dev)
+    qp = torch.empty(m, gptq.packed_words(d, bits), dtype=torch.int32, device=dev)
+    sc = torch.empty(m, dtype=torch.float32, device=dev)
+    zr = torch.empty(m, dtype=torch.int32, device=dev)
+    ws_p = gptq.workspace(gptq.gptq_prepare_workspace_bytes(d), dev)
+    ws_q = gptq.workspace(gptq.gptq_quantize_workspace_bytes(m, d, bits, block), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(record=None):
+        e = [ev() for _ in range(4)] if record is not None else None
+        if e: e[0].record(stream)
+        gptq.hessian(X, H, accumulate=False, stream=stream)
+        if e: e[1].record(stream)
+        gptq.prepare(H, damp, U=U, dead_mask=dm, ws=ws_p, stream=stream)
+        if e: e[2].record(stream)
+        gptq.quantize(W, U, bits, block, dm, ws=ws_q, stream=stream, out=(qp, sc, zr, None))
+        if e:
+            e[3].record(stream)
+            record.append(e)
+
+    args.warmup = max(3, args.warmup)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region (device-resident inputs) -----------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.4)  # let the sampler produce a first row
+    launches0 = gptq.gptq_kernel_launches()
+    stage_events = []
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(stage_events)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = gptq.gptq_kernel_launches() - launches0
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        dist.barrier()
+    ms_total = reduce_max(ms_total, dev)
+    ms_step = ms_total / args.steps
+    st_h = statistics.mean(e[0].elapsed_time(e[1]) for e in stage_events)
+    st_p = statistics.mean(e[1].elapsed_time(e[2]) for e in stage_events)
+    st_q = statistics.mean(e[2].elapsed_time(e[3]) for e in stage_events)
+    weights = m * d
+    value = whole_job_value(weights, world, ms_step)
+
+    peaks, peak_src = measured_peaks()
+    h_flops = float(d) * (d + 1) * n
+    h_tflops = h_flops / (st_h / 1e3) / 1e12
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    roofline = {"kernel": "hessian (gptq_hessian_accumulate)", "bound": "tensor",
+                "achieved": round(h_tflops, 3), "peak": peak_t, "unit": "TFLOP/s",
+                "frac": round(h_tflops / peak_t, 4), "traffic": None,
+                "algorithmic": f"d(d+1)N = {h_flops:.4e} flop per launch (lower triangle of "
+                               f"2 X^T X incl. diagonal)",
+                "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"}
+
+    # ---- end to end through the C ABI from host buffers --------------------------------
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+        Xh.copy_(X)
+        Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+        Wh.copy_(W)
+        qh = torch.empty(qp.shape, dtype=qp.dtype, pin_memory=True)
+        sh = torch.empty(sc.shape, dtype=sc.dtype, pin_memory=True)
+        zh = torch.empty(zr.shape, dtype=zr.dtype, pin_memory=True)
+        Xd = torch.empty_like(X)
+        Wd = torch.empty_like(W)
+
+        def e2e_step():
+            Xd.copy_(Xh, non_blocking=True)
+            Wd.copy_(Wh, non_blocking=True)
+            gptq.hessian(Xd, H, accumulate=False, stream=stream)
+            gptq.prepare(H, damp, U=U, dead_mask=dm, ws=ws_p, stream=stream)
+            gptq.quantize(Wd, U, bits, block, dm, ws=ws_q, stream=stream,
+                          out=(qp, sc, zr, None))
+            qh.copy_(qp, non_blocking=True)
+            sh.copy_(sc, non_blocking=True)
+            zh.copy_(zr, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = reduce_max(a.elapsed_time(b) / args.steps, dev)
+        h2d = X.numel() * X.element_size() + W.numel() * W.element_size()
+        d2h = qp.numel() * 4 + sc.numel() * 4 + zr.numel() * 4
+        e2e = {"value": whole_job_value(weights, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del Xh, Xd
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only) ---------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        Xs = X[:2048].float().cpu().numpy()
+        Wn = W.float().cpu().numpy()
+        est, det = oracle_sample(Xs, Wn, layer, bits, block, damp, tok_sample=2048,
+                                 row_sample=64)
+        cpu = {"value": weights / est, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": (f"fp64 NumPy oracle: Hessian over the first {det['tok_sample']} "
+                          f"tokens scaled x{n / det['tok_sample']:.0f}, full prepare at "
+                          f"d_in={d}, sweep of {det['row_sample']} rows scaled "
+                          f"x{m / det['row_sample']:.0f}"),
+               "est_seconds_per_layer": est, "detail": det}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded correlated activations and N(0, 0.02^2) weights)",
+            "config": {"workload": wl.name, "d_out": m, "d_in": d, "n_tok": n, "bits": bits,
+                       "block": block, "damp": damp, "x_dtype": act.dtype,
+                       "w_dtype": layer.w_dtype,
+                       "arith": "fp16 products exact, fp32 accumulation (Hessian); fp32 "
+                                "elsewhere; 3xTF32-split operands for rank-K updates",
+                       "l2": f"inputs exceed L2: X is {X.numel() * X.element_size() / 1e9:.2f}"
+                             f" GB per step",
+                       "parallelism": f"replicas x{world} (independent layers)"},
+            "stages_ms": {"hessian": st_h, "prepare": st_p, "quantize": st_q},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores, each step a bounded sample scaled to the full layer."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from post_weight_quantization_03_gb300 import synthetic as S
+
+    wl = S.WORKLOADS[args.workload]
+    layer = wl.layers[0]
+    bits, block, damp = wl.bits[-1], wl.block, wl.damp
+    m, d, n = layer.d_out, layer.act.d_in, layer.act.n_tok
+    X = S.activations(layer.act, device="cpu", n_tok=2048).float().numpy()
+    W = S.layer_weights(layer).float().numpy()
+    total = args.steps + args.warmup
+    rows = 64 if total <= 15 else 32
+    times = []
+    det = None
+    for i in range(total):
+        est, det = oracle_sample(X, W, layer, bits, block, damp, tok_sample=2048,
+                                 row_sample=rows)
+        if i >= args.warmup:
+            times.append(est)
+    sec = statistics.mean(times)
+    value = m * d / sec
+    sample = (f"fp64 NumPy oracle per step: Hessian over 2048 tokens scaled x{n // 2048}, "
+              f"full prepare at d_in={d}, sweep of {rows} rows scaled x{m // rows}")
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": wl.name, "d_out": m, "d_in": d, "n_tok": n, "bits": bits,
+                      "block": block, "damp": damp},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0},
+           "detail": det}
+    _ = (np, torch)
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

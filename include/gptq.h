@@ -1,0 +1,185 @@
+/*
+ * gptq.h -- C ABI of a GB300 (sm_103a) library for GPTQ's per-layer second-order
+ * weight quantization.
+ *
+ * The operation (three web pages on GPTQ: "GPTQ › Mathematical Details of the Update";
+ * "tm_gptq_math"; "GPTQ Hessian", excerpt of "GPTQ: Block Structure in Quantization"):
+ * for one linear layer with weights W [d_out, d_in] and calibration inputs X, find a
+ * few-bit W_hat whose outputs on X stay close to W's, one row at a time, all rows sharing
+ * the Hessian H = 2 X X^T of the per-row quadratic error.  The path is split into the
+ * three calls below, in the pages' order:
+ *
+ *   gptq_hessian_accumulate   X -> H          ("tm_gptq_math", "Why it is second-order:
+ *                                               the Hessian")
+ *   gptq_prepare              H -> U          ("tm_gptq_math", "The Cholesky trick for the
+ *                                               inverse Hessian"; "GPTQ Hessian")
+ *   gptq_quantize_layer       W, U -> codes   ("tm_gptq_math", "Greedy quantization with
+ *                                               error compensation" and "GPTQ's speedups:
+ *                                               fixed order and lazy batches"; "GPTQ Hessian")
+ *
+ * Conventions shared by every call
+ *   - All matrices are row-major.  X is token-major [n_tok, d_in] (row t = input x_t, so
+ *     the pages' X of shape [d_in, N] is X^T here).  W is [d_out, d_in].
+ *   - Every pointer is a DEVICE pointer on the current CUDA device unless marked "host".
+ *     The library never allocates, frees or keeps device memory beyond a call; the caller
+ *     owns every buffer.  Scratch memory is a caller-supplied workspace whose size the
+ *     *_workspace_bytes functions give; it must be 256-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Kernels are
+ *     enqueued on it; calls return once work is enqueued unless stated otherwise.
+ *   - Argument errors are reported synchronously, before anything is enqueued.  A failed
+ *     kernel launch returns GPTQ_ERR_CUDA.
+ *   - The calls are thread-compatible: concurrent calls must use distinct outputs and
+ *     workspaces.
+ */
+#ifndef GPTQ_GB300_H
+#define GPTQ_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GPTQ_ABI_VERSION 1
+
+typedef struct CUstream_st *gptq_stream_t; /* identical to cudaStream_t */
+
+typedef enum gptq_status {
+  GPTQ_OK = 0,
+  GPTQ_ERR_INVALID_ARG = 1,  /* bad size, dtype, bit width, block, null or misaligned ptr */
+  GPTQ_ERR_NOT_PD = 2,       /* damped Hessian not positive definite (gptq_prepare)       */
+  GPTQ_ERR_NONFINITE = 3,    /* NaN/Inf found in an input                                 */
+  GPTQ_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up                        */
+  GPTQ_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed               */
+  GPTQ_ERR_UNSUPPORTED = 6,  /* valid request this build does not implement               */
+  GPTQ_ERR_WORKSPACE = 7     /* workspace missing, too small or not 256-byte aligned      */
+} gptq_status;
+
+typedef enum gptq_dtype { GPTQ_F16 = 0, GPTQ_BF16 = 1, GPTQ_F32 = 2 } gptq_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gptq_status_str(int status);
+
+/* GPTQ_ABI_VERSION of the loaded library. */
+int gptq_abi_version(void);
+
+/* Number of CUDA kernels this library has launched in this process (all threads). */
+unsigned long long gptq_kernel_launches(void);
+
+/*
+ * gptq_hessian_accumulate: H = (accumulate ? H : 0) + 2 * X^T X.
+ *
+ * Source: "tm_gptq_math", "Why it is second-order: the Hessian" -- the per-row output
+ * error is a quadratic in the row's weights whose constant Hessian is twice the Gram
+ * matrix of the inputs; "GPTQ Hessian" -- every row of the layer shares it.  Calling this
+ * once per token chunk with accumulate=1 after the first accumulates the Hessian of the
+ * whole calibration set while only one chunk of X is resident.
+ *
+ *   X          [n_tok, ldx] elements of type `xdtype`, first d_in columns used; 16-byte
+ *              aligned, ldx * sizeof(elem) a multiple of 16 bytes.
+ *   xdtype     GPTQ_F16 / GPTQ_BF16 (tensor-core path, fp32 accumulation) or GPTQ_F32.
+ *   n_tok      >= 0 tokens (0 leaves H as is, or zero when accumulate=0).
+ *   d_in       >= 1 input channels.
+ *   H          [d_in, d_in] fp32, both triangles written.  With accumulate=1 the lower
+ *              triangle of the existing H is read and the result is written symmetric.
+ * Asynchronous.  Errors: INVALID_ARG, CUDA.
+ */
+gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, int64_t d_in,
+                                    int64_t ldx, float *H, int accumulate,
+                                    gptq_stream_t stream);
+
+/*
+ * gptq_prepare_workspace_bytes: workspace size gptq_prepare needs for this d_in.
+ */
+size_t gptq_prepare_workspace_bytes(int64_t d_in);
+
+/*
+ * gptq_prepare: dead columns, damping and the inverse-Hessian Cholesky factor.
+ *
+ * Source: "tm_gptq_math", "The Cholesky trick for the inverse Hessian" -- channels with a
+ * zero Hessian diagonal are skipped, the diagonal is damped by lambda = damp * mean(diag)
+ * (about 1 %), and one Cholesky factorization of the inverse supplies every row the
+ * fixed-order sweep needs; "GPTQ Hessian" -- U is the upper-triangular factor with
+ * H^-1 = U^T U; "GPTQ › Mathematical Details of the Update" writes it as L = U^T.
+ *
+ * Steps: dead = {i : H_ii == 0}; H_ii = 1 for dead i; lambda = damp * mean(diag H) (after
+ * that fix, over all d_in entries); H += lambda I; U = upper Cholesky factor of H^-1.
+ * U is computed as the inverse of the reversed-order ("UL") Cholesky factor R of H
+ * (H = R R^T, R upper), which is the same matrix.
+ *
+ *   H          [d_in, d_in] fp32 symmetric, CONSUMED: overwritten as scratch.
+ *   d_in       >= 1.
+ *   damp       >= 0 relative damping (0.01 for the pages' 1 %).
+ *   U          [d_in, d_in] fp32 out, upper triangular (lower triangle written as 0).
+ *   dead_mask  [d_in] uint8 out (1 = dead), may be NULL.
+ *   n_dead     HOST int32 out, may be NULL.
+ *   ws         workspace of ws_bytes >= gptq_prepare_workspace_bytes(d_in).
+ * SYNCHRONIZES `stream` before returning.  Errors: INVALID_ARG, WORKSPACE, NOT_PD (a
+ * pivot <= 0: U is then undefined), NONFINITE (NaN/Inf in H), CUDA.
+ */
+gptq_status gptq_prepare(float *H, int64_t d_in, float damp, float *U, uint8_t *dead_mask,
+                         int32_t *n_dead, void *ws, size_t ws_bytes, gptq_stream_t stream);
+
+/*
+ * gptq_quantize_workspace_bytes: workspace size gptq_quantize_layer needs.
+ */
+size_t gptq_quantize_workspace_bytes(int64_t d_out, int64_t d_in, int bits, int block);
+
+/*
+ * gptq_quantize_layer: the GPTQ column sweep of one layer.
+ *
+ * Source: "tm_gptq_math", "Greedy quantization with error compensation" (quantize one
+ * weight, move the still-free weights by the optimal correction), "GPTQ's speedups:
+ * fixed order and lazy batches" (one left-to-right column order for all rows; blocks of
+ * `block` columns, corrections inside the block applied at once, corrections of later
+ * columns deferred to one product per block); "GPTQ Hessian" (row j of U supplies the
+ * correction of column j); "GPTQ › Mathematical Details of the Update" (O(d_in) work per
+ * column once the factor exists).
+ *
+ * Grid (the pages define none; this library's reading): per output row i, asymmetric
+ * min-max over W's row as given, with 0 inside the range:
+ *   x_min = min(0, min_j W_ij), x_max = max(0, max_j W_ij),
+ *   scale_i = (x_max - x_min) / (2^bits - 1)  (1 if that is 0),  zero_i = rint(-x_min/scale_i)
+ * in fp32.  Dead columns (dead_mask) are set to 0 before the sweep.  For each column j in
+ * order, with w the current fp32 working value:
+ *   code = clamp(rint(w / scale) + zero, 0, 2^bits - 1)      (IEEE division, ties to even)
+ *   q = scale * (code - zero);  e = (w - q) / U_jj
+ *   w_k -= e * U_jk for every later column k (inside the block at once, later columns
+ *   through the deferred block product).
+ *
+ *   W          [d_out, ldw] of type `wdtype` (GPTQ_BF16, GPTQ_F16 or GPTQ_F32), not modified.
+ *   d_out      >= 1 rows;  d_in >= 1 columns;  ldw >= d_in.
+ *   U          [d_in, d_in] fp32 upper factor from gptq_prepare (only the upper triangle
+ *              is read).
+ *   dead_mask  [d_in] uint8 (nonzero = dead) or NULL.
+ *   bits       2, 3, 4 or 8.
+ *   block      lazy-batch width B: 1 <= B <= 128 (128 is the pages' value).
+ *   qpacked    [d_out, ceil(d_in/32) * bits] uint32 out: row-wise little-endian
+ *              bitstream, the code of column c in bits [c*bits, (c+1)*bits) of its row
+ *              (bit b of the stream = bit b%32 of word b/32); padding bits are 0.
+ *   scale      [d_out] fp32 out;  zero: [d_out] int32 out.
+ *   W_hat      [d_out, d_in] fp32 out (scale * (code - zero)), or NULL.
+ *   ws         workspace of ws_bytes >= gptq_quantize_workspace_bytes(d_out, d_in, bits,
+ *              block); its contents need no initialisation.
+ * Asynchronous.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.  Non-finite weights
+ * are flagged in the workspace; read the flag with gptq_workspace_status.
+ */
+gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                                int64_t ldw, const float *U, const uint8_t *dead_mask,
+                                int bits, int block, uint32_t *qpacked, float *scale,
+                                int32_t *zero, float *W_hat, void *ws, size_t ws_bytes,
+                                gptq_stream_t stream);
+
+/*
+ * gptq_workspace_status: synchronize `stream`, then return the device-side status the
+ * last gptq_quantize_layer on workspace `ws` recorded (GPTQ_OK, GPTQ_ERR_NONFINITE or
+ * GPTQ_ERR_TIMEOUT).  `ws` must be a workspace that call used.
+ */
+gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_GB300_H */

@@ -1,0 +1,113 @@
+// C ABI entry points: argument validation, workspace sizing, launch sequencing.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace gptq {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static size_t elem_size(int dt) {
+  switch (dt) {
+    case GPTQ_F16:
+    case GPTQ_BF16: return 2;
+    case GPTQ_F32: return 4;
+    default: return 0;
+  }
+}
+
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" {
+
+const char *gptq_status_str(int status) {
+  switch (status) {
+    case GPTQ_OK: return "GPTQ_OK";
+    case GPTQ_ERR_INVALID_ARG: return "GPTQ_ERR_INVALID_ARG";
+    case GPTQ_ERR_NOT_PD: return "GPTQ_ERR_NOT_PD";
+    case GPTQ_ERR_NONFINITE: return "GPTQ_ERR_NONFINITE";
+    case GPTQ_ERR_TIMEOUT: return "GPTQ_ERR_TIMEOUT";
+    case GPTQ_ERR_CUDA: return "GPTQ_ERR_CUDA";
+    case GPTQ_ERR_UNSUPPORTED: return "GPTQ_ERR_UNSUPPORTED";
+    case GPTQ_ERR_WORKSPACE: return "GPTQ_ERR_WORKSPACE";
+    default: return "GPTQ_ERR_UNKNOWN";
+  }
+}
+
+int gptq_abi_version(void) { return GPTQ_ABI_VERSION; }
+
+unsigned long long gptq_kernel_launches(void) { return g_launches.load(); }
+
+gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, int64_t d_in,
+                                    int64_t ldx, float *H, int accumulate,
+                                    gptq_stream_t stream) {
+  const size_t es = elem_size(xdtype);
+  if (es == 0 || n_tok < 0 || d_in < 1 || ldx < d_in || !H) return GPTQ_ERR_INVALID_ARG;
+  if (n_tok > 0 && (!X || !aligned(X, 16) || (ldx * (int64_t)es) % 16 != 0))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(H, 16)) return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 20) return GPTQ_ERR_UNSUPPORTED;
+  return launch_hessian(X, xdtype, n_tok, d_in, ldx, H, accumulate ? 1 : 0,
+                        (cudaStream_t)stream);
+}
+
+size_t gptq_prepare_workspace_bytes(int64_t d_in) {
+  if (d_in < 1) return 0;
+  return prepare_ws_bytes(d_in);
+}
+
+gptq_status gptq_prepare(float *H, int64_t d_in, float damp, float *U, uint8_t *dead_mask,
+                         int32_t *n_dead, void *ws, size_t ws_bytes, gptq_stream_t stream) {
+  if (!H || !U || d_in < 1 || !(damp >= 0.0f) || !aligned(H, 16) || !aligned(U, 16))
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 17) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < prepare_ws_bytes(d_in)) return GPTQ_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  GPTQ_TRY(launch_prepare(H, d_in, damp, U, dead_mask, ws, s));
+  DevStatus st;
+  GPTQ_CUDA_CHECK(cudaMemcpyAsync(&st, ws, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  GPTQ_CUDA_CHECK(cudaStreamSynchronize(s));
+  if (n_dead) *n_dead = st.n_dead;
+  return (gptq_status)st.status;
+}
+
+size_t gptq_quantize_workspace_bytes(int64_t d_out, int64_t d_in, int bits, int block) {
+  if (d_out < 1 || d_in < 1) return 0;
+  return quantize_ws_bytes(d_out, d_in, bits, block);
+}
+
+gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                                int64_t ldw, const float *U, const uint8_t *dead_mask,
+                                int bits, int block, uint32_t *qpacked, float *scale,
+                                int32_t *zero, float *W_hat, void *ws, size_t ws_bytes,
+                                gptq_stream_t stream) {
+  const size_t es = elem_size(wdtype);
+  if (es == 0 || !W || !U || !qpacked || !scale || !zero) return GPTQ_ERR_INVALID_ARG;
+  if (d_out < 1 || d_in < 1 || ldw < d_in) return GPTQ_ERR_INVALID_ARG;
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
+  if (block < 1 || block > 128) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, es) || !aligned(U, 16) || !aligned(qpacked, 4) || !aligned(scale, 4) ||
+      !aligned(zero, 4) || (W_hat && !aligned(W_hat, 4)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 17 || d_out > (int64_t)1 << 24) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < quantize_ws_bytes(d_out, d_in, bits, block))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_quantize(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
+                         scale, zero, W_hat, ws, (cudaStream_t)stream);
+}
+
+gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {
+  if (!ws || !aligned(ws, 256)) return GPTQ_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  DevStatus st;
+  GPTQ_CUDA_CHECK(cudaMemcpyAsync(&st, ws, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  GPTQ_CUDA_CHECK(cudaStreamSynchronize(s));
+  return (gptq_status)st.status;
+}
+
+}  // extern "C"

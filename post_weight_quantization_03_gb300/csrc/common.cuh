@@ -1,0 +1,113 @@
+// Internal definitions shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/gptq.h"
+
+namespace gptq {
+
+// ----------------------------------------------------------------------------------------
+// Host-side bookkeeping
+// ----------------------------------------------------------------------------------------
+
+// Counts every kernel this library launches (reported by gptq_kernel_launches()).
+void count_launch(unsigned n = 1);
+
+#define GPTQ_LAUNCH_CHECK()                                   \
+  do {                                                        \
+    ::gptq::count_launch();                                   \
+    if (cudaPeekAtLastError() != cudaSuccess) {               \
+      (void)cudaGetLastError();                               \
+      return GPTQ_ERR_CUDA;                                   \
+    }                                                         \
+  } while (0)
+
+#define GPTQ_CUDA_CHECK(call)                                 \
+  do {                                                        \
+    if ((call) != cudaSuccess) {                              \
+      (void)cudaGetLastError();                               \
+      return GPTQ_ERR_CUDA;                                   \
+    }                                                         \
+  } while (0)
+
+#define GPTQ_TRY(expr)                                        \
+  do {                                                        \
+    gptq_status _s = (expr);                                  \
+    if (_s != GPTQ_OK) return _s;                             \
+  } while (0)
+
+static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Device-side status block at the start of every workspace.
+struct DevStatus {
+  int status;        // gptq_status recorded by kernels (0 = OK); first writer wins
+  int info;          // NOT_PD: first failing pivot (global index) + 1
+  int n_dead;        // number of dead columns
+  int pad0;
+  double lam;        // damping actually added
+  double diag_sum;   // sum of the (dead-fixed) diagonal
+  unsigned long long pad[4];
+};
+static_assert(sizeof(DevStatus) <= 256, "status block must fit in 256 bytes");
+
+// Records `code` unless a status is already recorded.
+__device__ __forceinline__ void set_status(DevStatus *st, int code) {
+  atomicCAS(&st->status, 0, code);
+}
+
+// ----------------------------------------------------------------------------------------
+// Element loads
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Splits x into a TF32-representable head (low 13 mantissa bits cleared) and the exact
+// remainder x - head, so that head*y_head + head*y_tail + tail*y_head reproduces a fp32
+// product to about 2^-21 relative on a TF32 tensor core (the "3xTF32" scheme).
+__device__ __forceinline__ float tf32_head(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// ----------------------------------------------------------------------------------------
+// Kernel launchers implemented in the .cu files (all enqueue on `s`, return a status)
+// ----------------------------------------------------------------------------------------
+
+// hessian.cu
+gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
+                           float *H, int accumulate, cudaStream_t s);
+
+// gemm.cu: C[m, n] (+)= alpha * sum_k A[m, k] * B[n, k], operands given as a TF32 head
+// and tail pair each (tail may be null = 0).  lower_only skips tiles strictly above the
+// diagonal of C (C square, row/col offsets equal).  trans_c stores C(m, n) at
+// C[n * ldc + m].
+struct GemmArgs {
+  const float *a_hi, *a_lo; int64_t lda;
+  const float *b_hi, *b_lo; int64_t ldb;
+  float *c; int64_t ldc;
+  int64_t M, N, K;
+  float alpha;
+  int lower_only;
+  int trans_c;
+};
+gptq_status launch_gemm_nt(const GemmArgs &g, const DevStatus *st, cudaStream_t s);
+
+// factor.cu
+gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
+                           void *ws, cudaStream_t s);
+size_t prepare_ws_bytes(int64_t d);
+
+// quantize.cu
+gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                            const float *U, const uint8_t *dead_mask, int bits, int block,
+                            uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                            void *ws, cudaStream_t s);
+size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block);
+
+}  // namespace gptq

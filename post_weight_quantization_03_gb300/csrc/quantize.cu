@@ -1,0 +1,336 @@
+// Steps 4 and 5 of the path: the GPTQ column sweep of one layer ("tm_gptq_math",
+// "Greedy quantization with error compensation" and "GPTQ's speedups: fixed order and
+// lazy batches"; "GPTQ Hessian", "GPTQ: Block Structure in Quantization").
+//
+// Per block of B columns [b0, b1):
+//   sweep    : every row (one thread each, the row's B working weights in registers)
+//              quantizes columns b0..b1-1 in order, spreading each column's scaled error
+//              e_j = (w_j - q_j) / U_jj along row j of U inside the block at once;
+//              writes the codes and E = [e_b0 .. e_b1-1] (as a TF32 head/tail pair)
+//   trailing : W[:, b1:] -= E U[b0:b1, b1:]   (the deferred lazy-batch product, run as
+//              C -= A B^T with B = U^T rows, i.e. Lt = U^T split into head/tail)
+// then one pass packs the codes and writes W_hat.
+#include "common.cuh"
+
+namespace gptq {
+
+namespace {
+
+constexpr int SB = 128;          // maximum block width held by one thread
+constexpr int SW_ROWS = 64;      // rows (threads) per sweep CTA
+constexpr int LDU = SB + 4;      // smem leading dimension of the U block
+constexpr int LDW = SB + 1;      // smem leading dimension of the staging tile
+
+// ---------------------------------------------------------------------------------------
+// Grid: per-row asymmetric min-max with 0 in the range; fp32 working copy of W with dead
+// columns zeroed.  One warp per row.
+// ---------------------------------------------------------------------------------------
+template <typename T>
+__global__ void grid_kernel(const T *__restrict__ W, int64_t m, int64_t d, int64_t ldw,
+                            const uint8_t *__restrict__ dead, float maxq,
+                            float *__restrict__ scale, int32_t *__restrict__ zero,
+                            float *__restrict__ Wf, int64_t ldwf, DevStatus *st) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= m) return;
+  const T *w = W + row * ldw;
+  float lo = 0.f, hi = 0.f;
+  int bad = 0;
+  for (int64_t j = lane; j < d; j += 32) {
+    const float v = to_f32(w[j]);
+    bad |= !isfinite(v);
+    lo = fminf(lo, v);
+    hi = fmaxf(hi, v);
+  }
+  for (int o = 16; o; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+  }
+  const float width = __fsub_rn(hi, lo);
+  const float s = (width == 0.0f) ? 1.0f : __fdiv_rn(width, maxq);
+  const float z = rintf(__fdiv_rn(-lo, s));
+  if (lane == 0) {
+    scale[row] = s;
+    zero[row] = (int32_t)z;
+    if (bad) set_status(st, GPTQ_ERR_NONFINITE);
+  }
+  float *wf = Wf + row * ldwf;
+  for (int64_t j = lane; j < d; j += 32) wf[j] = (dead && dead[j]) ? 0.0f : to_f32(w[j]);
+}
+
+// ---------------------------------------------------------------------------------------
+// Lt = U^T (lower part only: Lt[i][j] = U[j][i], j <= i) as a TF32 head/tail pair.
+// ---------------------------------------------------------------------------------------
+__global__ void lt_split_kernel(const float *__restrict__ U, int64_t d, float *__restrict__ hi,
+                                float *__restrict__ lo, int64_t ld) {
+  __shared__ float tile[32][33];
+  const int64_t bi = blockIdx.y, bj = blockIdx.x;  // Lt tile (rows bi, cols bj)
+  if (bi < bj) return;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  // Lt[bi*32 + r][bj*32 + c] = U[bj*32 + c][bi*32 + r]: read U rows bj*32+yy, cols bi*32+tx
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int64_t ur = bj * 32 + yy, uc = bi * 32 + tx;
+    tile[yy][tx] = (ur < d && uc < d && ur <= uc) ? U[ur * d + uc] : 0.0f;
+  }
+  __syncthreads();
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int64_t r = bi * 32 + yy, c = bj * 32 + tx;
+    if (r < d && c < d) {
+      const float v = tile[tx][yy];
+      const float h = tf32_head(v);
+      hi[r * ld + c] = h;
+      lo[r * ld + c] = v - h;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// One column step of the in-block sweep, unrolled at compile time over the block so the
+// row's working weights stay in registers:
+//   code = clamp(rint(w_J / s) + z, 0, maxq);  q = s (code - z);  e = (w_J - q) / U_JJ
+//   w_k -= e U_Jk  for k > J inside the block.
+// ---------------------------------------------------------------------------------------
+template <int J>
+struct SweepStep {
+  static __device__ __forceinline__ void run(float (&w)[SB], uint32_t (&cw)[SB / 4],
+                                             const float *Us, const float *rdiag, float s,
+                                             float z, float maxq) {
+    const float x = __fdiv_rn(w[J], s);
+    const float c = fminf(fmaxf(rintf(x) + z, 0.0f), maxq);
+    const float q = s * (c - z);
+    const float e = (w[J] - q) * rdiag[J];
+    cw[J / 4] |= (uint32_t)c << (8 * (J % 4));
+    w[J] = e;  // the register now holds the scaled error of column J
+#pragma unroll
+    for (int k = J + 1; k < SB; ++k) w[k] = fmaf(-e, Us[J * LDU + k], w[k]);
+    SweepStep<J + 1>::run(w, cw, Us, rdiag, s, z, maxq);
+  }
+};
+template <>
+struct SweepStep<SB> {
+  static __device__ __forceinline__ void run(float (&)[SB], uint32_t (&)[SB / 4],
+                                             const float *, const float *, float, float,
+                                             float) {}
+};
+
+// ---------------------------------------------------------------------------------------
+// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(SW_ROWS)
+sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, int nb,
+             const float *__restrict__ U, int64_t d, const float *__restrict__ scale,
+             const int32_t *__restrict__ zero, float maxq, float *__restrict__ Ehi,
+             float *__restrict__ Elo, uint8_t *__restrict__ codes, int64_t ldc,
+             const DevStatus *st) {
+  extern __shared__ float sm[];
+  float *Us = sm;                       // SB x LDU, upper part of U's diagonal block
+  float *stage = sm + SB * LDU;         // SW_ROWS x LDW
+  float *rdiag = stage + SW_ROWS * LDW; // SB reciprocals of U_jj
+  const int tid = threadIdx.x;
+  const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
+  // U block (upper triangle only); padding columns get U_jj = 1 and no coupling
+  for (int e = tid; e < SB * SB; e += blockDim.x) {
+    const int i = e / SB, j = e % SB;
+    float v = 0.f;
+    if (i < nb && j < nb) {
+      if (i <= j) v = U[(b0 + i) * d + (b0 + j)];
+    } else if (i == j) {
+      v = 1.f;
+    }
+    Us[i * LDU + j] = v;
+  }
+  // working weights, coalesced
+  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
+    const int r = e / SB, j = e % SB;
+    const int64_t gr = r0 + r;
+    stage[r * LDW + j] = (gr < m && j < nb) ? Wf[gr * ldwf + b0 + j] : 0.f;
+  }
+  __syncthreads();
+  for (int j = tid; j < SB; j += blockDim.x) rdiag[j] = 1.0f / Us[j * LDU + j];
+  __syncthreads();
+  const int64_t row = r0 + tid;
+  const float s = row < m ? scale[row] : 1.f;
+  const float z = row < m ? (float)zero[row] : 0.f;
+  float w[SB];
+#pragma unroll
+  for (int j = 0; j < SB; ++j) w[j] = stage[tid * LDW + j];
+  uint32_t cw[SB / 4];  // codes, 4 per word (byte j%4 of word j/4)
+#pragma unroll
+  for (int i = 0; i < SB / 4; ++i) cw[i] = 0u;
+  SweepStep<0>::run(w, cw, Us, rdiag, s, z, maxq);
+  // stage E, then store coalesced as a head/tail pair
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < SB; ++j) stage[tid * LDW + j] = (j < nb) ? w[j] : 0.f;
+  __syncthreads();
+  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
+    const int r = e / SB, j = e % SB;
+    const int64_t gr = r0 + r;
+    if (gr < m) {
+      const float v = stage[r * LDW + j];
+      const float h = tf32_head(v);
+      Ehi[gr * SB + j] = h;
+      Elo[gr * SB + j] = v - h;
+    }
+  }
+  __syncthreads();
+  // codes: stage as bytes, store coalesced
+  uint32_t *cstage = (uint32_t *)stage;  // SW_ROWS x (SB/4 + 1) words
+#pragma unroll
+  for (int i = 0; i < SB / 4; ++i) cstage[tid * (SB / 4 + 1) + i] = cw[i];
+  __syncthreads();
+  const uint8_t *cb = (const uint8_t *)cstage;
+  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
+    const int r = e / SB, j = e % SB;
+    const int64_t gr = r0 + r;
+    if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
+  }
+  (void)st;
+}
+
+// ---------------------------------------------------------------------------------------
+// Pack codes into the row bitstream; write W_hat = scale * (code - zero).
+// One thread per output word.
+// ---------------------------------------------------------------------------------------
+__global__ void pack_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m,
+                            int64_t d, int bits, int64_t words, uint32_t *__restrict__ qp) {
+  const int64_t total = m * words;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = idx / words, wi = idx % words;
+    const int64_t bit0 = wi * 32;
+    const int64_t c0 = bit0 / bits, c1 = (bit0 + 31) / bits;
+    uint32_t v = 0;
+    for (int64_t c = c0; c <= c1 && c < d; ++c) {
+      const uint32_t code = codes[row * ldc + c];
+      const int64_t sh = c * bits - bit0;
+      if (sh >= 0)
+        v |= (sh < 32) ? (code << sh) : 0u;
+      else
+        v |= code >> (-sh);
+    }
+    qp[idx] = v;
+  }
+}
+
+__global__ void dequant_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m,
+                               int64_t d, const float *__restrict__ scale,
+                               const int32_t *__restrict__ zero, float *__restrict__ Wh) {
+  const int64_t total = m * d;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = idx / d, c = idx % d;
+    Wh[idx] = scale[row] * ((float)codes[row * ldc + c] - (float)zero[row]);
+  }
+}
+
+struct QuantWs {
+  DevStatus *st;
+  float *Wf; int64_t ldwf;
+  float *Ehi, *Elo;
+  float *Lhi, *Llo; int64_t ldl;
+  uint8_t *codes; int64_t ldc;
+};
+
+QuantWs carve_quantize(void *ws, int64_t m, int64_t d) {
+  QuantWs q;
+  char *p = (char *)ws;
+  q.st = (DevStatus *)p; p += 256;
+  q.ldwf = (int64_t)round_up((size_t)d, 4);
+  q.Wf = (float *)p; p += round_up((size_t)m * q.ldwf * 4, 256);
+  q.Ehi = (float *)p; p += round_up((size_t)m * SB * 4, 256);
+  q.Elo = (float *)p; p += round_up((size_t)m * SB * 4, 256);
+  q.ldl = (int64_t)round_up((size_t)d, 4);
+  q.Lhi = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
+  q.Llo = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
+  q.ldc = (int64_t)round_up((size_t)d, 16);
+  q.codes = (uint8_t *)p;
+  return q;
+}
+
+}  // namespace
+
+size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
+  (void)bits; (void)block;
+  const size_t ldwf = round_up((size_t)d, 4), ldl = round_up((size_t)d, 4);
+  const size_t ldc = round_up((size_t)d, 16);
+  return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * SB * 4, 256) +
+         2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256);
+}
+
+gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                            const float *U, const uint8_t *dead_mask, int bits, int block,
+                            uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                            void *ws, cudaStream_t s) {
+  static bool attr_done = false;
+  const size_t sweep_smem = (SB * LDU + SW_ROWS * LDW + SB) * sizeof(float);
+  if (!attr_done) {
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sweep_smem));
+    attr_done = true;
+  }
+  QuantWs q = carve_quantize(ws, m, d);
+  const float maxq = (float)((1 << bits) - 1);
+  GPTQ_CUDA_CHECK(cudaMemsetAsync(q.st, 0, sizeof(DevStatus), s));
+  {
+    const int warps = 8;
+    const unsigned g = (unsigned)ceil_div(m, warps);
+    switch (wdtype) {
+      case GPTQ_F32:
+        grid_kernel<float><<<g, warps * 32, 0, s>>>((const float *)W, m, d, ldw, dead_mask,
+                                                    maxq, scale, zero, q.Wf, q.ldwf, q.st);
+        break;
+      case GPTQ_F16:
+        grid_kernel<__half><<<g, warps * 32, 0, s>>>((const __half *)W, m, d, ldw, dead_mask,
+                                                     maxq, scale, zero, q.Wf, q.ldwf, q.st);
+        break;
+      case GPTQ_BF16:
+        grid_kernel<__nv_bfloat16><<<g, warps * 32, 0, s>>>(
+            (const __nv_bfloat16 *)W, m, d, ldw, dead_mask, maxq, scale, zero, q.Wf, q.ldwf,
+            q.st);
+        break;
+      default:
+        return GPTQ_ERR_INVALID_ARG;
+    }
+    GPTQ_LAUNCH_CHECK();
+  }
+  {
+    dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
+    lt_split_kernel<<<tg, dim3(32, 8), 0, s>>>(U, d, q.Lhi, q.Llo, q.ldl);
+    GPTQ_LAUNCH_CHECK();
+  }
+  const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
+  for (int64_t b0 = 0; b0 < d; b0 += block) {
+    const int nb = (int)((d - b0) < block ? (d - b0) : block);
+    const int64_t b1 = b0 + nb;
+    sweep_kernel<<<sweep_grid, SW_ROWS, sweep_smem, s>>>(q.Wf, q.ldwf, m, b0, nb, U, d, scale,
+                                                         zero, maxq, q.Ehi, q.Elo, q.codes,
+                                                         q.ldc, q.st);
+    GPTQ_LAUNCH_CHECK();
+    if (b1 < d) {
+      GemmArgs g{};
+      g.a_hi = q.Ehi; g.a_lo = q.Elo; g.lda = SB;
+      g.b_hi = q.Lhi + b1 * q.ldl + b0; g.b_lo = q.Llo + b1 * q.ldl + b0; g.ldb = q.ldl;
+      g.c = q.Wf + b1; g.ldc = q.ldwf;
+      g.M = m; g.N = d - b1; g.K = nb;
+      g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0;
+      GPTQ_TRY(launch_gemm_nt(g, nullptr, s));
+    }
+  }
+  {
+    const int64_t words = ceil_div(d, 32) * bits;
+    pack_kernel<<<2048, 256, 0, s>>>(q.codes, q.ldc, m, d, bits, words, qpacked);
+    GPTQ_LAUNCH_CHECK();
+    if (W_hat) {
+      dequant_kernel<<<2048, 256, 0, s>>>(q.codes, q.ldc, m, d, scale, zero, W_hat);
+      GPTQ_LAUNCH_CHECK();
+    }
+  }
+  return GPTQ_OK;
+}
+
+size_t quantize_status_offset() { return 0; }
+
+}  // namespace gptq

@@ -1,0 +1,229 @@
+"""Thin Python binding of ``libgptq.so`` (argument marshalling only).
+
+The functions named like the C entry points (``gptq_hessian_accumulate``, ``gptq_prepare``,
+``gptq_quantize_layer``, ...) take raw device pointers, sizes and a stream handle exactly as
+the C ABI does.  The tensor helpers below them (``hessian``, ``prepare``, ``quantize``) only
+allocate outputs/workspaces with torch, pass pointers, and raise on a non-OK status: every
+step of the computation runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import build_lib
+
+GPTQ_OK = 0
+STATUS_NAMES = {
+    0: "GPTQ_OK", 1: "GPTQ_ERR_INVALID_ARG", 2: "GPTQ_ERR_NOT_PD", 3: "GPTQ_ERR_NONFINITE",
+    4: "GPTQ_ERR_TIMEOUT", 5: "GPTQ_ERR_CUDA", 6: "GPTQ_ERR_UNSUPPORTED", 7: "GPTQ_ERR_WORKSPACE",
+}
+DTYPES = {"f16": 0, "bf16": 1, "f32": 2}
+
+_c = ctypes
+_SIGS = {
+    "gptq_status_str": (_c.c_char_p, [_c.c_int]),
+    "gptq_abi_version": (_c.c_int, []),
+    "gptq_kernel_launches": (_c.c_ulonglong, []),
+    "gptq_hessian_accumulate": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+                                           _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
+    "gptq_prepare_workspace_bytes": (_c.c_size_t, [_c.c_int64]),
+    "gptq_prepare": (_c.c_int, [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_void_p, _c.c_void_p,
+                                _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "gptq_quantize_workspace_bytes": (_c.c_size_t, [_c.c_int64, _c.c_int64, _c.c_int, _c.c_int]),
+    "gptq_quantize_layer": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+                                       _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_int,
+                                       _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                       _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "gptq_workspace_status": (_c.c_int, [_c.c_void_p, _c.c_void_p]),
+}
+
+_lib = None
+
+
+class GptqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def library_path() -> str:
+    return build_lib.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it is missing: build it with
+    ``python -m post_weight_quantization_03_gb300.build_lib``."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: the CUDA library must be built (build_lib.build())")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def declared_symbols(header: str | None = None):
+    """Names of the functions ``include/gptq.h`` declares."""
+    header = header or os.path.join(build_lib.INCLUDE, "gptq.h")
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gptq_[a-z_0-9]+)\s*\(", text)))
+
+
+# ---------------------------------------------------------------------------------------
+# C entry points, same names and arguments
+# ---------------------------------------------------------------------------------------
+
+def gptq_status_str(status):
+    return load().gptq_status_str(status).decode()
+
+
+def gptq_abi_version():
+    return load().gptq_abi_version()
+
+
+def gptq_kernel_launches():
+    return load().gptq_kernel_launches()
+
+
+def gptq_hessian_accumulate(X, xdtype, n_tok, d_in, ldx, H, accumulate, stream):
+    return load().gptq_hessian_accumulate(X, xdtype, n_tok, d_in, ldx, H, accumulate, stream)
+
+
+def gptq_prepare_workspace_bytes(d_in):
+    return load().gptq_prepare_workspace_bytes(d_in)
+
+
+def gptq_prepare(H, d_in, damp, U, dead_mask, n_dead, ws, ws_bytes, stream):
+    return load().gptq_prepare(H, d_in, damp, U, dead_mask, n_dead, ws, ws_bytes, stream)
+
+
+def gptq_quantize_workspace_bytes(d_out, d_in, bits, block):
+    return load().gptq_quantize_workspace_bytes(d_out, d_in, bits, block)
+
+
+def gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
+                        scale, zero, W_hat, ws, ws_bytes, stream):
+    return load().gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
+                                      qpacked, scale, zero, W_hat, ws, ws_bytes, stream)
+
+
+def gptq_workspace_status(ws, stream):
+    return load().gptq_workspace_status(ws, stream)
+
+
+# ---------------------------------------------------------------------------------------
+# torch-tensor helpers (marshalling only)
+# ---------------------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    m = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, where):
+    if status != GPTQ_OK:
+        raise GptqError(status, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def workspace(nbytes, device):
+    """A 256-byte aligned byte workspace (torch allocations are 256-byte aligned)."""
+    torch = _torch()
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+def hessian(X, H=None, accumulate=False, stream=None):
+    """``H (+)= 2 X^T X`` for token-major X ``[n_tok, d_in]`` (row stride X.stride(0))."""
+    torch = _torch()
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be a row-major [n_tok, d_in] matrix")
+    n, d = X.shape
+    if H is None:
+        H = torch.empty(d, d, dtype=torch.float32, device=X.device)
+        accumulate = False
+    _check(gptq_hessian_accumulate(_ptr(X), _dtype_code(X), n, d, X.stride(0), _ptr(H),
+                                   1 if accumulate else 0, _stream(stream)),
+           "gptq_hessian_accumulate")
+    return H
+
+
+def prepare(H, damp=0.01, U=None, dead_mask=None, ws=None, stream=None):
+    """Dead columns + damping + ``U`` with ``U^T U = H_damped^-1``.  CONSUMES ``H``.
+
+    Returns ``(U, dead_mask, n_dead)``.
+    """
+    torch = _torch()
+    d = H.shape[0]
+    if H.dtype != torch.float32 or not H.is_contiguous() or H.shape != (d, d):
+        raise ValueError("H must be a contiguous float32 [d, d] matrix")
+    if U is None:
+        U = torch.empty(d, d, dtype=torch.float32, device=H.device)
+    if dead_mask is None:
+        dead_mask = torch.empty(d, dtype=torch.uint8, device=H.device)
+    nbytes = gptq_prepare_workspace_bytes(d)
+    if ws is None:
+        ws = workspace(nbytes, H.device)
+    n_dead = ctypes.c_int32(0)
+    _check(gptq_prepare(_ptr(H), d, float(damp), _ptr(U), _ptr(dead_mask),
+                        ctypes.byref(n_dead), _ptr(ws), ws.numel(), _stream(stream)),
+           "gptq_prepare")
+    return U, dead_mask, n_dead.value
+
+
+def packed_words(d_in, bits):
+    return ((d_in + 31) // 32) * bits
+
+
+def quantize(W, U, bits=4, block=128, dead_mask=None, want_w_hat=True, ws=None, stream=None,
+             out=None):
+    """The GPTQ sweep of one layer.  Returns ``(qpacked, scale, zero, W_hat or None)``."""
+    torch = _torch()
+    if W.dim() != 2 or W.stride(1) != 1:
+        raise ValueError("W must be a row-major [d_out, d_in] matrix")
+    m, d = W.shape
+    dev = W.device
+    if out is None:
+        qpacked = torch.empty(m, packed_words(d, bits), dtype=torch.int32, device=dev)
+        scale = torch.empty(m, dtype=torch.float32, device=dev)
+        zero = torch.empty(m, dtype=torch.int32, device=dev)
+        W_hat = torch.empty(m, d, dtype=torch.float32, device=dev) if want_w_hat else None
+    else:
+        qpacked, scale, zero, W_hat = out
+    if ws is None:
+        ws = workspace(gptq_quantize_workspace_bytes(m, d, bits, block), dev)
+    _check(gptq_quantize_layer(_ptr(W), _dtype_code(W), m, d, W.stride(0), _ptr(U),
+                               _ptr(dead_mask), bits, block, _ptr(qpacked), _ptr(scale),
+                               _ptr(zero), _ptr(W_hat), _ptr(ws), ws.numel(), _stream(stream)),
+           "gptq_quantize_layer")
+    return qpacked, scale, zero, W_hat

@@ -1,0 +1,82 @@
+"""The C-ABI library builds, loads and exports every symbol include/gptq.h declares.
+
+No compute call runs here: only calls whose arguments fail validation, which the
+library rejects synchronously before touching the GPU.
+"""
+
+import ctypes
+
+import pytest
+
+from post_weight_quantization_03_gb300 import build_lib, gptq
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return gptq.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = gptq.declared_symbols()
+    assert {"gptq_hessian_accumulate", "gptq_prepare", "gptq_quantize_layer"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in gptq._SIGS, f"binding lacks a signature for {n}"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in gptq.STATUS_NAMES.items():
+        assert gptq.gptq_status_str(code) == name
+    assert gptq.gptq_status_str(99) == "GPTQ_ERR_UNKNOWN"
+    assert gptq.gptq_abi_version() == 1
+    assert gptq.gptq_kernel_launches() >= 0
+
+
+def test_workspace_sizes(lib):
+    assert gptq.gptq_prepare_workspace_bytes(0) == 0
+    assert gptq.gptq_prepare_workspace_bytes(4096) >= 4096 * 4096 * 4
+    q = gptq.gptq_quantize_workspace_bytes(4096, 4096, 4, 128)
+    assert q >= 4096 * 4096 * 4 * 3  # fp32 working copy + split U^T
+    assert gptq.gptq_quantize_workspace_bytes(0, 10, 4, 128) == 0
+
+
+P = ctypes.c_void_p
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    fake = P(256 * 1024)  # never dereferenced: validation fails first
+    INV, WS = 1, 7
+    # bad dtype, negative tokens, ldx < d_in, null H
+    assert gptq.gptq_hessian_accumulate(fake, 9, 10, 8, 8, fake, 0, None) == INV
+    assert gptq.gptq_hessian_accumulate(fake, 0, -1, 8, 8, fake, 0, None) == INV
+    assert gptq.gptq_hessian_accumulate(fake, 0, 10, 8, 4, fake, 0, None) == INV
+    assert gptq.gptq_hessian_accumulate(fake, 0, 10, 8, 8, None, 0, None) == INV
+    # misaligned X row stride (f16, ldx = 9 -> 18 bytes)
+    assert gptq.gptq_hessian_accumulate(fake, 0, 10, 8, 9, fake, 0, None) == INV
+    # prepare: negative damp, missing or short workspace
+    assert gptq.gptq_prepare(fake, 8, -1.0, fake, None, None, fake, 1 << 20, None) == INV
+    assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, None, 0, None) == WS
+    assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, fake, 16, None) == WS
+    assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, P(256 * 1024 + 8), 1 << 30,
+                             None) == WS
+    # quantize: bits, block, shapes, workspace
+    args = dict(W=fake, wdtype=1, d_out=4, d_in=8, ldw=8, U=fake, dead_mask=None, bits=4,
+                block=128, qpacked=fake, scale=fake, zero=fake, W_hat=None, ws=fake,
+                ws_bytes=1 << 30, stream=None)
+
+    def q(**kw):
+        a = dict(args)
+        a.update(kw)
+        return gptq.gptq_quantize_layer(*a.values())
+
+    assert q(bits=5) == INV
+    assert q(bits=1) == INV
+    assert q(block=0) == INV
+    assert q(block=129) == INV
+    assert q(ldw=7) == INV
+    assert q(d_out=0) == INV
+    assert q(wdtype=7) == INV
+    assert q(qpacked=None) == INV
+    assert q(ws=None) == WS
+    assert q(ws_bytes=10) == WS

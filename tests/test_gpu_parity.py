@@ -1,0 +1,213 @@
+"""GPU parity: every step of the CUDA path against the fp64 oracle, through the C ABI.
+
+Each stage gets identical inputs on both sides.  Inputs come from the seeded generators
+or from the oracle itself (e.g. the prepare stage takes the oracle's Hessian rounded to
+fp32; the quantize stage takes the oracle's U rounded to fp32); no oracle input is ever
+produced by the CUDA path.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gptq_oracle as O
+from post_weight_quantization_03_gb300 import build_lib, gptq
+from post_weight_quantization_03_gb300 import synthetic as S
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build_lib.build()
+    gptq.load()
+    torch.cuda.init()
+
+
+def _x(spec, n_tok=None):
+    X = S.activations(spec, device="cpu", n_tok=n_tok)
+    return X
+
+
+def _codes(qpacked, bits, d):
+    return O.unpack_codes(qpacked.cpu().numpy().view(np.uint32), bits, d)
+
+
+# ---------------------------------------------------------------------------------------
+# Step 1: Hessian
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,n,dtype,dead,outl", [
+    (256, 512, "f32", 0, 0),        # the 256 x 256, 512-token fp32 layer
+    (300, 777, "f16", 3, 2),        # ragged channels and tokens
+    (512, 2048, "bf16", 5, 4),
+    (1024, 4096, "f16", 10, 8),
+    (130, 64, "f16", 0, 0),
+])
+def test_hessian_parity(d, n, dtype, dead, outl):
+    spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=dead, n_outlier=outl, seed=d + n)
+    X = _x(spec)
+    Hg = gptq.hessian(X.to(DEV))
+    torch.cuda.synchronize()
+    Hr = O.hessian(X.float().numpy() if dtype != "f32" else X.numpy())
+    Hg = Hg.cpu().numpy()
+    assert PT.rel_fro(Hg, Hr) <= PT.TOL_H
+    assert np.array_equal(Hg, Hg.T)
+
+
+def test_hessian_accumulates_over_chunks():
+    spec = S.ActivationSpec(d_in=384, n_tok=6144, dtype="f16", n_dead=2, seed=77)
+    X = _x(spec).to(DEV)
+    H = gptq.hessian(X[:2048])
+    gptq.hessian(X[2048:4096], H, accumulate=True)
+    gptq.hessian(X[4096:], H, accumulate=True)
+    Hr = O.hessian(X.cpu().float().numpy())
+    assert PT.rel_fro(H.cpu().numpy(), Hr) <= PT.TOL_H
+
+
+def test_hessian_zero_tokens():
+    H = torch.full((40, 40), 3.0, device=DEV)
+    X = torch.empty(0, 40, dtype=torch.float16, device=DEV)
+    gptq.hessian(X, H, accumulate=True)
+    assert torch.all(H == 3.0)
+    gptq.hessian(X, H, accumulate=False)
+    assert torch.all(H == 0.0)
+
+
+# ---------------------------------------------------------------------------------------
+# Steps 2-3: dead columns, damping, U
+# ---------------------------------------------------------------------------------------
+
+def _oracle_h(d, n, dead, outl, seed, dtype="f16", relu=False):
+    spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=dead, n_outlier=outl,
+                            relu_t4=relu, seed=seed)
+    X = _x(spec).float().numpy()
+    return O.hessian(X)
+
+
+@pytest.mark.parametrize("d,n,dead,outl", [(256, 512, 0, 0), (300, 900, 3, 2),
+                                           (777, 3000, 7, 4), (1024, 4096, 10, 8)])
+def test_prepare_parity(d, n, dead, outl):
+    H64 = _oracle_h(d, n, dead, outl, seed=d)
+    H32 = H64.astype(np.float32)
+    Hd, dmask, lam = O.damp_hessian(H32.astype(np.float64))
+    Ur = O.inverse_cholesky_upper(Hd)
+    Hg = torch.from_numpy(H32).to(DEV)
+    U, mask, n_dead = gptq.prepare(Hg, 0.01)
+    U = U.cpu().numpy()
+    assert n_dead == dead
+    assert np.array_equal(mask.cpu().numpy().astype(bool), dmask)
+    assert np.all(np.tril(U, -1) == 0)
+    assert PT.u_rowwise_err(U, Ur) <= PT.TOL_U
+
+
+def test_prepare_relu_t4_inputs():
+    H64 = _oracle_h(640, 4096, 0, 0, seed=5, relu=True)
+    H32 = H64.astype(np.float32)
+    Ur = O.inverse_cholesky_upper(O.damp_hessian(H32.astype(np.float64))[0])
+    U, _, _ = gptq.prepare(torch.from_numpy(H32).to(DEV), 0.01)
+    assert PT.u_rowwise_err(U.cpu().numpy(), Ur) <= PT.TOL_U
+
+
+def test_prepare_not_positive_definite():
+    H = torch.eye(200, device=DEV)
+    H[150, 150] = -50.0
+    with pytest.raises(gptq.GptqError) as ei:
+        gptq.prepare(H, 0.0)
+    assert ei.value.status == 2
+
+
+def test_prepare_nonfinite():
+    H = torch.eye(64, device=DEV)
+    H[3, 5] = float("nan")
+    with pytest.raises(gptq.GptqError) as ei:
+        gptq.prepare(H, 0.01)
+    assert ei.value.status == 3
+
+
+# ---------------------------------------------------------------------------------------
+# Steps 4-5 (+ packing): the sweep, on the oracle's U
+# ---------------------------------------------------------------------------------------
+
+def _quant_case(m, d, bits, block, wdtype, seed, dead=0, outl=0, n=None):
+    H64 = _oracle_h(d, n or 2 * d, dead, outl, seed=seed)
+    Hd, dmask, _ = O.damp_hessian(H64)
+    U32 = O.inverse_cholesky_upper(Hd).astype(np.float32)
+    W = S.weights(m, d, 0.02, wdtype, seed)
+    return W, U32, dmask
+
+
+@pytest.mark.parametrize("m,d,bits,block,wdtype", [
+    (256, 256, 4, 128, "f32"),
+    (200, 300, 4, 128, "bf16"),
+    (64, 257, 3, 128, "bf16"),
+    (130, 384, 2, 128, "f16"),
+    (96, 200, 8, 128, "bf16"),
+    (100, 256, 4, 32, "bf16"),
+    (70, 150, 3, 7, "f32"),
+    (33, 65, 4, 1, "f32"),
+])
+def test_quantize_parity(m, d, bits, block, wdtype):
+    W, U32, dmask = _quant_case(m, d, bits, block, wdtype, seed=m * 7 + d, dead=2, outl=1)
+    dm = torch.from_numpy(dmask.astype(np.uint8)).to(DEV)
+    qp, sc, zr, Wh = gptq.quantize(W.to(DEV), torch.from_numpy(U32).to(DEV), bits, block, dm)
+    torch.cuda.synchronize()
+    Wn = W.float().numpy()
+    s_ref, z_ref = O.row_grid(Wn, bits)
+    assert np.array_equal(sc.cpu().numpy(), s_ref)          # grid is bit-exact
+    assert np.array_equal(zr.cpu().numpy(), z_ref)
+    codes = _codes(qp, bits, d)
+    # packing layout: the oracle's packing of these codes gives the same words
+    assert np.array_equal(O.pack_codes(codes, bits), qp.cpu().numpy().view(np.uint32))
+    st = PT.check_codes(codes, Wn, U32.astype(np.float64), s_ref, z_ref, bits, block, dmask)
+    # W_hat is the dequantized code, in fp32
+    Wh_ref = (s_ref[:, None] * (codes - z_ref[:, None]).astype(np.float32)).astype(np.float32)
+    assert np.array_equal(Wh.cpu().numpy(), Wh_ref)
+    assert st["entries"] == m * d
+
+
+def test_quantize_dead_columns_quantize_to_zero():
+    W, U32, dmask = _quant_case(64, 256, 4, 128, "bf16", seed=3, dead=6)
+    dm = torch.from_numpy(dmask.astype(np.uint8)).to(DEV)
+    qp, sc, zr, Wh = gptq.quantize(W.to(DEV), torch.from_numpy(U32).to(DEV), 4, 128, dm)
+    Wh = Wh.cpu().numpy()
+    assert np.all(Wh[:, dmask] == 0.0)
+
+
+def test_quantize_nonfinite_weights_flagged():
+    W = torch.zeros(8, 64, device=DEV)
+    W[2, 7] = float("inf")
+    U = torch.eye(64, device=DEV)
+    ws = gptq.workspace(gptq.gptq_quantize_workspace_bytes(8, 64, 4, 128), DEV)
+    gptq.quantize(W, U, 4, 128, ws=ws)
+    st = gptq.gptq_workspace_status(gptq._ptr(ws), gptq._stream(None))
+    assert st == 3
+
+
+# ---------------------------------------------------------------------------------------
+# The whole path on the 256 x 256, 512-token layer
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [3, 4])
+def test_layer_end_to_end_small(bits):
+    wl = S.WORKLOADS["layer256_n512"]
+    layer = wl.layers[0]
+    X = S.activations(layer.act, device="cpu")
+    W = S.layer_weights(layer)
+    ref = O.gptq_layer(X.numpy(), W.numpy(), bits)
+    Xg, Wg = X.to(DEV), W.to(DEV)
+    H = gptq.hessian(Xg)
+    U, dm, nd = gptq.prepare(H, 0.01)
+    qp, sc, zr, Wh = gptq.quantize(Wg, U, bits, 128, dm)
+    torch.cuda.synchronize()
+    e_gpu = O.reconstruction_error(W.numpy(), Wh.cpu().numpy(), ref["H"])
+    e_ref = O.reconstruction_error(W.numpy(), ref["W_hat"], ref["H"])
+    assert abs(e_gpu - e_ref) <= PT.TOL_RECON * e_ref
+    _, q_rtn = O.rtn_quantize(W.numpy(), ref["scale"], ref["zero"], bits)
+    assert e_gpu < O.reconstruction_error(W.numpy(), q_rtn, ref["H"])
+    assert nd == 0
