@@ -96,7 +96,10 @@ struct GemmArgs {
   int lower_only;
   int trans_c;
 };
-gptq_status launch_gemm_nt(const GemmArgs &g, const DevStatus *st, cudaStream_t s);
+gptq_status launch_gemm_nt(const GemmArgs &g, DevStatus *st, cudaStream_t s);
+// tc_gemm.cu: the tcgen05 3xTF32 kernel; UNSUPPORTED when the operands do not meet its
+// alignment requirements (launch_gemm_nt then takes the CUDA-core kernel).
+gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s);
 
 // factor.cu
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,

@@ -2,8 +2,10 @@
 // TF32 head/tail pair.  Used by the lazy-batch trailing update of the column sweep and by
 // the trailing updates of the blocked Cholesky factorization and inversion.
 //
-// This file holds the CUDA-core (SIMT) kernel: exact fp32 products of (head + tail) with
-// fp32 accumulation.  It serves shapes the tensor-core kernel does not take.
+// launch_gemm_nt takes the tcgen05 kernel (tc_gemm.cu) whenever the operands meet its
+// TMA alignment rules; this file's CUDA-core kernel (exact fp32 products of head + tail,
+// fp32 accumulation) serves the remaining shapes (e.g. lazy-batch widths that are not a
+// multiple of 4 columns).
 #include "common.cuh"
 
 namespace gptq {
@@ -82,8 +84,10 @@ gemm_nt_simt_kernel(GemmArgs g, const DevStatus *st) {
 
 }  // namespace
 
-gptq_status launch_gemm_nt(const GemmArgs &g, const DevStatus *st, cudaStream_t s) {
+gptq_status launch_gemm_nt(const GemmArgs &g, DevStatus *st, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPTQ_OK;
+  const gptq_status t = launch_gemm_nt_tc(g, st, s);
+  if (t != GPTQ_ERR_UNSUPPORTED) return t;
   dim3 grid((unsigned)ceil_div(g.N, TN), (unsigned)ceil_div(g.M, TM));
   gemm_nt_simt_kernel<<<grid, NT, 0, s>>>(g, st);
   GPTQ_LAUNCH_CHECK();

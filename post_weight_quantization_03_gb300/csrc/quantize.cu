@@ -316,7 +316,7 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
       g.c = q.Wf + b1; g.ldc = q.ldwf;
       g.M = m; g.N = d - b1; g.K = nb;
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0;
-      GPTQ_TRY(launch_gemm_nt(g, nullptr, s));
+      GPTQ_TRY(launch_gemm_nt(g, q.st, s));
     }
   }
   {

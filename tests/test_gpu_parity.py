@@ -34,6 +34,16 @@ def _x(spec, n_tok=None):
     return X
 
 
+def _padded(X, dev=DEV):
+    """X on the device with its row pitch rounded up to 16 bytes (an ABI requirement)."""
+    n, d = X.shape
+    step = 16 // X.element_size()
+    ld = (d + step - 1) // step * step
+    buf = torch.zeros(n, ld, dtype=X.dtype, device=dev)
+    buf[:, :d] = X.to(dev)
+    return buf[:, :d]
+
+
 def _codes(qpacked, bits, d):
     return O.unpack_codes(qpacked.cpu().numpy().view(np.uint32), bits, d)
 
@@ -52,7 +62,11 @@ def _codes(qpacked, bits, d):
 def test_hessian_parity(d, n, dtype, dead, outl):
     spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=dead, n_outlier=outl, seed=d + n)
     X = _x(spec)
-    Hg = gptq.hessian(X.to(DEV))
+    if (d * X.element_size()) % 16:
+        with pytest.raises(gptq.GptqError) as ei:   # unpadded row pitch is rejected
+            gptq.hessian(X.to(DEV))
+        assert ei.value.status == 1
+    Hg = gptq.hessian(_padded(X))
     torch.cuda.synchronize()
     Hr = O.hessian(X.float().numpy() if dtype != "f32" else X.numpy())
     Hg = Hg.cpu().numpy()
