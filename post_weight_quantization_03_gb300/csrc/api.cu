@@ -52,7 +52,7 @@ gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, in
     return GPTQ_ERR_INVALID_ARG;
   if (!aligned(H, 16)) return GPTQ_ERR_INVALID_ARG;
   if (d_in > (int64_t)1 << 20) return GPTQ_ERR_UNSUPPORTED;
-  return launch_hessian(X, xdtype, n_tok, d_in, ldx, H, accumulate ? 1 : 0,
+  return launch_hessian(X, xdtype, n_tok, d_in, ldx, H, accumulate ? 1 : 0, nullptr,
                         (cudaStream_t)stream);
 }
 

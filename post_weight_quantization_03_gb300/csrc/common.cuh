@@ -80,8 +80,9 @@ __device__ __forceinline__ float tf32_head(float x) {
 // ----------------------------------------------------------------------------------------
 
 // hessian.cu
+// `st` (may be null) receives TIMEOUT if a bounded wait of the tensor-core kernel gives up.
 gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
-                           float *H, int accumulate, cudaStream_t s);
+                           float *H, int accumulate, DevStatus *st, cudaStream_t s);
 
 // gemm.cu: C[m, n] (+)= alpha * sum_k A[m, k] * B[n, k], operands given as a TF32 head
 // and tail pair each (tail may be null = 0).  lower_only skips tiles strictly above the

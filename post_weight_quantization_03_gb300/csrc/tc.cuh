@@ -186,5 +186,13 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
          | ((M >> 4) << 24);       // M / 16
 }
 
+// ---------------------------------------------------------------------------------------
+// Host: 2D tensor map over a row-major [rows, cols] matrix (row pitch `ld_bytes`), box =
+// box_cols x box_rows elements, 128-byte swizzle, zero fill out of bounds.  Returns false
+// when the driver entry point is missing or the base / pitch are not 16-byte aligned.
+// ---------------------------------------------------------------------------------------
+bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int64_t rows,
+                  int64_t cols, int64_t ld_bytes, int box_cols, int box_rows);
+
 }  // namespace tc
 }  // namespace gptq

@@ -165,23 +165,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-}  // namespace
-
-// 2D fp32 tensor map over a row-major [rows, cols] matrix with row pitch `ld` elements,
-// box = 32 columns (128 bytes) x box_rows, 128-byte swizzle, zero fill out of bounds.
 bool make_tmap_f32(CUtensorMap *m, const float *base, int64_t rows, int64_t cols, int64_t ld,
                    int box_rows) {
+  return tc::make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rows, cols, ld * 4, BK,
+                          box_rows);
+}
+
+}  // namespace
+
+bool tc::make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int64_t rows,
+                      int64_t cols, int64_t ld_bytes, int box_cols, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  if (((uintptr_t)base & 15) || ((ld * 4) & 15)) return false;
+  if (((uintptr_t)base & 15) || (ld_bytes & 15) || rows < 1 || cols < 1) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)base, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  return fn(m, dt, 2, (void *)base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tensor-core path of launch_gemm_nt.  Requirements (else returns UNSUPPORTED so the

@@ -74,6 +74,19 @@ def test_hessian_parity(d, n, dtype, dead, outl):
     assert np.array_equal(Hg, Hg.T)
 
 
+def test_hessian_long_token_sum():
+    # 262144 tokens into one H: the accumulation precision over a long sum
+    spec = S.ActivationSpec(d_in=256, n_tok=262144, dtype="f16", n_dead=2, n_outlier=3, seed=91)
+    Xg = S.activations(spec, device=DEV)
+    Hg = gptq.hessian(Xg).cpu().numpy()
+    Hr = O.hessian(Xg.cpu().float().numpy())
+    assert PT.rel_fro(Hg, Hr) <= PT.TOL_H
+    # diagonal entries (long sums of positive terms) individually
+    dg, dr = np.diag(Hg), np.diag(Hr)
+    live = dr > 0
+    assert np.max(np.abs(dg[live] - dr[live]) / dr[live]) <= 1e-5
+
+
 def test_hessian_accumulates_over_chunks():
     spec = S.ActivationSpec(d_in=384, n_tok=6144, dtype="f16", n_dead=2, seed=77)
     X = _x(spec).to(DEV)
