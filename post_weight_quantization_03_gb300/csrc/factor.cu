@@ -24,7 +24,6 @@ namespace gptq {
 namespace {
 
 constexpr int NB = 128;            // panel width
-constexpr int POTRF_THREADS = 256;
 constexpr int LDS = NB + 1;        // padded smem leading dimension
 
 // ---------------------------------------------------------------------------------------
@@ -96,94 +95,128 @@ __global__ void identity_kernel(float *Y, int64_t d) {
 }
 
 // ---------------------------------------------------------------------------------------
-// potrf: Cholesky of the n x n diagonal block at (k0, k0) of A (n <= NB), then its
-// inverse.  Writes Linv (NB x NB, zero-padded, lower) in fp32.  A non-positive pivot
-// records NOT_PD with its global index.
+// potrf: Cholesky factor of the n x n diagonal block at (k0, k0) of A (n <= NB) and, in
+// the same pass, its inverse Linv (the forward substitution L X = I run alongside).  Only
+// Linv leaves the kernel (NB x NB, lower, zero padded): the panel below is L_ik = A_ik
+// Linv^T and the inversion needs Linv only.
+//
+// Register blocked, 16 warps: warp w owns columns [8w, 8w+8), lane owns rows lane + 32a,
+// of both the working block S and the right-hand side B (identity at start).  Column j:
+//   publish S[:, j] and B[j, :]; one barrier; then with p = S[j][j] (pivot):
+//   S[i][l] -= S[i][j] S[l][j] / p          for i >= l > j      (outer-product Cholesky)
+//   B[i][c] -= S[i][j] B[j][c] / p  (i > j), B[j][c] /= sqrt(p)  (forward substitution)
+// which leaves B = L^-1.  Warps whose columns are finished (or not yet reached, for B)
+// skip their update; column buffers are double buffered so one barrier per column suffices.
+// A non-positive pivot records NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(POTRF_THREADS)
-potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatus *st) {
-  extern __shared__ float sm[];
-  float *S = sm;               // NB x LDS: working block, lower part, then L
-  float *X = sm + NB * LDS;    // NB x LDS: Linv
-  if (st->status != 0) return;
-  const int tid = threadIdx.x;
-  for (int e = tid; e < NB * NB; e += blockDim.x) {
-    const int i = e / NB, j = e % NB;
-    float v;
-    if (i < n && j < n)
-      v = (i >= j) ? A[(k0 + i) * d + (k0 + j)] : 0.0f;
-    else
-      v = (i == j) ? 1.0f : 0.0f;
-    S[i * LDS + j] = v;
-  }
-  __syncthreads();
-  // right-looking outer-product form on the unscaled columns:
-  //   S[i][l] -= S[i][j] * S[l][j] / S[j][j]   for i >= l > j
-  // then L[i][j] = S[i][j] / sqrt(S[j][j]).
-  __shared__ int bad_pivot;
-  if (tid == 0) bad_pivot = -1;
-  __syncthreads();
-  for (int j = 0; j < NB; ++j) {
-    const float piv = S[j * LDS + j];
-    if (!(piv > 0.0f)) {
-      if (tid == 0 && bad_pivot < 0) bad_pivot = j;
-      break;  // every thread sees the same pivot value: uniform exit
+constexpr int PF_THREADS = 512;
+
+template <int J>
+struct PotrfStep {
+  static __device__ __forceinline__ void run(float (&s)[4][8], float (&x)[4][8],
+                                             float *colbuf, float *rowbuf, int warp, int lane,
+                                             int &bad) {
+    constexpr int BJ = J % 8, AJ = J / 32, LJ = J % 32;
+    float *cb = colbuf + (J & 1) * NB;
+    float *rb = rowbuf + (J & 1) * NB;
+    if (warp == J / 8) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) cb[lane + 32 * a] = s[a][BJ];
     }
-    const float rp = 1.0f / piv;
-    const int rem = NB - 1 - j;                 // trailing order
-    const int cnt = rem * (rem + 1) / 2;        // lower-triangle elements incl. diagonal
-    for (int e = tid; e < cnt; e += blockDim.x) {
-      // decode e -> (ii, ll), ii >= ll, within the trailing block
-      int ii = (int)((sqrtf(8.0f * (float)e + 1.0f) - 1.0f) * 0.5f);
-      while (ii * (ii + 1) / 2 > e) --ii;
-      while ((ii + 1) * (ii + 2) / 2 <= e) ++ii;
-      const int ll = e - ii * (ii + 1) / 2;
-      const int i = j + 1 + ii, l = j + 1 + ll;
-      S[i * LDS + l] -= S[i * LDS + j] * S[l * LDS + j] * rp;
+    if (lane == LJ) {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) rb[8 * warp + b] = x[AJ][b];
     }
     __syncthreads();
-  }
-  __syncthreads();
-  if (bad_pivot >= 0) {
-    if (tid == 0) {
-      if (bad_pivot < n) {
-        if (atomicCAS(&st->status, 0, GPTQ_ERR_NOT_PD) == 0) st->info = (int)(k0 + bad_pivot) + 1;
+    const float piv = cb[J];
+    const bool okp = piv > 0.0f;  // false for NaN as well
+    if (!okp && bad < 0) bad = J;
+    const float rp = okp ? 1.0f / piv : 0.0f;
+    const float rl = okp ? 1.0f / sqrtf(piv) : 0.0f;
+    float ci[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) ci[a] = cb[lane + 32 * a] * rp;
+    if (8 * warp + 7 > J) {  // this warp still has unfinished columns l > J
+      float cl[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) cl[b] = cb[8 * warp + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int i = lane + 32 * a, l = 8 * warp + b;
+          if (l > J && i >= l) s[a][b] = fmaf(-ci[a], cl[b], s[a][b]);
+        }
+    }
+    if (8 * warp <= J) {  // B row J is zero beyond column J
+      float rc[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) rc[b] = rb[8 * warp + b];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int i = lane + 32 * a;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (i > J) x[a][b] = fmaf(-ci[a], rc[b], x[a][b]);
+          else if (i == J) x[a][b] = rc[b] * rl;
+        }
       }
     }
+    PotrfStep<J + 1>::run(s, x, colbuf, rowbuf, warp, lane, bad);
+  }
+};
+template <>
+struct PotrfStep<NB> {
+  static __device__ __forceinline__ void run(float (&)[4][8], float (&)[4][8], float *, float *,
+                                             int, int, int &) {}
+};
+
+__global__ void __launch_bounds__(PF_THREADS)
+potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatus *st) {
+  __shared__ float colbuf[2 * NB], rowbuf[2 * NB];
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = st->status != 0;
+  __syncthreads();
+  if (s_skip) return;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float s[4][8], x[4][8];
+  const bool vec = (d % 4 == 0);
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = lane + 32 * a;
+    const float *row = A + (k0 + i) * d + k0 + 8 * warp;
+    if (i < n && vec && 8 * warp + 8 <= n) {
+      const float4 u = *reinterpret_cast<const float4 *>(row);
+      const float4 v = *reinterpret_cast<const float4 *>(row + 4);
+      s[a][0] = u.x; s[a][1] = u.y; s[a][2] = u.z; s[a][3] = u.w;
+      s[a][4] = v.x; s[a][5] = v.y; s[a][6] = v.z; s[a][7] = v.w;
+    } else {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) s[a][b] = (i < n && 8 * warp + b < n) ? row[b] : 0.0f;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int l = 8 * warp + b;
+      if (i >= n || l >= n) s[a][b] = (i == l) ? 1.0f : 0.0f;  // identity padding
+      x[a][b] = (i == l) ? 1.0f : 0.0f;
+    }
+  }
+  int bad = -1;
+  PotrfStep<0>::run(s, x, colbuf, rowbuf, warp, lane, bad);
+  if (bad >= 0) {
+    if (threadIdx.x == 0 && bad < n &&
+        atomicCAS(&st->status, 0, (int)GPTQ_ERR_NOT_PD) == 0)
+      st->info = (int)(k0 + bad) + 1;
     return;
   }
-  // scale columns: L[i][j] = S[i][j] / sqrt(S[j][j]) (i >= j)
-  __shared__ float rsd[NB];
-  for (int j = tid; j < NB; j += blockDim.x) rsd[j] = sqrtf(S[j * LDS + j]);
-  __syncthreads();
-  for (int e = tid; e < NB * NB; e += blockDim.x) {
-    const int i = e / NB, j = e % NB;
-    if (i > j) S[i * LDS + j] = S[i * LDS + j] / rsd[j];
-  }
-  for (int j = tid; j < NB; j += blockDim.x) S[j * LDS + j] = rsd[j];
-  __syncthreads();
-  // forward substitution for Linv = L^-1, one column t per thread:
-  //   X[i][t] = (delta_it - sum_{l<i} L[i][l] X[l][t]) / L[i][i]
-  for (int t = tid; t < NB; t += blockDim.x) {
-    for (int i = 0; i < NB; ++i) {
-      float acc = (i == t) ? 1.0f : 0.0f;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      int l = t;  // X[l][t] = 0 for l < t
-      for (; l + 3 < i; l += 4) {
-        a0 = fmaf(S[i * LDS + l], X[l * LDS + t], a0);
-        a1 = fmaf(S[i * LDS + l + 1], X[(l + 1) * LDS + t], a1);
-        a2 = fmaf(S[i * LDS + l + 2], X[(l + 2) * LDS + t], a2);
-        a3 = fmaf(S[i * LDS + l + 3], X[(l + 3) * LDS + t], a3);
-      }
-      for (; l < i; ++l) a0 = fmaf(S[i * LDS + l], X[l * LDS + t], a0);
-      acc -= (a0 + a1) + (a2 + a3);
-      X[i * LDS + t] = (i < t) ? 0.0f : acc / S[i * LDS + i];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = lane + 32 * a;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int c = 8 * warp + b;
+      Linv[i * NB + c] = (i < n && c < n) ? x[a][b] : 0.0f;
     }
-  }
-  __syncthreads();
-  for (int e = tid; e < NB * NB; e += blockDim.x) {
-    const int i = e / NB, j = e % NB;
-    Linv[e] = (i < n && j < n) ? X[i * LDS + j] : 0.0f;
   }
 }
 
@@ -203,8 +236,14 @@ rowmul_kernel(const float *In, int64_t ldi, float *Out, int64_t ldo, int64_t r0,
   if (st->status != 0) return;
   const int tid = threadIdx.x;
   const int64_t rb = r0 + (int64_t)blockIdx.x * RM_ROWS;
-  for (int e = tid; e < NB * NB; e += blockDim.x) Bs[(e / NB) * LDS + e % NB] = Bm[e];
-  for (int e = tid; e < RM_ROWS * NB; e += blockDim.x) {
+#pragma unroll 16
+  for (int it = 0; it < NB * NB / RM_THREADS; ++it) {
+    const int e = it * RM_THREADS + tid;
+    Bs[(e / NB) * LDS + e % NB] = Bm[e];
+  }
+#pragma unroll 16
+  for (int it = 0; it < RM_ROWS * NB / RM_THREADS; ++it) {
+    const int e = it * RM_THREADS + tid;
     const int r = e / NB, t = e % NB;
     const int64_t gr = rb + r;
     Is[r * LDS + t] = (gr < r1 && t < n) ? In[gr * ldi + t] : 0.0f;
@@ -288,12 +327,8 @@ size_t prepare_ws_bytes(int64_t d) {
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                            void *ws, cudaStream_t s) {
   static bool attr_done = false;
-  const size_t potrf_smem = 2 * NB * LDS * sizeof(float);
   const size_t rm_smem = (NB + RM_ROWS) * LDS * sizeof(float);
   if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)potrf_smem));
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rm_smem));
@@ -311,7 +346,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   for (int64_t k0 = 0; k0 < d; k0 += NB) {
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
-    potrf_kernel<<<1, POTRF_THREADS, potrf_smem, s>>>(A, d, k0, n, w.Linv, w.st);
+    potrf_kernel<<<1, PF_THREADS, 0, s>>>(A, d, k0, n, w.Linv, w.st);
     GPTQ_LAUNCH_CHECK();
     // trsm: rows [k1, d) of panel k -> L panel (hi/lo) only (A's panel is not reused)
     if (k1 < d) {

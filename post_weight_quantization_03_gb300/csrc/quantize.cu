@@ -10,7 +10,7 @@
 //   trailing : W[:, b1:] -= E U[b0:b1, b1:]   (the deferred lazy-batch product, run as
 //              C -= A B^T with B = U^T rows, i.e. Lt = U^T split into head/tail)
 // then one pass packs the codes and writes W_hat.
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace gptq {
 
@@ -18,8 +18,12 @@ namespace {
 
 constexpr int SB = 128;          // maximum block width held by one thread
 constexpr int SW_ROWS = 64;      // rows (threads) per sweep CTA
-constexpr int LDU = SB + 4;      // smem leading dimension of the U block
-constexpr int LDW = SB + 1;      // smem leading dimension of the staging tile
+constexpr int LDU = SB + 4;      // leading dimension of a packed U diagonal block
+constexpr int LDW = SB + 4;      // smem leading dimension of the staging tile (float4 rows
+                                 // of consecutive threads fall in distinct bank groups)
+// One packed diagonal block: U[b0:b0+nb, b0:b0+nb] upper part in SB x LDU (identity
+// padding), then the SB reciprocal pivots 1 / U_jj.
+constexpr int UD_FLOATS = SB * LDU + SB;
 
 // ---------------------------------------------------------------------------------------
 // Grid: per-row asymmetric min-max with 0 in the range; fp32 working copy of W with dead
@@ -86,6 +90,33 @@ __global__ void lt_split_kernel(const float *__restrict__ U, int64_t d, float *_
 }
 
 // ---------------------------------------------------------------------------------------
+// Packs the diagonal blocks of U (one CTA per block) for the sweep: upper triangle of
+// U[b0:b0+nb, b0:b0+nb], identity padding to SB x SB, then 1 / U_jj.
+// ---------------------------------------------------------------------------------------
+__global__ void diag_blocks_kernel(const float *__restrict__ U, int64_t d, int block,
+                                   float *__restrict__ Ud) {
+  const int64_t b0 = (int64_t)blockIdx.x * block;
+  const int nb = (int)((d - b0) < block ? (d - b0) : block);
+  float *out = Ud + (int64_t)blockIdx.x * UD_FLOATS;
+#pragma unroll 8
+  for (int it = 0; it < SB * SB / 256; ++it) {
+    const int e = it * 256 + threadIdx.x;
+    const int i = e / SB, j = e % SB;
+    float v = 0.f;
+    if (i < nb && j < nb) {
+      if (i <= j) v = U[(b0 + i) * d + (b0 + j)];
+    } else if (i == j) {
+      v = 1.f;
+    }
+    out[i * LDU + j] = v;
+  }
+  for (int i = threadIdx.x; i < SB * (LDU - SB); i += 256)
+    out[(i / (LDU - SB)) * LDU + SB + i % (LDU - SB)] = 0.f;
+  for (int j = threadIdx.x; j < SB; j += 256)
+    out[SB * LDU + j] = (j < nb) ? 1.0f / U[(b0 + j) * d + (b0 + j)] : 1.0f;
+}
+
+// ---------------------------------------------------------------------------------------
 // One column step of the in-block sweep, unrolled at compile time over the block so the
 // row's working weights stay in registers:
 //   code = clamp(rint(w_J / s) + z, 0, maxq);  q = s (code - z);  e = (w_J - q) / U_JJ
@@ -115,63 +146,94 @@ struct SweepStep<SB> {
 };
 
 // ---------------------------------------------------------------------------------------
-// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA.
+// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA.  The packed U
+// block arrives by one bulk copy while the threads stage the working-weight tile.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(SW_ROWS)
 sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, int nb,
-             const float *__restrict__ U, int64_t d, const float *__restrict__ scale,
+             const float *__restrict__ Ud, const float *__restrict__ scale,
              const int32_t *__restrict__ zero, float maxq, float *__restrict__ Ehi,
              float *__restrict__ Elo, uint8_t *__restrict__ codes, int64_t ldc,
-             const DevStatus *st) {
-  extern __shared__ float sm[];
-  float *Us = sm;                       // SB x LDU, upper part of U's diagonal block
-  float *stage = sm + SB * LDU;         // SW_ROWS x LDW
-  float *rdiag = stage + SW_ROWS * LDW; // SB reciprocals of U_jj
+             DevStatus *st) {
+  extern __shared__ __align__(16) float sm[];
+  float *Us = sm;                        // SB x LDU, then SB reciprocals
+  float *rdiag = sm + SB * LDU;
+  float *stage = sm + UD_FLOATS;         // SW_ROWS x LDW
+  __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
-  // U block (upper triangle only); padding columns get U_jj = 1 and no coupling
-  for (int e = tid; e < SB * SB; e += blockDim.x) {
-    const int i = e / SB, j = e % SB;
-    float v = 0.f;
-    if (i < nb && j < nb) {
-      if (i <= j) v = U[(b0 + i) * d + (b0 + j)];
-    } else if (i == j) {
-      v = 1.f;
+  if (tid == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar, UD_FLOATS * 4);
+    tc::bulk_load(Us, Ud, UD_FLOATS * 4, &bar);
+  }
+  // working weights, coalesced; float4 when the tile rows are 16-byte aligned
+  if ((b0 % 4) == 0 && (ldwf % 4) == 0) {
+#pragma unroll 8
+    for (int it = 0; it < SB / 4; ++it) {
+      const int e = it * SW_ROWS + tid;      // float4 index in the tile
+      const int r = e / (SB / 4), q = e % (SB / 4);
+      const int64_t gr = r0 + r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (gr < m && 4 * q < nb) v = *reinterpret_cast<const float4 *>(Wf + gr * ldwf + b0 + 4 * q);
+      if (4 * q + 4 > nb) {  // ragged last block: clear columns >= nb
+        if (4 * q + 0 >= nb) v.x = 0.f;
+        if (4 * q + 1 >= nb) v.y = 0.f;
+        if (4 * q + 2 >= nb) v.z = 0.f;
+        if (4 * q + 3 >= nb) v.w = 0.f;
+      }
+      *reinterpret_cast<float4 *>(stage + r * LDW + 4 * q) = v;
     }
-    Us[i * LDU + j] = v;
+  } else {
+#pragma unroll 16
+    for (int it = 0; it < SB; ++it) {
+      const int e = it * SW_ROWS + tid;
+      const int r = e / SB, j = e % SB;
+      const int64_t gr = r0 + r;
+      stage[r * LDW + j] = (gr < m && j < nb) ? Wf[gr * ldwf + b0 + j] : 0.f;
+    }
   }
-  // working weights, coalesced
-  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
-    const int r = e / SB, j = e % SB;
-    const int64_t gr = r0 + r;
-    stage[r * LDW + j] = (gr < m && j < nb) ? Wf[gr * ldwf + b0 + j] : 0.f;
-  }
-  __syncthreads();
-  for (int j = tid; j < SB; j += blockDim.x) rdiag[j] = 1.0f / Us[j * LDU + j];
-  __syncthreads();
+  const int got = tc::mbar_wait(&bar, 0, st) ? 1 : 0;
+  if (!__syncthreads_and(got)) return;  // CTA-uniform: later barriers stay matched
   const int64_t row = r0 + tid;
   const float s = row < m ? scale[row] : 1.f;
   const float z = row < m ? (float)zero[row] : 0.f;
   float w[SB];
 #pragma unroll
-  for (int j = 0; j < SB; ++j) w[j] = stage[tid * LDW + j];
+  for (int q = 0; q < SB / 4; ++q) {
+    const float4 v = *reinterpret_cast<const float4 *>(stage + tid * LDW + 4 * q);
+    w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+  }
   uint32_t cw[SB / 4];  // codes, 4 per word (byte j%4 of word j/4)
 #pragma unroll
   for (int i = 0; i < SB / 4; ++i) cw[i] = 0u;
   SweepStep<0>::run(w, cw, Us, rdiag, s, z, maxq);
-  // stage E, then store coalesced as a head/tail pair
-  __syncthreads();
+  // stage E (own row), then store coalesced as head/tail
 #pragma unroll
-  for (int j = 0; j < SB; ++j) stage[tid * LDW + j] = (j < nb) ? w[j] : 0.f;
+  for (int q = 0; q < SB / 4; ++q) {
+    float4 v = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    if (4 * q + 0 >= nb) v.x = 0.f;
+    if (4 * q + 1 >= nb) v.y = 0.f;
+    if (4 * q + 2 >= nb) v.z = 0.f;
+    if (4 * q + 3 >= nb) v.w = 0.f;
+    *reinterpret_cast<float4 *>(stage + tid * LDW + 4 * q) = v;
+  }
   __syncthreads();
-  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
-    const int r = e / SB, j = e % SB;
+#pragma unroll 8
+  for (int it = 0; it < SB / 4; ++it) {
+    const int e = it * SW_ROWS + tid;
+    const int r = e / (SB / 4), q = e % (SB / 4);
     const int64_t gr = r0 + r;
     if (gr < m) {
-      const float v = stage[r * LDW + j];
-      const float h = tf32_head(v);
-      Ehi[gr * SB + j] = h;
-      Elo[gr * SB + j] = v - h;
+      const float4 v = *reinterpret_cast<const float4 *>(stage + r * LDW + 4 * q);
+      const float4 h = make_float4(tf32_head(v.x), tf32_head(v.y), tf32_head(v.z), tf32_head(v.w));
+      *reinterpret_cast<float4 *>(Ehi + gr * SB + 4 * q) = h;
+      *reinterpret_cast<float4 *>(Elo + gr * SB + 4 * q) =
+          make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
     }
   }
   __syncthreads();
@@ -186,7 +248,6 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
     const int64_t gr = r0 + r;
     if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
   }
-  (void)st;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -231,6 +292,7 @@ struct QuantWs {
   float *Ehi, *Elo;
   float *Lhi, *Llo; int64_t ldl;
   uint8_t *codes; int64_t ldc;
+  float *Ud;
 };
 
 QuantWs carve_quantize(void *ws, int64_t m, int64_t d) {
@@ -245,18 +307,21 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d) {
   q.Lhi = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
   q.Llo = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
   q.ldc = (int64_t)round_up((size_t)d, 16);
-  q.codes = (uint8_t *)p;
+  q.codes = (uint8_t *)p; p += round_up((size_t)m * q.ldc, 256);
+  q.Ud = (float *)p;
   return q;
 }
 
 }  // namespace
 
 size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
-  (void)bits; (void)block;
+  (void)bits;
   const size_t ldwf = round_up((size_t)d, 4), ldl = round_up((size_t)d, 4);
   const size_t ldc = round_up((size_t)d, 16);
+  const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
   return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * SB * 4, 256) +
-         2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256);
+         2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
+         nblk * UD_FLOATS * 4;
 }
 
 gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
@@ -264,7 +329,7 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
                             uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
                             void *ws, cudaStream_t s) {
   static bool attr_done = false;
-  const size_t sweep_smem = (SB * LDU + SW_ROWS * LDW + SB) * sizeof(float);
+  const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW) * sizeof(float);
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -300,14 +365,16 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
     dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
     lt_split_kernel<<<tg, dim3(32, 8), 0, s>>>(U, d, q.Lhi, q.Llo, q.ldl);
     GPTQ_LAUNCH_CHECK();
+    diag_blocks_kernel<<<(unsigned)ceil_div(d, block), 256, 0, s>>>(U, d, block, q.Ud);
+    GPTQ_LAUNCH_CHECK();
   }
   const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
   for (int64_t b0 = 0; b0 < d; b0 += block) {
     const int nb = (int)((d - b0) < block ? (d - b0) : block);
     const int64_t b1 = b0 + nb;
-    sweep_kernel<<<sweep_grid, SW_ROWS, sweep_smem, s>>>(q.Wf, q.ldwf, m, b0, nb, U, d, scale,
-                                                         zero, maxq, q.Ehi, q.Elo, q.codes,
-                                                         q.ldc, q.st);
+    sweep_kernel<<<sweep_grid, SW_ROWS, sweep_smem, s>>>(
+        q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
+        q.Elo, q.codes, q.ldc, q.st);
     GPTQ_LAUNCH_CHECK();
     if (b1 < d) {
       GemmArgs g{};
@@ -331,6 +398,5 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
   return GPTQ_OK;
 }
 
-size_t quantize_status_offset() { return 0; }
 
 }  // namespace gptq

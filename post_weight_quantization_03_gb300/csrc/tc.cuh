@@ -79,6 +79,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, int
       : "memory");
 }
 
+// Contiguous global -> shared bulk copy (no tensor map); `bytes` a multiple of 16, both
+// addresses 16-byte aligned; completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // tcgen05: TMEM allocation, MMA, commit, loads, fences
 // ---------------------------------------------------------------------------------------
