@@ -172,6 +172,41 @@ gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_
                                 gptq_stream_t stream);
 
 /*
+ * GPTQ_NOALLOC_SCRATCH_BYTES: size of the fixed scratch array behind
+ * gptq_quantize_layer_noalloc (32 MiB, held on every GPU that loads this library until the
+ * process exits).  A layer fits when
+ * gptq_quantize_workspace_bytes(d_out, d_in, bits, block) <= GPTQ_NOALLOC_SCRATCH_BYTES
+ * (for example 1024 x 1024 at 4 bits, B = 128).
+ */
+#define GPTQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * gptq_quantize_layer_noalloc: gptq_quantize_layer for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc: code embedded in a host framework that owns all device memory and forbids
+ * allocations while it runs, or code that must not cause the device-wide synchronization
+ * an allocation or free can bring.  It computes exactly what gptq_quantize_layer computes,
+ * with the same arguments minus the workspace: its scratch is a fixed array inside the
+ * library (GPTQ_NOALLOC_SCRATCH_BYTES per GPU), and the call itself allocates nothing.
+ *
+ *   - Sizes: returns GPTQ_ERR_WORKSPACE, before touching the GPU, when the layer needs more
+ *     scratch than GPTQ_NOALLOC_SCRATCH_BYTES; use gptq_quantize_layer with a workspace then.
+ *   - First call on a device: looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the last call's
+ *     contents (each call clears what it needs).  Calls whose GPU work overlaps (e.g. on
+ *     two unordered streams) race and give wrong results: keep them on one stream.
+ *   - Non-finite weights are flagged in the shared array, which callers cannot address;
+ *     check inputs beforehand if that matters.
+ * Asynchronous.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+gptq_status gptq_quantize_layer_noalloc(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                                        int64_t ldw, const float *U, const uint8_t *dead_mask,
+                                        int bits, int block, uint32_t *qpacked, float *scale,
+                                        int32_t *zero, float *W_hat, gptq_stream_t stream);
+
+/*
  * gptq_workspace_status: synchronize `stream`, then return the device-side status the
  * last gptq_quantize_layer on workspace `ws` recorded (GPTQ_OK, GPTQ_ERR_NONFINITE or
  * GPTQ_ERR_TIMEOUT).  `ws` must be a workspace that call used.

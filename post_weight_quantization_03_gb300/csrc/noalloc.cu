@@ -1,0 +1,69 @@
+// gptq_quantize_layer_noalloc: the layer sweep for callers that cannot allocate device
+// memory themselves -- code that runs inside a host framework which owns the device
+// memory pool and forbids allocations on its hot path, or code that must never trigger
+// the device-wide synchronization that cudaMalloc/cudaFree can imply.  Instead of a
+// caller workspace it uses a fixed scratch array that is part of this library's device
+// image, so a call allocates nothing.
+//
+// The array is GPTQ_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads the library and
+// stays there until the process exits.  All calls on a device share it, and it keeps the
+// contents of the last call; the sweep overwrites every scratch byte it reads and clears
+// its status block at the start of each call, so nothing needs to be zeroed beforehand.
+// Two calls whose work overlaps on the GPU (different streams, no ordering between them)
+// race on the array and produce garbage: order them on one stream.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace gptq {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GPTQ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// The array's name is only a host-side stand-in in host code; the device address must be
+// looked up once per device, with that device current.
+gptq_status scratch_address(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GPTQ_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return GPTQ_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return GPTQ_OK;
+}
+
+}  // namespace
+}  // namespace gptq
+
+extern "C" gptq_status gptq_quantize_layer_noalloc(
+    const void *W, int wdtype, int64_t d_out, int64_t d_in, int64_t ldw, const float *U,
+    const uint8_t *dead_mask, int bits, int block, uint32_t *qpacked, float *scale,
+    int32_t *zero, float *W_hat, gptq_stream_t stream) {
+  // Size check first: a layer whose scratch exceeds the fixed array is refused before
+  // anything touches the GPU.
+  if (d_out < 1 || d_in < 1) return GPTQ_ERR_INVALID_ARG;
+  if (block < 1 || block > 128) return GPTQ_ERR_INVALID_ARG;
+  const size_t need = gptq_quantize_workspace_bytes(d_out, d_in, bits, block);
+  if (need == 0) return GPTQ_ERR_INVALID_ARG;
+  if (need > (size_t)GPTQ_NOALLOC_SCRATCH_BYTES) return GPTQ_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const gptq_status st = gptq::scratch_address(&scratch);
+  if (st != GPTQ_OK) return st;
+  return gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
+                             scale, zero, W_hat, scratch, (size_t)GPTQ_NOALLOC_SCRATCH_BYTES,
+                             stream);
+}

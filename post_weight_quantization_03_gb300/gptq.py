@@ -39,7 +39,12 @@ _SIGS = {
                                        _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                        _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_workspace_status": (_c.c_int, [_c.c_void_p, _c.c_void_p]),
+    "gptq_quantize_layer_noalloc": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+                                               _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_int,
+                                               _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                               _c.c_void_p, _c.c_void_p]),
 }
+NOALLOC_SCRATCH_BYTES = 32 << 20  # GPTQ_NOALLOC_SCRATCH_BYTES in include/gptq.h
 
 _lib = None
 
@@ -121,6 +126,12 @@ def gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, 
 
 def gptq_workspace_status(ws, stream):
     return load().gptq_workspace_status(ws, stream)
+
+
+def gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
+                                qpacked, scale, zero, W_hat, stream):
+    return load().gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits,
+                                              block, qpacked, scale, zero, W_hat, stream)
 
 
 # ---------------------------------------------------------------------------------------
