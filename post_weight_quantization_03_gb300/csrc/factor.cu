@@ -24,7 +24,6 @@ namespace gptq {
 namespace {
 
 constexpr int NB = 128;            // panel width
-constexpr int LDS = NB + 1;        // padded smem leading dimension
 
 // ---------------------------------------------------------------------------------------
 // Dead columns and damping (one CTA): dead = {i : H_ii == 0}; H_ii <- 1 for dead i;
@@ -95,128 +94,224 @@ __global__ void identity_kernel(float *Y, int64_t d) {
 }
 
 // ---------------------------------------------------------------------------------------
-// potrf: Cholesky factor of the n x n diagonal block at (k0, k0) of A (n <= NB) and, in
-// the same pass, its inverse Linv (the forward substitution L X = I run alongside).  Only
-// Linv leaves the kernel (NB x NB, lower, zero padded): the panel below is L_ik = A_ik
-// Linv^T and the inversion needs Linv only.
+// potrf: Cholesky factor L of the n x n diagonal block at (k0, k0) of A (n <= NB) and its
+// inverse Linv.  Only Linv leaves the kernel (NB x NB, lower, zero padded): the panel below
+// is L_ik = A_ik Linv^T and the inversion needs Linv only.
 //
-// Register blocked, 16 warps: warp w owns columns [8w, 8w+8), lane owns rows lane + 32a,
-// of both the working block S and the right-hand side B (identity at start).  Column j:
-//   publish S[:, j] and B[j, :]; one barrier; then with p = S[j][j] (pivot):
-//   S[i][l] -= S[i][j] S[l][j] / p          for i >= l > j      (outer-product Cholesky)
-//   B[i][c] -= S[i][j] B[j][c] / p  (i > j), B[j][c] /= sqrt(p)  (forward substitution)
-// which leaves B = L^-1.  Warps whose columns are finished (or not yet reached, for B)
-// skip their update; column buffers are double buffered so one barrier per column suffices.
+// Recursive over four 32-column sub-panels p (P0 = 32p, R0 = P0 + 32), in shared memory,
+// with the inverse built alongside in transposed form (Bt = right-hand side of L Y = I,
+// transposed, which becomes Yt = Linv^T), exactly like the panel loop of the whole
+// factorization:
+//   leaf   : one warp factors the 32 x 32 tile (lane i holds row i; pivots and multipliers
+//            travel by shuffles) and inverts it (lane c solves column c)
+//   phase 1: L_ip  = A_ip Linv_pp^T              rows i >= R0      (trsm)
+//            Yt_cp = Bt_cp Linv_pp^T              rows c <  R0      (inverse, step a)
+//   phase 2: A_il -= L_ip L_lp^T                  R0 <= l <= i      (syrk)
+//            Bt_cr -= Yt_cp L_rp^T                c < R0 <= r       (inverse, step b)
+// Every product is C(m, n) = sum_k A(m, k) B(n, k) over 32 k; a warp takes a group of 4
+// rows and 32 lanes x 4 columns, so A reads are broadcasts and B reads are conflict free
+// (row stride 129); each phase is exactly 32 row groups, two per warp.
 // A non-positive pivot records NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
 constexpr int PF_THREADS = 512;
+constexpr int PT = 32;             // leaf tile
+constexpr int PL = NB + 1;         // smem leading dimension
 
+// Column J of the leaf factorization (lane i holds row i of the tile in a[]):
+//   L_JJ = sqrt(a_JJ);  L_iJ = a_iJ / L_JJ;  a_il -= L_iJ L_lJ  for l in (J, i]
 template <int J>
-struct PotrfStep {
-  static __device__ __forceinline__ void run(float (&s)[4][8], float (&x)[4][8],
-                                             float *colbuf, float *rowbuf, int warp, int lane,
+struct LeafChol {
+  static __device__ __forceinline__ void run(float (&a)[PT], float &rdl, int lane, int t0,
                                              int &bad) {
-    constexpr int BJ = J % 8, AJ = J / 32, LJ = J % 32;
-    float *cb = colbuf + (J & 1) * NB;
-    float *rb = rowbuf + (J & 1) * NB;
-    if (warp == J / 8) {
+    const float piv = __shfl_sync(0xffffffffu, a[J], J);
+    const bool okp = piv > 0.0f;
+    if (!okp && bad < 0) bad = t0 + J;
+    const float rl = okp ? rsqrtf(piv) : 0.0f;
+    if (lane == J) rdl = rl;      // 1 / L_JJ, kept by the lane owning row J
+    const float lij = a[J] * rl;  // L[i][J] (lane J: sqrt(piv); lanes above: 0)
+    a[J] = lij;
 #pragma unroll
-      for (int a = 0; a < 4; ++a) cb[lane + 32 * a] = s[a][BJ];
+    for (int l = J + 1; l < PT; ++l) {
+      const float llj = __shfl_sync(0xffffffffu, lij, l);
+      if (lane >= l) a[l] = fmaf(-lij, llj, a[l]);
     }
-    if (lane == LJ) {
-#pragma unroll
-      for (int b = 0; b < 8; ++b) rb[8 * warp + b] = x[AJ][b];
-    }
-    __syncthreads();
-    const float piv = cb[J];
-    const bool okp = piv > 0.0f;  // false for NaN as well
-    if (!okp && bad < 0) bad = J;
-    const float rp = okp ? 1.0f / piv : 0.0f;
-    const float rl = okp ? 1.0f / sqrtf(piv) : 0.0f;
-    float ci[4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) ci[a] = cb[lane + 32 * a] * rp;
-    if (8 * warp + 7 > J) {  // this warp still has unfinished columns l > J
-      float cl[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) cl[b] = cb[8 * warp + b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int i = lane + 32 * a, l = 8 * warp + b;
-          if (l > J && i >= l) s[a][b] = fmaf(-ci[a], cl[b], s[a][b]);
-        }
-    }
-    if (8 * warp <= J) {  // B row J is zero beyond column J
-      float rc[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) rc[b] = rb[8 * warp + b];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int i = lane + 32 * a;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          if (i > J) x[a][b] = fmaf(-ci[a], rc[b], x[a][b]);
-          else if (i == J) x[a][b] = rc[b] * rl;
-        }
-      }
-    }
-    PotrfStep<J + 1>::run(s, x, colbuf, rowbuf, warp, lane, bad);
+    LeafChol<J + 1>::run(a, rdl, lane, t0, bad);
   }
 };
 template <>
-struct PotrfStep<NB> {
-  static __device__ __forceinline__ void run(float (&)[4][8], float (&)[4][8], float *, float *,
-                                             int, int, int &) {}
+struct LeafChol<PT> {
+  static __device__ __forceinline__ void run(float (&)[PT], float &, int, int, int &) {}
 };
 
-__global__ void __launch_bounds__(PF_THREADS)
+// Row I of the tile inverse for column c = lane:  x_I = (delta_Ic - sum_{l<I} L_Il x_l) / L_II
+template <int I>
+struct LeafInv {
+  static __device__ __forceinline__ void run(float (&x)[PT], const float *Lt, const float *rd,
+                                             int lane) {
+    float a0 = (I == lane) ? 1.0f : 0.0f, a1 = 0.0f;
+#pragma unroll
+    for (int l = 0; l < I; ++l) {
+      if (l & 1) a1 = fmaf(-Lt[I * PL + l], x[l], a1);
+      else a0 = fmaf(-Lt[I * PL + l], x[l], a0);
+    }
+    x[I] = (I < lane) ? 0.0f : (a0 + a1) * rd[I];
+    LeafInv<I + 1>::run(x, Lt, rd, lane);
+  }
+};
+template <>
+struct LeafInv<PT> {
+  static __device__ __forceinline__ void run(float (&)[PT], const float *, const float *, int) {}
+};
+
+// Factor + invert the 32 x 32 tile at (t0, t0) of S (lower part) into S and Li (tile
+// inverse, lower, at (t0, t0)), one warp.
+__device__ __forceinline__ void leaf_factor(float *S, float *Li, float *rd, int t0, int lane,
+                                            int &bad) {
+  float a[PT];
+#pragma unroll
+  for (int l = 0; l < PT; ++l) a[l] = (l <= lane) ? S[(t0 + lane) * PL + t0 + l] : 0.0f;
+  float rdl = 0.0f;
+  LeafChol<0>::run(a, rdl, lane, t0, bad);
+#pragma unroll
+  for (int l = 0; l < PT; ++l) S[(t0 + lane) * PL + t0 + l] = (l <= lane) ? a[l] : 0.0f;
+  rd[lane] = rdl;
+  __syncwarp();
+  float x[PT];
+  LeafInv<0>::run(x, S + t0 * PL + t0, rd, lane);
+#pragma unroll
+  for (int i = 0; i < PT; ++i) Li[(t0 + i) * PL + t0 + lane] = x[i];
+}
+
+// 4 rows (A rows m0..m0+3) x columns n = nb + lane + 32q (q < nq) of sum_k A(m,k) B(n,k),
+// k < 32.  A(m, k) = Am[m * PL + k], B(n, k) = Bm[n * PL + k].
+__device__ __forceinline__ void group_nt(const float *Am, const float *Bm, int m0, int nb,
+                                         int nq, int lane, float (&acc)[4][4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < PT; ++k) {
+    float a[4], b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = Am[(m0 + i) * PL + k];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = (q < nq) ? Bm[(nb + lane + 32 * q) * PL + k] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(a[i], b[q], acc[i][q]);
+  }
+}
+
+__global__ void __launch_bounds__(PF_THREADS, 1)
 potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatus *st) {
-  __shared__ float colbuf[2 * NB], rowbuf[2 * NB];
-  __shared__ int s_skip;
-  if (threadIdx.x == 0) s_skip = st->status != 0;
+  extern __shared__ float psm[];
+  float *S = psm;                // NB x PL: working block, becomes L (lower)
+  float *Bt = psm + NB * PL;     // NB x PL: transposed right-hand side -> Linv^T
+  float *Li = Bt + NB * PL;      // PT x PL: current leaf's tile inverse (rows P0.., cols 0..)
+  float *rd = Li + PT * PL;      // PT reciprocal pivots of the current leaf
+  __shared__ int s_skip, s_bad;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  if (tid == 0) { s_skip = st->status != 0; s_bad = -1; }
   __syncthreads();
   if (s_skip) return;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float s[4][8], x[4][8];
-  const bool vec = (d % 4 == 0);
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int i = lane + 32 * a;
-    const float *row = A + (k0 + i) * d + k0 + 8 * warp;
-    if (i < n && vec && 8 * warp + 8 <= n) {
-      const float4 u = *reinterpret_cast<const float4 *>(row);
-      const float4 v = *reinterpret_cast<const float4 *>(row + 4);
-      s[a][0] = u.x; s[a][1] = u.y; s[a][2] = u.z; s[a][3] = u.w;
-      s[a][4] = v.x; s[a][5] = v.y; s[a][6] = v.z; s[a][7] = v.w;
+  for (int e = tid; e < NB * NB / 4; e += PF_THREADS) {
+    const int i = e / (NB / 4), l4 = 4 * (e % (NB / 4));
+    float v[4];
+    if (i < n && (d % 4) == 0 && l4 + 4 <= n) {
+      const float4 u = *reinterpret_cast<const float4 *>(A + (k0 + i) * d + k0 + l4);
+      v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
     } else {
 #pragma unroll
-      for (int b = 0; b < 8; ++b) s[a][b] = (i < n && 8 * warp + b < n) ? row[b] : 0.0f;
+      for (int q = 0; q < 4; ++q) v[q] = (i < n && l4 + q < n) ? A[(k0 + i) * d + k0 + l4 + q] : 0.f;
     }
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int l = 8 * warp + b;
-      if (i >= n || l >= n) s[a][b] = (i == l) ? 1.0f : 0.0f;  // identity padding
-      x[a][b] = (i == l) ? 1.0f : 0.0f;
+    for (int q = 0; q < 4; ++q) {
+      const int l = l4 + q;
+      S[i * PL + l] = (i < n && l < n) ? v[q] : (i == l ? 1.0f : 0.0f);
+      Bt[i * PL + l] = (i == l) ? 1.0f : 0.0f;
     }
   }
+  __syncthreads();
   int bad = -1;
-  PotrfStep<0>::run(s, x, colbuf, rowbuf, warp, lane, bad);
-  if (bad >= 0) {
-    if (threadIdx.x == 0 && bad < n &&
-        atomicCAS(&st->status, 0, (int)GPTQ_ERR_NOT_PD) == 0)
-      st->info = (int)(k0 + bad) + 1;
+#pragma unroll 1
+  for (int p = 0; p < NB / PT; ++p) {
+    const int P0 = p * PT, R0 = P0 + PT;
+    if (warp == 0) {
+      // the leaf writes its tile inverse at rows P0.. of a PT x PL scratch (shifted)
+      leaf_factor(S, Li - P0 * PL - P0, rd, P0, lane, bad);
+      if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
+    }
+    __syncthreads();
+    // phase 1: 32 row groups of 4 rows: groups g < (NB-R0)/4 are rows R0 + 4g of S (trsm),
+    // the rest rows 4(g - (NB-R0)/4) of Bt (inverse step a); 32 output columns each.
+    const float *LiT = Li;  // Linv_pp rows (B operand): LiT[j * PL + t]
+    float res[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int g = warp + 16 * r;
+      const int ns = (NB - R0) / 4;
+      float acc[4][4];
+      const float *Am = (g < ns) ? (S + P0) : (Bt + P0);
+      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
+      group_nt(Am, LiT, m0, 0, 1, lane, acc);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) res[r][i] = acc[i][0];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int g = warp + 16 * r;
+      const int ns = (NB - R0) / 4;
+      float *Cm = (g < ns) ? (S + P0) : (Bt + P0);
+      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) Cm[(m0 + i) * PL + lane] = res[r][i];
+    }
+    __syncthreads();
+    // phase 2: syrk on S rows >= R0 (columns R0..row), inverse step b on Bt rows < R0
+    // (columns R0..NB-1)
+#pragma unroll 1
+    for (int r = 0; r < 2; ++r) {
+      const int g = warp + 16 * r;
+      const int ns = (NB - R0) / 4;
+      float acc[4][4];
+      if (g < ns) {
+        const int m0 = R0 + 4 * g;
+        const int nq = (m0 + 3 - R0) / 32 + 1;   // column blocks reaching the diagonal
+        group_nt(S + P0, S + P0, m0, R0, nq, lane, acc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = R0 + lane + 32 * q;
+            if (q < nq && col <= m0 + i) S[(m0 + i) * PL + col] -= acc[i][q];
+          }
+      } else {
+        const int m0 = 4 * (g - ns);
+        const int nq = (NB - R0) / 32;
+        if (nq > 0) {
+          group_nt(Bt + P0, S + P0, m0, R0, nq, lane, acc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q < nq) Bt[(m0 + i) * PL + R0 + lane + 32 * q] -= acc[i][q];
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (s_bad >= 0) {
+    if (tid == 0 && s_bad < n && atomicCAS(&st->status, 0, (int)GPTQ_ERR_NOT_PD) == 0)
+      st->info = (int)(k0 + s_bad) + 1;
     return;
   }
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int i = lane + 32 * a;
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int c = 8 * warp + b;
-      Linv[i * NB + c] = (i < n && c < n) ? x[a][b] : 0.0f;
-    }
+  // Linv[i][c] = Yt[c][i]
+  for (int e = tid; e < NB * NB; e += PF_THREADS) {
+    const int i = e / NB, c = e % NB;
+    Linv[e] = (i < n && c < n) ? Bt[c * PL + i] : 0.0f;
   }
 }
 
@@ -226,54 +321,82 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
 // TF32 head/tail split of Out into (hi, lo) panels (row r -> hi[r * NB + j]).
 // ---------------------------------------------------------------------------------------
 constexpr int RM_ROWS = 32, RM_THREADS = 256;
+constexpr int RML = NB + 4;  // smem leading dimension: float4 rows of 8 consecutive
+                             // threads fall in distinct bank groups
 
+// Thread (rg, cg) computes rows 4rg..4rg+3 x columns cg + 32q (q < 4) of the CTA's
+// 32 x 128 output block: per 4-wide K step, 8 float4 shared loads feed 64 FMAs.
 __global__ void __launch_bounds__(RM_THREADS)
 rowmul_kernel(const float *In, int64_t ldi, float *Out, int64_t ldo, int64_t r0, int64_t r1,
               const float *Bm, int n, float *hi, float *lo, const DevStatus *st) {
-  extern __shared__ float sm[];
-  float *Bs = sm;                 // NB x LDS
-  float *Is = sm + NB * LDS;      // RM_ROWS x LDS
+  extern __shared__ __align__(16) float sm[];
+  float *Bs = sm;                 // NB x RML: Bm rows (output column index, K)
+  float *Is = sm + NB * RML;      // RM_ROWS x RML: the CTA's input rows
   if (st->status != 0) return;
   const int tid = threadIdx.x;
   const int64_t rb = r0 + (int64_t)blockIdx.x * RM_ROWS;
-#pragma unroll 16
-  for (int it = 0; it < NB * NB / RM_THREADS; ++it) {
-    const int e = it * RM_THREADS + tid;
-    Bs[(e / NB) * LDS + e % NB] = Bm[e];
+#pragma unroll 4
+  for (int it = 0; it < NB * NB / 4 / RM_THREADS; ++it) {
+    const int e = it * RM_THREADS + tid;  // float4 index
+    const float4 v = reinterpret_cast<const float4 *>(Bm)[e];
+    *reinterpret_cast<float4 *>(Bs + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = v;
   }
-#pragma unroll 16
-  for (int it = 0; it < RM_ROWS * NB / RM_THREADS; ++it) {
+  const bool vec = (ldi % 4) == 0 && (((uintptr_t)In) % 16) == 0;
+#pragma unroll 4
+  for (int it = 0; it < RM_ROWS * NB / 4 / RM_THREADS; ++it) {
     const int e = it * RM_THREADS + tid;
-    const int r = e / NB, t = e % NB;
+    const int r = e / (NB / 4), t4 = 4 * (e % (NB / 4));
     const int64_t gr = rb + r;
-    Is[r * LDS + t] = (gr < r1 && t < n) ? In[gr * ldi + t] : 0.0f;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gr < r1) {
+      if (vec && t4 + 4 <= n) {
+        v = *reinterpret_cast<const float4 *>(In + gr * ldi + t4);
+      } else {
+        v.x = (t4 + 0 < n) ? In[gr * ldi + t4 + 0] : 0.f;
+        v.y = (t4 + 1 < n) ? In[gr * ldi + t4 + 1] : 0.f;
+        v.z = (t4 + 2 < n) ? In[gr * ldi + t4 + 2] : 0.f;
+        v.w = (t4 + 3 < n) ? In[gr * ldi + t4 + 3] : 0.f;
+      }
+    }
+    *reinterpret_cast<float4 *>(Is + r * RML + t4) = v;
   }
   __syncthreads();
-  // thread -> row (tid / 8), 16 columns j = (tid % 8) + 8 * u
-  const int r = tid / 8, jb = tid % 8;
-  float acc[16];
+  const int rg = tid / 32, cg = tid % 32;
+  float acc[4][4];
 #pragma unroll
-  for (int u = 0; u < 16; ++u) acc[u] = 0.f;
-  for (int t = 0; t < NB; ++t) {
-    const float a = Is[r * LDS + t];
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int u = 0; u < 16; ++u) acc[u] = fmaf(a, Bs[(jb + 8 * u) * LDS + t], acc[u]);
+    for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
+#pragma unroll 2
+  for (int t = 0; t < NB; t += 4) {
+    float4 a[4], b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Is + (4 * rg + i) * RML + t);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = *reinterpret_cast<const float4 *>(Bs + (cg + 32 * q) * RML + t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[i][q] = fmaf(a[i].x, b[q].x, acc[i][q]);
+        acc[i][q] = fmaf(a[i].y, b[q].y, acc[i][q]);
+        acc[i][q] = fmaf(a[i].z, b[q].z, acc[i][q]);
+        acc[i][q] = fmaf(a[i].w, b[q].w, acc[i][q]);
+      }
   }
-  const int64_t gr = rb + r;
-  if (gr < r1) {
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int j = jb + 8 * u;
-      if (j < n) {
-        if (Out) Out[gr * ldo + j] = acc[u];
-        if (hi) {
-          const float h = tf32_head(acc[u]);
-          hi[gr * NB + j] = h;
-          lo[gr * NB + j] = acc[u] - h;
-        }
-      } else if (hi) {
-        hi[gr * NB + j] = 0.f;
-        lo[gr * NB + j] = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    const int64_t gr = rb + 4 * rg + i;
+    if (gr >= r1) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = cg + 32 * q;
+      const float v = (j < n) ? acc[i][q] : 0.f;
+      if (Out && j < n) Out[gr * ldo + j] = v;
+      if (hi) {
+        const float h = tf32_head(v);
+        hi[gr * NB + j] = h;
+        lo[gr * NB + j] = v - h;
       }
     }
   }
@@ -327,8 +450,12 @@ size_t prepare_ws_bytes(int64_t d) {
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                            void *ws, cudaStream_t s) {
   static bool attr_done = false;
-  const size_t rm_smem = (NB + RM_ROWS) * LDS * sizeof(float);
+  const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);
+  const size_t potrf_smem = (2 * NB * PL + PT * PL + PT) * sizeof(float);
   if (!attr_done) {
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)potrf_smem));
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rm_smem));
@@ -346,7 +473,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   for (int64_t k0 = 0; k0 < d; k0 += NB) {
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
-    potrf_kernel<<<1, PF_THREADS, 0, s>>>(A, d, k0, n, w.Linv, w.st);
+    potrf_kernel<<<1, PF_THREADS, potrf_smem, s>>>(A, d, k0, n, w.Linv, w.st);
     GPTQ_LAUNCH_CHECK();
     // trsm: rows [k1, d) of panel k -> L panel (hi/lo) only (A's panel is not reused)
     if (k1 < d) {

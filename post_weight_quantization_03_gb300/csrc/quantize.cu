@@ -117,30 +117,34 @@ __global__ void diag_blocks_kernel(const float *__restrict__ U, int64_t d, int b
 }
 
 // ---------------------------------------------------------------------------------------
-// One column step of the in-block sweep, unrolled at compile time over the block so the
-// row's working weights stay in registers:
+// One column step of the in-block sweep within a 32-column sub-block, unrolled at compile
+// time over the sub-block so its working weights stay in registers:
 //   code = clamp(rint(w_J / s) + z, 0, maxq);  q = s (code - z);  e = (w_J - q) / U_JJ
-//   w_k -= e U_Jk  for k > J inside the block.
+//   w_k -= e U_Jk  for the later columns k of the sub-block.
+// The same 32-step code serves all four sub-blocks of a block (runtime loop), which keeps
+// the kernel inside the instruction cache.
 // ---------------------------------------------------------------------------------------
+constexpr int SUB = 32;
+
 template <int J>
 struct SweepStep {
-  static __device__ __forceinline__ void run(float (&w)[SB], uint32_t (&cw)[SB / 4],
-                                             const float *Us, const float *rdiag, float s,
+  static __device__ __forceinline__ void run(float (&w)[SUB], uint32_t (&cw)[SUB / 4],
+                                             const float *Ub, const float *rd, float s,
                                              float z, float maxq) {
     const float x = __fdiv_rn(w[J], s);
     const float c = fminf(fmaxf(rintf(x) + z, 0.0f), maxq);
     const float q = s * (c - z);
-    const float e = (w[J] - q) * rdiag[J];
+    const float e = (w[J] - q) * rd[J];
     cw[J / 4] |= (uint32_t)c << (8 * (J % 4));
     w[J] = e;  // the register now holds the scaled error of column J
 #pragma unroll
-    for (int k = J + 1; k < SB; ++k) w[k] = fmaf(-e, Us[J * LDU + k], w[k]);
-    SweepStep<J + 1>::run(w, cw, Us, rdiag, s, z, maxq);
+    for (int k = J + 1; k < SUB; ++k) w[k] = fmaf(-e, Ub[J * LDU + k], w[k]);
+    SweepStep<J + 1>::run(w, cw, Ub, rd, s, z, maxq);
   }
 };
 template <>
-struct SweepStep<SB> {
-  static __device__ __forceinline__ void run(float (&)[SB], uint32_t (&)[SB / 4],
+struct SweepStep<SUB> {
+  static __device__ __forceinline__ void run(float (&)[SUB], uint32_t (&)[SUB / 4],
                                              const float *, const float *, float, float,
                                              float) {}
 };
@@ -202,46 +206,64 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   const int64_t row = r0 + tid;
   const float s = row < m ? scale[row] : 1.f;
   const float z = row < m ? (float)zero[row] : 0.f;
-  float w[SB];
+  float *my = stage + tid * LDW;           // this thread's row of the block
+  uint32_t *cstage = (uint32_t *)(stage + SW_ROWS * LDW);  // SW_ROWS x (SB/4 + 1) words
+#pragma unroll 1
+  for (int sb = 0; sb < SB / SUB; ++sb) {
+    const int c0 = sb * SUB;
+    float w[SUB];
 #pragma unroll
-  for (int q = 0; q < SB / 4; ++q) {
-    const float4 v = *reinterpret_cast<const float4 *>(stage + tid * LDW + 4 * q);
-    w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-  }
-  uint32_t cw[SB / 4];  // codes, 4 per word (byte j%4 of word j/4)
+    for (int q = 0; q < SUB / 4; ++q) {
+      const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
+      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+    uint32_t cw[SUB / 4];
 #pragma unroll
-  for (int i = 0; i < SB / 4; ++i) cw[i] = 0u;
-  SweepStep<0>::run(w, cw, Us, rdiag, s, z, maxq);
-  // stage E (own row), then store coalesced as head/tail
+    for (int i = 0; i < SUB / 4; ++i) cw[i] = 0u;
+    SweepStep<0>::run(w, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
+    // errors replace the consumed weights; codes go to their own staging area
 #pragma unroll
-  for (int q = 0; q < SB / 4; ++q) {
-    float4 v = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-    if (4 * q + 0 >= nb) v.x = 0.f;
-    if (4 * q + 1 >= nb) v.y = 0.f;
-    if (4 * q + 2 >= nb) v.z = 0.f;
-    if (4 * q + 3 >= nb) v.w = 0.f;
-    *reinterpret_cast<float4 *>(stage + tid * LDW + 4 * q) = v;
+    for (int q = 0; q < SUB / 4; ++q)
+      *reinterpret_cast<float4 *>(my + c0 + 4 * q) =
+          make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+#pragma unroll
+    for (int i = 0; i < SUB / 4; ++i) cstage[tid * (SB / 4 + 1) + sb * (SUB / 4) + i] = cw[i];
+    // the sub-block's errors update the later columns of the block:
+    //   w_c -= sum_k e_k U[c0 + k][c]
+#pragma unroll 1
+    for (int c = c0 + SUB; c < SB; c += 4) {
+      float4 acc = *reinterpret_cast<const float4 *>(my + c);
+#pragma unroll
+      for (int k = 0; k < SUB; ++k) {
+        const float4 u = *reinterpret_cast<const float4 *>(Us + (c0 + k) * LDU + c);
+        acc.x = fmaf(-w[k], u.x, acc.x);
+        acc.y = fmaf(-w[k], u.y, acc.y);
+        acc.z = fmaf(-w[k], u.z, acc.z);
+        acc.w = fmaf(-w[k], u.w, acc.w);
+      }
+      *reinterpret_cast<float4 *>(my + c) = acc;
+    }
   }
   __syncthreads();
+  // E (now in the stage rows) -> global as a TF32 head/tail pair, coalesced
 #pragma unroll 8
   for (int it = 0; it < SB / 4; ++it) {
     const int e = it * SW_ROWS + tid;
     const int r = e / (SB / 4), q = e % (SB / 4);
     const int64_t gr = r0 + r;
     if (gr < m) {
-      const float4 v = *reinterpret_cast<const float4 *>(stage + r * LDW + 4 * q);
+      float4 v = *reinterpret_cast<const float4 *>(stage + r * LDW + 4 * q);
+      if (4 * q + 0 >= nb) v.x = 0.f;
+      if (4 * q + 1 >= nb) v.y = 0.f;
+      if (4 * q + 2 >= nb) v.z = 0.f;
+      if (4 * q + 3 >= nb) v.w = 0.f;
       const float4 h = make_float4(tf32_head(v.x), tf32_head(v.y), tf32_head(v.z), tf32_head(v.w));
       *reinterpret_cast<float4 *>(Ehi + gr * SB + 4 * q) = h;
       *reinterpret_cast<float4 *>(Elo + gr * SB + 4 * q) =
           make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
     }
   }
-  __syncthreads();
-  // codes: stage as bytes, store coalesced
-  uint32_t *cstage = (uint32_t *)stage;  // SW_ROWS x (SB/4 + 1) words
-#pragma unroll
-  for (int i = 0; i < SB / 4; ++i) cstage[tid * (SB / 4 + 1) + i] = cw[i];
-  __syncthreads();
+  // codes: staged as bytes, stored coalesced
   const uint8_t *cb = (const uint8_t *)cstage;
   for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
     const int r = e / SB, j = e % SB;
@@ -329,7 +351,7 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
                             uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
                             void *ws, cudaStream_t s) {
   static bool attr_done = false;
-  const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW) * sizeof(float);
+  const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -8,10 +8,13 @@
 // One CTA per 128 x 128 output tile; warp roles:
 //   warp 0      : TMA producer (one lane): 4 operand tiles per 32-wide K stage
 //   warp 1      : TMEM allocator + MMA issuer (one lane)
-//   warps 2..5  : epilogue: TMEM -> registers -> C read-modify-write
+//   warps 2..5  : epilogue: TMEM -> registers -> alpha * acc staged in shared memory in
+//                 the 128-byte-swizzled box layout -> TMA reduce-add into C (the add
+//                 happens in L2); plain read-modify-write when C is not 16-byte aligned
 // Stages live in a ring of kStages shared-memory buffers guarded by full/empty
 // mbarriers; every wait is bounded (tc.cuh).
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "tc.cuh"
 
@@ -35,13 +38,15 @@ struct TcGemmParams {
   float *c; int64_t ldc;
   float alpha;
   int lower_only, trans_c;
+  int tma_c;            // 1: epilogue through the C tensor map (reduce-add)
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
                       const __grid_constant__ CUtensorMap ma_lo,
                       const __grid_constant__ CUtensorMap mb_hi,
-                      const __grid_constant__ CUtensorMap mb_lo, TcGemmParams p,
+                      const __grid_constant__ CUtensorMap mb_lo,
+                      const __grid_constant__ CUtensorMap mc, TcGemmParams p,
                       DevStatus *st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -128,7 +133,34 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
     __syncwarp();
     tc::tc_fence_after();
     const int64_t row = m0 + q * 32 + lane;
-    if (ok && ktiles > 0) {
+    if (ok && ktiles > 0 && p.tma_c) {
+      // every stage buffer is free once `done` fired: reuse stage 0 (4 boxes of 32 cols)
+      const int rl = q * 32 + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+        tc::tmem_ld_wait();
+        uint8_t *rowp = smem + (c0 / 32) * (BM * 128) + rl * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 v = make_float4(p.alpha * __uint_as_float(r[4 * u]),
+                                       p.alpha * __uint_as_float(r[4 * u + 1]),
+                                       p.alpha * __uint_as_float(r[4 * u + 2]),
+                                       p.alpha * __uint_as_float(r[4 * u + 3]));
+          *reinterpret_cast<float4 *>(rowp + ((u ^ (rl & 7)) * 16)) = v;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::named_barrier(1, 128);  // the four epilogue warps
+      if (warp == 2 && lane == 0) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + 32 * c), (int32_t)m0, smem + c * (BM * 128));
+        tc::bulk_commit();
+        tc::bulk_wait_read_all();
+      }
+    } else if (ok && ktiles > 0) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
@@ -207,13 +239,17 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
       !make_tmap_f32(&mbh, g.b_hi, g.N, g.K, g.ldb, BN) ||
       !make_tmap_f32(&mbl, g.b_lo, g.N, g.K, g.ldb, BN))
     return GPTQ_ERR_UNSUPPORTED;
+  CUtensorMap mc;
+  memset(&mc, 0, sizeof(mc));
+  const bool tma_c = !g.trans_c && make_tmap_f32(&mc, g.c, g.M, g.N, g.ldc, BM);
   TcGemmParams p{};
+  p.tma_c = tma_c ? 1 : 0;
   p.a_k0 = 0; p.a_m0 = 0; p.b_k0 = 0; p.b_n0 = 0;
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.c = g.c; p.ldc = g.ldc; p.alpha = g.alpha;
   p.lower_only = g.lower_only; p.trans_c = g.trans_c;
   dim3 grid((unsigned)ceil_div(g.N, BN), (unsigned)ceil_div(g.M, BM));
-  tc_gemm_3xtf32_kernel<<<grid, kThreads, kSmemBytes, s>>>(mah, mal, mbh, mbl, p, st);
+  tc_gemm_3xtf32_kernel<<<grid, kThreads, kSmemBytes, s>>>(mah, mal, mbh, mbl, mc, p, st);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
