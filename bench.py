@@ -69,6 +69,24 @@ def whole_job_value(weights_per_rank, world, ms_step):
     return world * weights_per_rank / (ms_step / 1e3)
 
 
+def profiled_traffic(n_tok):
+    """DRAM bytes per Hessian launch from the committed ncu summary, or None when the
+    kernel source changed since the capture or the token count differs."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "hessian_tc_layer4096.md")
+    src = os.path.join(ROOT, "post_weight_quantization_03_gb300", "csrc", "hessian.cu")
+    try:
+        text = open(prof).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    fields = dict(line.split(": ", 1) for line in text.splitlines()
+                  if line.startswith(("traffic_bytes_per_launch_262144:", "source_sha256_16:")))
+    if fields.get("source_sha256_16:".rstrip(":"), "").strip() != digest or n_tok != 262144:
+        return None
+    return int(fields["traffic_bytes_per_launch_262144"])
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -279,7 +297,9 @@ def main():
     peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     roofline = {"kernel": "hessian (gptq_hessian_accumulate)", "bound": "tensor",
                 "achieved": round(h_tflops, 3), "peak": peak_t, "unit": "TFLOP/s",
-                "frac": round(h_tflops / peak_t, 4), "traffic": None,
+                "frac": round(h_tflops / peak_t, 4), "traffic": profiled_traffic(n),
+                "traffic_unit": "bytes per launch (dram read + write, ncu, scaled from a "
+                                "65536-token capture; profiles/hessian_tc_layer4096.md)",
                 "algorithmic": f"d(d+1)N = {h_flops:.4e} flop per launch (lower triangle of "
                                f"2 X^T X incl. diagonal)",
                 "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"}
