@@ -38,7 +38,10 @@ import numpy as np
 __all__ = [
     "NotPositiveDefinite",
     "hessian",
+    "hessian_block",
+    "hessian_diagonal",
     "damp_hessian",
+    "damp_principal_block",
     "inverse_cholesky_upper",
     "row_grid",
     "quantize_to_grid",
@@ -79,9 +82,43 @@ def hessian(X, H=None):
     return np.asarray(H, dtype=np.float64) + G
 
 
+def hessian_block(X, rows, cols):
+    """The block ``H[rows][:, cols]`` of ``2 X^T X`` without forming the rest of H."""
+    X = np.asarray(X)
+    return 2.0 * (X[:, rows].astype(np.float64).T @ X[:, cols].astype(np.float64))
+
+
+def hessian_diagonal(X, chunk=8192):
+    """The diagonal of ``2 X^T X``: twice each channel's sum of squares (token chunks)."""
+    X = np.asarray(X)
+    out = np.zeros(X.shape[1], dtype=np.float64)
+    for t0 in range(0, X.shape[0], chunk):
+        Xc = X[t0:t0 + chunk].astype(np.float64)
+        out += np.einsum("ti,ti->i", Xc, Xc)
+    return 2.0 * out
+
+
 # ---------------------------------------------------------------------------------------
 # Step 2: dead columns and damping
 # ---------------------------------------------------------------------------------------
+
+def damp_principal_block(H_block, diag_full, idx, damp=0.01):
+    """Dead-column fix and damping of the principal block ``H[idx][:, idx]`` of a Hessian
+    whose full diagonal is ``diag_full``; returns ``(H_block_damped, dead_full, lam)``.
+
+    Same rule as :func:`damp_hessian` (lam from the mean of the whole dead-fixed diagonal),
+    restricted to the rows and columns ``idx``.
+    """
+    diag_full = np.asarray(diag_full, dtype=np.float64)
+    dead = diag_full == 0.0
+    lam = float(damp) * float(np.mean(np.where(dead, 1.0, diag_full)))
+    Hb = np.array(H_block, dtype=np.float64, copy=True)
+    idx = np.asarray(idx)
+    sub_dead = np.flatnonzero(dead[idx])
+    Hb[sub_dead, sub_dead] = 1.0
+    Hb[np.diag_indices_from(Hb)] += lam
+    return Hb, dead, lam
+
 
 def damp_hessian(H, damp=0.01):
     """Dead-column fix and diagonal damping; returns ``(H_damped, dead, lam)``.

@@ -160,6 +160,24 @@ def weights(d_out: int, d_in: int, std: float, dtype: str, seed: int,
     return W.to(_DTYPES[dtype])
 
 
+def upper_factor(d: int, seed: int, coupling: float = 0.5, device="cpu") -> torch.Tensor:
+    """A seeded upper-triangular ``[d, d]`` float32 matrix with positive diagonal: a valid
+    inverse-Hessian factor input for the sweep at sizes where no Hessian is factored for it
+    (any such U is the upper Cholesky factor of the inverse of the SPD matrix (U^T U)^-1).
+
+    Diagonal ``exp(N(0, 0.25))``, strictly upper entries ``coupling * N(0, 1) / sqrt(d)``
+    scaled by their row's diagonal.
+    """
+    g = _gen(device, _seed(seed, "A", 7))
+    diag = torch.exp(0.5 * torch.randn(d, generator=g, device=device, dtype=torch.float32))
+    U = torch.randn(d, d, generator=g, device=device, dtype=torch.float32)
+    U.mul_(coupling / math.sqrt(d))
+    U = torch.triu(U, diagonal=1)
+    U.mul_(diag[:, None])
+    U.diagonal().copy_(diag)
+    return U
+
+
 def layer_weights(layer: LayerSpec, device="cpu") -> torch.Tensor:
     return weights(layer.d_out, layer.act.d_in, layer.w_std, layer.w_dtype,
                    layer.act.seed * 131 + layer.w_seed, device)

@@ -310,3 +310,42 @@ def test_pack_roundtrip_random(bits):
     rng = np.random.default_rng(bits)
     codes = rng.integers(0, 2 ** bits, size=(7, 101))
     np.testing.assert_array_equal(O.unpack_codes(O.pack_codes(codes, bits), bits, 101), codes)
+
+
+# ---------------------------------------------------------------------------------------
+# Block helpers used by the full-size GPU checks
+# ---------------------------------------------------------------------------------------
+
+def test_hessian_block_and_diagonal_match_full():
+    rng = np.random.default_rng(15)
+    ints = rng.integers(-512, 512, size=(300, 40))
+    ints[:, 7] = 0                                   # a dead channel
+    X = (ints * 2.0 ** -6).astype(np.float16)
+    H = O.hessian(X)
+    rows, cols = np.array([3, 7, 39]), np.arange(20, 40)
+    np.testing.assert_array_equal(O.hessian_block(X, rows, cols), H[np.ix_(rows, cols)])
+    np.testing.assert_array_equal(O.hessian_diagonal(X, chunk=64), np.diag(H))
+    # exact against integers
+    np.testing.assert_array_equal(O.hessian_diagonal(X), 2.0 * (ints ** 2).sum(0) * 2.0 ** -12)
+
+
+def test_damped_principal_block_matches_full_damping():
+    X, _ = correlated_problem(4, 30, 60, 16, dead=(2, 25))
+    H = O.hessian(X)
+    Hd, dead, lam = O.damp_hessian(H, 0.01)
+    idx = np.arange(20, 30)
+    Hb, dead_b, lam_b = O.damp_principal_block(H[np.ix_(idx, idx)], np.diag(H), idx, 0.01)
+    assert lam_b == lam and np.array_equal(dead_b, dead)
+    np.testing.assert_array_equal(Hb, Hd[np.ix_(idx, idx)])
+
+
+@pytest.mark.parametrize("t", [1, 5, 17])
+def test_trailing_block_of_u_depends_only_on_trailing_block_of_h(t):
+    # H^-1 = U^T U with U upper  =>  H = R R^T, R = U^-1 upper  =>  H[t:, t:] = R22 R22^T,
+    # so U[t:, t:] is the factor of H[t:, t:] alone: this lets a full-size GPU factor be
+    # checked on a trailing block the oracle can afford.
+    X, _ = correlated_problem(4, 24, 50, 17, dead=(20,))
+    Hd, _, _ = O.damp_hessian(O.hessian(X))
+    U = O.inverse_cholesky_upper(Hd)
+    Ut = O.inverse_cholesky_upper(Hd[t:, t:])
+    np.testing.assert_allclose(U[t:, t:], Ut, rtol=0, atol=1e-12 * np.abs(U).max())
