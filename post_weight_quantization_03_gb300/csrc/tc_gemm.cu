@@ -5,14 +5,19 @@
 // tensor core accumulates head_A head_B^T + head_A tail_B^T + tail_A head_B^T into an fp32
 // TMEM accumulator, which reproduces fp32 products to about 2^-21 relative.
 //
-// One CTA per 128 x 128 output tile; warp roles:
-//   warp 0      : TMA producer (one lane): 4 operand tiles per 32-wide K stage
-//   warp 1      : TMEM allocator + MMA issuer (one lane)
+// Persistent: each CTA walks a static list of 128 x 128 output tiles; warp roles:
+//   warp 0      : TMA producer (one lane): 4 operand tiles per 32-wide K stage, running
+//                 ahead across tile boundaries through a 3-stage ring
+//   warp 1      : TMEM allocator + MMA issuer (one lane), alternating between two
+//                 128-column TMEM accumulators so the next tile's MMAs overlap this
+//                 tile's epilogue
 //   warps 2..5  : epilogue: TMEM -> registers -> alpha * acc staged in shared memory in
-//                 the 128-byte-swizzled box layout -> TMA reduce-add into C (the add
-//                 happens in L2); plain read-modify-write when C is not 16-byte aligned
-// Stages live in a ring of kStages shared-memory buffers guarded by full/empty
-// mbarriers; every wait is bounded (tc.cuh).
+//                 the 128-byte-swizzled box layout (two 64-column halves) -> TMA
+//                 reduce-add into C (the add happens in L2, so concurrent updates of
+//                 the same C are safe); plain read-modify-write when C is not 16-byte
+//                 aligned
+// Every mbarrier wait is bounded (tc.cuh); the epilogue's wait is taken by one leader
+// thread and broadcast, so all four epilogue warps leave their loop together.
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -28,18 +33,34 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTileA = BM * BK * 4;  // 16 KB
 constexpr uint32_t kTileB = BN * BK * 4;  // 16 KB
 constexpr uint32_t kStageBytes = 2 * kTileA + 2 * kTileB;
-constexpr uint32_t kTmemCols = BN;  // fp32 accumulator: one column per output column
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
+constexpr uint32_t kStagingBytes = 2 * BM * 128;  // two 32-column boxes (one 64-col half)
+constexpr uint32_t kTmemCols = 2 * BN;            // two accumulators
+constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 
 struct TcGemmParams {
-  int32_t a_k0, a_m0;   // coordinates of A(0, 0) in its tensor map (x = k, y = row)
-  int32_t b_k0, b_n0;   // coordinates of B(0, 0)
   int64_t M, N, K;
   float *c; int64_t ldc;
   float alpha;
-  int lower_only, trans_c;
+  int lower_only;
   int tma_c;            // 1: epilogue through the C tensor map (reduce-add)
+  int n_m, n_n;         // tile grid
+  int n_tiles;          // tiles to process (lower ones only when lower_only)
 };
+
+// Linear tile index -> (tm, tn): row-major over the tile grid, or over its lower
+// triangle (tm >= tn) when lower_only.
+__device__ __forceinline__ void tile_coords(const TcGemmParams &p, int t, int &tm, int &tn) {
+  if (p.lower_only) {
+    int r = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
+    while (r * (r + 1) / 2 > t) --r;
+    while ((r + 1) * (r + 2) / 2 <= t) ++r;
+    tm = r;
+    tn = t - r * (r + 1) / 2;
+  } else {
+    tm = t / p.n_n;
+    tn = t % p.n_n;
+  }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
@@ -50,19 +71,19 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
                       DevStatus *st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t *full = (uint64_t *)(smem + kStages * kStageBytes);
+  uint8_t *staging = smem + kStages * kStageBytes;
+  uint64_t *full = (uint64_t *)(staging + kStagingBytes);
   uint64_t *empty = full + kStages;
-  uint64_t *done = empty + kStages;
-  uint32_t *tmem_slot = (uint32_t *)(done + 1);
+  uint64_t *tfull = empty + kStages;   // [2] accumulator ready
+  uint64_t *tempty = tfull + 2;        // [2] accumulator drained
+  uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+  int *epi_ok = (int *)(tmem_slot + 1);
 
   __shared__ int s_skip;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tile_m = blockIdx.y, tile_n = blockIdx.x;
-  if (threadIdx.x == 0)
-    s_skip = (st && st->status != 0) || (p.lower_only && tile_m < tile_n);
+  if (threadIdx.x == 0) s_skip = (st && st->status != 0);
   __syncthreads();
   if (s_skip) return;  // uniform for the whole CTA, before any barrier or TMEM use
-  const int64_t m0 = (int64_t)tile_m * BM, n0 = (int64_t)tile_n * BN;
   const int ktiles = (int)((p.K + BK - 1) / BK);
 
   if (threadIdx.x == 0) {
@@ -70,7 +91,10 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
     tc::mbar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -85,99 +109,127 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
     tc::tma_prefetch_desc(&ma_lo);
     tc::tma_prefetch_desc(&mb_hi);
     tc::tma_prefetch_desc(&mb_lo);
-    for (int kt = 0; kt < ktiles; ++kt) {
-      const int s = kt % kStages;
-      if (kt >= kStages && !tc::mbar_wait(&empty[s], ((kt / kStages) - 1) & 1, st)) break;
-      uint8_t *base = smem + s * kStageBytes;
-      tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
-      const int32_t ka = p.a_k0 + kt * BK, kb = p.b_k0 + kt * BK;
-      tc::tma_load_2d(base, &ma_hi, ka, p.a_m0 + (int32_t)m0, &full[s]);
-      tc::tma_load_2d(base + kTileA, &ma_lo, ka, p.a_m0 + (int32_t)m0, &full[s]);
-      tc::tma_load_2d(base + 2 * kTileA, &mb_hi, kb, p.b_n0 + (int32_t)n0, &full[s]);
-      tc::tma_load_2d(base + 2 * kTileA + kTileB, &mb_lo, kb, p.b_n0 + (int32_t)n0, &full[s]);
+    int g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(p, t, tm, tn);
+      const int32_t m0 = tm * BM, n0 = tn * BN;
+      for (int kt = 0; kt < ktiles; ++kt, ++g) {
+        const int s = g % kStages;
+        if (g >= kStages && !tc::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, st)) {
+          ok = false;
+          break;
+        }
+        uint8_t *base = smem + s * kStageBytes;
+        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+        const int32_t k0 = kt * BK;
+        tc::tma_load_2d(base, &ma_hi, k0, m0, &full[s]);
+        tc::tma_load_2d(base + kTileA, &ma_lo, k0, m0, &full[s]);
+        tc::tma_load_2d(base + 2 * kTileA, &mb_hi, k0, n0, &full[s]);
+        tc::tma_load_2d(base + 2 * kTileA + kTileB, &mb_lo, k0, n0, &full[s]);
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
+    int g = 0, it = 0;
     bool ok = true;
-    for (int kt = 0; kt < ktiles && ok; ++kt) {
-      const int s = kt % kStages;
-      ok = tc::mbar_wait(&full[s], (kt / kStages) & 1, st);
-      if (!ok) break;
-      tc::tc_fence_after();
-      const uint32_t a_hi = tc::smem_u32(smem + s * kStageBytes);
-      const uint32_t a_lo = a_hi + kTileA;
-      const uint32_t b_hi = a_hi + 2 * kTileA;
-      const uint32_t b_lo = b_hi + kTileB;
-#pragma unroll
-      for (int kk = 0; kk < BK / 8; ++kk) {  // 8 tf32 = 32 bytes per MMA
-        const uint32_t off = kk * 32;
-        const uint64_t dah = tc::smem_desc_sw128(a_hi + off, 16, 1024);
-        const uint64_t dal = tc::smem_desc_sw128(a_lo + off, 16, 1024);
-        const uint64_t dbh = tc::smem_desc_sw128(b_hi + off, 16, 1024);
-        const uint64_t dbl = tc::smem_desc_sw128(b_lo + off, 16, 1024);
-        const uint32_t acc0 = (kt > 0 || kk > 0) ? 1u : 0u;
-        tc::mma_tf32(tmem, dah, dbh, idesc, acc0);
-        tc::mma_tf32(tmem, dah, dbl, idesc, 1u);
-        tc::mma_tf32(tmem, dal, dbh, idesc, 1u);
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      if (it >= 2) {
+        ok = tc::mbar_wait(&tempty[b], ((it / 2) - 1) & 1, st);
+        if (!ok) break;
+        tc::tc_fence_after();
       }
-      tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+      const uint32_t dt = tmem + (uint32_t)(b * BN);
+      for (int kt = 0; kt < ktiles; ++kt, ++g) {
+        const int s = g % kStages;
+        ok = tc::mbar_wait(&full[s], (g / kStages) & 1, st);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t a_hi = tc::smem_u32(smem + s * kStageBytes);
+        const uint32_t a_lo = a_hi + kTileA;
+        const uint32_t b_hi = a_hi + 2 * kTileA;
+        const uint32_t b_lo = b_hi + kTileB;
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {  // 8 tf32 = 32 bytes per MMA
+          const uint32_t off = kk * 32;
+          const uint64_t dah = tc::smem_desc_sw128(a_hi + off, 16, 1024);
+          const uint64_t dal = tc::smem_desc_sw128(a_lo + off, 16, 1024);
+          const uint64_t dbh = tc::smem_desc_sw128(b_hi + off, 16, 1024);
+          const uint64_t dbl = tc::smem_desc_sw128(b_lo + off, 16, 1024);
+          const uint32_t acc0 = (kt > 0 || kk > 0) ? 1u : 0u;
+          tc::mma_tf32(dt, dah, dbh, idesc, acc0);
+          tc::mma_tf32(dt, dah, dbl, idesc, 1u);
+          tc::mma_tf32(dt, dal, dbh, idesc, 1u);
+        }
+        tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+      }
+      tc::mma_commit(&tfull[b]);    // accumulator complete (or abandoned after a timeout)
     }
-    tc::mma_commit(done);  // accumulator complete (or abandoned after a timeout)
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int okl = 0;
-    if (lane == 0) okl = tc::mbar_wait(done, 0, st) ? 1 : 0;
-    const bool ok = __shfl_sync(0xffffffffu, okl, 0) != 0;  // warp-uniform
-    __syncwarp();
-    tc::tc_fence_after();
-    const int64_t row = m0 + q * 32 + lane;
-    if (ok && ktiles > 0 && p.tma_c) {
-      // every stage buffer is free once `done` fired: reuse stage 0 (4 boxes of 32 cols)
-      const int rl = q * 32 + lane;
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int rl = q * 32 + lane;      // row within the tile
+    const bool leader = (warp == 2 && lane == 0);
+    int it = 0;
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      if (leader) *epi_ok = tc::mbar_wait(&tfull[b], (it / 2) & 1, st) ? 1 : 0;
+      tc::named_barrier(1, 128);
+      if (!*epi_ok) break;             // same value for all four warps
+      tc::tc_fence_after();
+      int tm, tn;
+      tile_coords(p, t, tm, tn);
+      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
+      const int64_t row = m0 + rl;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32];
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + h * 64);
+        tc::tmem_ld32(ta, r0);
+        tc::tmem_ld32(ta + 32, r1);
         tc::tmem_ld_wait();
-        uint8_t *rowp = smem + (c0 / 32) * (BM * 128) + rl * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 v = make_float4(p.alpha * __uint_as_float(r[4 * u]),
-                                       p.alpha * __uint_as_float(r[4 * u + 1]),
-                                       p.alpha * __uint_as_float(r[4 * u + 2]),
-                                       p.alpha * __uint_as_float(r[4 * u + 3]));
-          *reinterpret_cast<float4 *>(rowp + ((u ^ (rl & 7)) * 16)) = v;
+        if (h == 1) {  // this warp's reads of the accumulator are done: release it
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[b]);
         }
-      }
-      tc::fence_proxy_async_smem();
-      tc::named_barrier(1, 128);  // the four epilogue warps
-      if (warp == 2 && lane == 0) {
+        if (p.tma_c) {
+          uint8_t *rowp0 = staging + rl * 128;
+          uint8_t *rowp1 = staging + BM * 128 + rl * 128;
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + 32 * c), (int32_t)m0, smem + c * (BM * 128));
-        tc::bulk_commit();
-        tc::bulk_wait_read_all();
-      }
-    } else if (ok && ktiles > 0) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
-        tc::tmem_ld_wait();
-        if (row < p.M) {
+          for (int u = 0; u < 8; ++u) {
+            const int su = (u ^ (rl & 7)) * 16;
+            *reinterpret_cast<float4 *>(rowp0 + su) =
+                make_float4(p.alpha * __uint_as_float(r0[4 * u]), p.alpha * __uint_as_float(r0[4 * u + 1]),
+                            p.alpha * __uint_as_float(r0[4 * u + 2]), p.alpha * __uint_as_float(r0[4 * u + 3]));
+            *reinterpret_cast<float4 *>(rowp1 + su) =
+                make_float4(p.alpha * __uint_as_float(r1[4 * u]), p.alpha * __uint_as_float(r1[4 * u + 1]),
+                            p.alpha * __uint_as_float(r1[4 * u + 2]), p.alpha * __uint_as_float(r1[4 * u + 3]));
+          }
+          tc::fence_proxy_async_smem();
+          tc::named_barrier(1, 128);
+          if (leader) {
+            tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + h * 64), (int32_t)m0, staging);
+            tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + h * 64 + 32), (int32_t)m0,
+                                  staging + BM * 128);
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();  // staging may be overwritten after the next barrier
+          }
+          tc::named_barrier(1, 128);
+        } else if (row < p.M) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int64_t col = n0 + c0 + i;
-            if (col < p.N) {
-              float *ptr = p.trans_c ? &p.c[col * p.ldc + row] : &p.c[row * p.ldc + col];
-              *ptr = fmaf(p.alpha, __uint_as_float(r[i]), *ptr);
-            }
+            const int64_t c0 = n0 + h * 64 + i, c1 = c0 + 32;
+            if (c0 < p.N) p.c[row * p.ldc + c0] = fmaf(p.alpha, __uint_as_float(r0[i]), p.c[row * p.ldc + c0]);
+            if (c1 < p.N) p.c[row * p.ldc + c1] = fmaf(p.alpha, __uint_as_float(r1[i]), p.c[row * p.ldc + c1]);
           }
         }
       }
     }
+    if (leader) tc::bulk_wait_all();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -242,13 +294,22 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   CUtensorMap mc;
   memset(&mc, 0, sizeof(mc));
   const bool tma_c = !g.trans_c && make_tmap_f32(&mc, g.c, g.M, g.N, g.ldc, BM);
+  if (g.trans_c) return GPTQ_ERR_UNSUPPORTED;
+  static int num_sms = 0;
+  if (!num_sms) {
+    int dev = 0;
+    GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+    GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  }
   TcGemmParams p{};
   p.tma_c = tma_c ? 1 : 0;
-  p.a_k0 = 0; p.a_m0 = 0; p.b_k0 = 0; p.b_n0 = 0;
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.c = g.c; p.ldc = g.ldc; p.alpha = g.alpha;
-  p.lower_only = g.lower_only; p.trans_c = g.trans_c;
-  dim3 grid((unsigned)ceil_div(g.N, BN), (unsigned)ceil_div(g.M, BM));
+  p.n_m = (int)ceil_div(g.M, BM);
+  p.n_n = (int)ceil_div(g.N, BN);
+  p.lower_only = g.lower_only && g.M == g.N;
+  p.n_tiles = p.lower_only ? p.n_n * (p.n_n + 1) / 2 : p.n_m * p.n_n;
+  const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
   tc_gemm_3xtf32_kernel<<<grid, kThreads, kSmemBytes, s>>>(mah, mal, mbh, mbl, mc, p, st);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
