@@ -16,6 +16,7 @@
 // where Bt is the transposed right-hand side of L Y = I, updated in place into Yt.
 // Finally U[i][j] = Yt[d-1-j][d-1-i] for i <= j.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -423,7 +424,8 @@ __global__ void assemble_u_kernel(const float *Yt, float *U, int64_t d) {
 
 struct PrepWs {
   DevStatus *st;
-  float *Yt, *Lhi, *Llo, *Yhi, *Ylo, *Linv;
+  float *Yt, *Yhi, *Ylo;
+  float *Lhi[2], *Llo[2], *Linv[2];   // double buffered by panel parity
 };
 
 PrepWs carve_prepare(void *ws, int64_t d) {
@@ -432,21 +434,62 @@ PrepWs carve_prepare(void *ws, int64_t d) {
   w.st = (DevStatus *)p;
   p += 256;
   w.Yt = (float *)p;  p += round_up((size_t)d * d * 4, 256);
-  w.Lhi = (float *)p; p += round_up((size_t)d * NB * 4, 256);
-  w.Llo = (float *)p; p += round_up((size_t)d * NB * 4, 256);
   w.Yhi = (float *)p; p += round_up((size_t)d * NB * 4, 256);
   w.Ylo = (float *)p; p += round_up((size_t)d * NB * 4, 256);
-  w.Linv = (float *)p;
+  for (int b = 0; b < 2; ++b) {
+    w.Lhi[b] = (float *)p; p += round_up((size_t)d * NB * 4, 256);
+    w.Llo[b] = (float *)p; p += round_up((size_t)d * NB * 4, 256);
+    w.Linv[b] = (float *)p; p += round_up((size_t)NB * NB * 4, 256);
+  }
   return w;
+}
+
+// A second stream and two event pairs per device, created once and kept for the process:
+// the panel loop runs its critical chain on the caller's stream and the rest beside it.
+struct SideStream {
+  std::mutex enqueue;  // one panel loop at a time enqueues on these events
+  cudaStream_t s = nullptr;
+  cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr;
+};
+constexpr int kMaxDevices = 128;
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+gptq_status side_stream(SideStream **out) {
+  int dev = -1;
+  GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream &ss = g_side[dev];
+  if (!ss.s) {
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking));
+    for (int b = 0; b < 2; ++b) {
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ea[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.eb[b], cudaEventDisableTiming));
+    }
+    GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e0, cudaEventDisableTiming));
+  }
+  *out = &ss;
+  return GPTQ_OK;
 }
 
 }  // namespace
 
 size_t prepare_ws_bytes(int64_t d) {
-  return 256 + round_up((size_t)d * d * 4, 256) + 4 * round_up((size_t)d * NB * 4, 256) +
-         round_up((size_t)NB * NB * 4, 256);
+  return 256 + round_up((size_t)d * d * 4, 256) + 6 * round_up((size_t)d * NB * 4, 256) +
+         2 * round_up((size_t)NB * NB * 4, 256);
 }
 
+// Panel loop.  On the caller's stream `s` (the critical chain):
+//   potrf(k) -> trsm(k) for all rows below -> the next panel column's update
+//   (rows >= k1, columns [k1, k1 + NB)) -> potrf(k + 1) ...
+// On the side stream `b`, once panel k's factor and L panel exist:
+//   inverse step a(k) -> the rest of the trailing update (the lower square from
+//   k1 + NB) -> inverse step b(k).
+// potrf(k) waits for the side stream's panel k - 2, which last wrote its diagonal block
+// and read the panel buffers it is about to overwrite.  Updates of one column block by
+// both streams are L2 reduce-adds (tensor-core epilogue); where C is not 16-byte aligned
+// the epilogue is a plain read-modify-write and everything runs on `s`.
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                            void *ws, cudaStream_t s) {
   static bool attr_done = false;
@@ -462,6 +505,12 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
     attr_done = true;
   }
   PrepWs w = carve_prepare(ws, d);
+  const bool overlap = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0;
+  SideStream *ss = nullptr;
+  if (overlap) GPTQ_TRY(side_stream(&ss));
+  std::unique_lock<std::mutex> enqueue_lock;
+  if (overlap) enqueue_lock = std::unique_lock<std::mutex>(ss->enqueue);
+  cudaStream_t b = overlap ? ss->s : s;
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
   dead_damp_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead_mask, w.st);
   GPTQ_LAUNCH_CHECK();
@@ -469,44 +518,71 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   GPTQ_LAUNCH_CHECK();
   identity_kernel<<<1024, 256, 0, s>>>(w.Yt, d);
   GPTQ_LAUNCH_CHECK();
+  if (overlap) {
+    GPTQ_CUDA_CHECK(cudaEventRecord(ss->e0, s));
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->e0, 0));
+  }
   float *A = H;  // reversed, damped Hessian; lower triangle is the Cholesky workspace
-  for (int64_t k0 = 0; k0 < d; k0 += NB) {
+  int k = 0;
+  for (int64_t k0 = 0; k0 < d; k0 += NB, ++k) {
+    const int par = k & 1;
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
-    potrf_kernel<<<1, PF_THREADS, potrf_smem, s>>>(A, d, k0, n, w.Linv, w.st);
+    if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[par], 0));
+    potrf_kernel<<<1, PF_THREADS, potrf_smem, s>>>(A, d, k0, n, w.Linv[par], w.st);
     GPTQ_LAUNCH_CHECK();
-    // trsm: rows [k1, d) of panel k -> L panel (hi/lo) only (A's panel is not reused)
     if (k1 < d) {
+      // trsm: rows [k1, d) of panel k -> L panel (hi/lo)
       const unsigned g = (unsigned)ceil_div(d - k1, RM_ROWS);
-      rowmul_kernel<<<g, RM_THREADS, rm_smem, s>>>(A + k0, d, nullptr, 0, k1, d, w.Linv, n,
-                                                  w.Lhi, w.Llo, w.st);
+      rowmul_kernel<<<g, RM_THREADS, rm_smem, s>>>(A + k0, d, nullptr, 0, k1, d, w.Linv[par], n,
+                                                  w.Lhi[par], w.Llo[par], w.st);
       GPTQ_LAUNCH_CHECK();
+      // next panel column: A[k1:, k1:k1+NB] -= L[k1:] L[k1:k1+NB]^T
+      GemmArgs g1{};
+      g1.a_hi = w.Lhi[par] + k1 * NB; g1.a_lo = w.Llo[par] + k1 * NB; g1.lda = NB;
+      g1.b_hi = w.Lhi[par] + k1 * NB; g1.b_lo = w.Llo[par] + k1 * NB; g1.ldb = NB;
+      g1.c = A + k1 * d + k1; g1.ldc = d;
+      g1.M = d - k1; g1.N = std::min<int64_t>(NB, d - k1); g1.K = n;
+      g1.alpha = -1.0f; g1.lower_only = 0; g1.trans_c = 0;
+      GPTQ_TRY(launch_gemm_nt(g1, w.st, s));
     }
-    // inv-a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
+    if (overlap) {
+      GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], s));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
+    }
+    // inverse step a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
     {
       const unsigned g = (unsigned)ceil_div(k1, RM_ROWS);
-      rowmul_kernel<<<g, RM_THREADS, rm_smem, s>>>(w.Yt + k0, d, w.Yt + k0, d, 0, k1, w.Linv,
-                                                  n, w.Yhi, w.Ylo, w.st);
+      rowmul_kernel<<<g, RM_THREADS, rm_smem, b>>>(w.Yt + k0, d, w.Yt + k0, d, 0, k1,
+                                                  w.Linv[par], n, w.Yhi, w.Ylo, w.st);
       GPTQ_LAUNCH_CHECK();
     }
     if (k1 < d) {
-      // syrk: A[k1:, k1:] -= Lp Lp^T (lower tiles)
-      GemmArgs g{};
-      g.a_hi = w.Lhi + k1 * NB; g.a_lo = w.Llo + k1 * NB; g.lda = NB;
-      g.b_hi = w.Lhi + k1 * NB; g.b_lo = w.Llo + k1 * NB; g.ldb = NB;
-      g.c = A + k1 * d + k1; g.ldc = d;
-      g.M = d - k1; g.N = d - k1; g.K = n;
-      g.alpha = -1.0f; g.lower_only = 1; g.trans_c = 0;
-      GPTQ_TRY(launch_gemm_nt(g, w.st, s));
-      // inv-b: Bt[c][k1:] -= Yp[c] Lp[k1:]^T for c < k1
+      if (d - k1 > NB) {
+        // the rest of the trailing update: lower square from (k1 + NB, k1 + NB)
+        const int64_t r0 = k1 + NB;
+        GemmArgs g2{};
+        g2.a_hi = w.Lhi[par] + r0 * NB; g2.a_lo = w.Llo[par] + r0 * NB; g2.lda = NB;
+        g2.b_hi = w.Lhi[par] + r0 * NB; g2.b_lo = w.Llo[par] + r0 * NB; g2.ldb = NB;
+        g2.c = A + r0 * d + r0; g2.ldc = d;
+        g2.M = d - r0; g2.N = d - r0; g2.K = n;
+        g2.alpha = -1.0f; g2.lower_only = 1; g2.trans_c = 0;
+        GPTQ_TRY(launch_gemm_nt(g2, w.st, b));
+      }
+      // inverse step b: Bt[c][k1:] -= Yp[c] Lp[k1:]^T for c < k1
       GemmArgs h{};
       h.a_hi = w.Yhi; h.a_lo = w.Ylo; h.lda = NB;
-      h.b_hi = w.Lhi + k1 * NB; h.b_lo = w.Llo + k1 * NB; h.ldb = NB;
+      h.b_hi = w.Lhi[par] + k1 * NB; h.b_lo = w.Llo[par] + k1 * NB; h.ldb = NB;
       h.c = w.Yt + k1; h.ldc = d;
       h.M = k1; h.N = d - k1; h.K = n;
       h.alpha = -1.0f; h.lower_only = 0; h.trans_c = 0;
-      GPTQ_TRY(launch_gemm_nt(h, w.st, s));
+      GPTQ_TRY(launch_gemm_nt(h, w.st, b));
     }
+    if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->eb[par], b));
+  }
+  if (overlap) {
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[0], 0));
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[1], 0));
   }
   dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
   assemble_u_kernel<<<tg, dim3(32, 8), 0, s>>>(w.Yt, U, d);
