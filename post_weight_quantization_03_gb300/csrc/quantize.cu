@@ -126,25 +126,34 @@ __global__ void diag_blocks_kernel(const float *__restrict__ U, int64_t d, int b
 // ---------------------------------------------------------------------------------------
 constexpr int SUB = 32;
 
+// k-th working weight of the sub-block, held as float2 pairs (k/2).(x|y)
+#define W_AT(wp, k) (((k) & 1) ? (wp)[(k) >> 1].y : (wp)[(k) >> 1].x)
+
 template <int J>
 struct SweepStep {
-  static __device__ __forceinline__ void run(float (&w)[SUB], uint32_t (&cw)[SUB / 4],
+  static __device__ __forceinline__ void run(float2 (&wp)[SUB / 2], uint32_t (&cw)[SUB / 4],
                                              const float *Ub, const float *rd, float s,
                                              float z, float maxq) {
-    const float x = __fdiv_rn(w[J], s);
+    const float wj = W_AT(wp, J);
+    const float x = __fdiv_rn(wj, s);
     const float c = fminf(fmaxf(rintf(x) + z, 0.0f), maxq);
     const float q = s * (c - z);
-    const float e = (w[J] - q) * rd[J];
+    const float e = (wj - q) * rd[J];
     cw[J / 4] |= (uint32_t)c << (8 * (J % 4));
-    w[J] = e;  // the register now holds the scaled error of column J
+    if (J & 1) wp[J >> 1].y = e; else wp[J >> 1].x = e;  // now the scaled error of column J
+    // w_k -= e U_Jk for k > J in the sub-block: a lone odd column, then pairs
+    constexpr int K0 = J + 1;
+    if (K0 < SUB && (K0 & 1)) wp[K0 >> 1].y = fmaf(-e, Ub[J * LDU + K0], wp[K0 >> 1].y);
+    const float2 ne = make_float2(-e, -e);
 #pragma unroll
-    for (int k = J + 1; k < SUB; ++k) w[k] = fmaf(-e, Ub[J * LDU + k], w[k]);
-    SweepStep<J + 1>::run(w, cw, Ub, rd, s, z, maxq);
+    for (int k = (K0 + 1) & ~1; k < SUB; k += 2)
+      wp[k >> 1] = __ffma2_rn(ne, *reinterpret_cast<const float2 *>(Ub + J * LDU + k), wp[k >> 1]);
+    SweepStep<J + 1>::run(wp, cw, Ub, rd, s, z, maxq);
   }
 };
 template <>
 struct SweepStep<SUB> {
-  static __device__ __forceinline__ void run(float (&)[SUB], uint32_t (&)[SUB / 4],
+  static __device__ __forceinline__ void run(float2 (&)[SUB / 2], uint32_t (&)[SUB / 4],
                                              const float *, const float *, float, float,
                                              float) {}
 };
@@ -211,37 +220,39 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
 #pragma unroll 1
   for (int sb = 0; sb < SB / SUB; ++sb) {
     const int c0 = sb * SUB;
-    float w[SUB];
+    float2 wp[SUB / 2];
 #pragma unroll
     for (int q = 0; q < SUB / 4; ++q) {
       const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
-      w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+      wp[2 * q] = make_float2(v.x, v.y);
+      wp[2 * q + 1] = make_float2(v.z, v.w);
     }
     uint32_t cw[SUB / 4];
 #pragma unroll
     for (int i = 0; i < SUB / 4; ++i) cw[i] = 0u;
-    SweepStep<0>::run(w, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
+    SweepStep<0>::run(wp, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
     // errors replace the consumed weights; codes go to their own staging area
 #pragma unroll
     for (int q = 0; q < SUB / 4; ++q)
       *reinterpret_cast<float4 *>(my + c0 + 4 * q) =
-          make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          make_float4(wp[2 * q].x, wp[2 * q].y, wp[2 * q + 1].x, wp[2 * q + 1].y);
 #pragma unroll
     for (int i = 0; i < SUB / 4; ++i) cstage[tid * (SB / 4 + 1) + sb * (SUB / 4) + i] = cw[i];
     // the sub-block's errors update the later columns of the block:
-    //   w_c -= sum_k e_k U[c0 + k][c]
+    //   w_c -= sum_k e_k U[c0 + k][c]     (paired fp32 FMAs, each rounded as fmaf)
 #pragma unroll 1
     for (int c = c0 + SUB; c < SB; c += 4) {
-      float4 acc = *reinterpret_cast<const float4 *>(my + c);
+      const float4 a = *reinterpret_cast<const float4 *>(my + c);
+      float2 lo = make_float2(a.x, a.y), hi = make_float2(a.z, a.w);
 #pragma unroll
       for (int k = 0; k < SUB; ++k) {
         const float4 u = *reinterpret_cast<const float4 *>(Us + (c0 + k) * LDU + c);
-        acc.x = fmaf(-w[k], u.x, acc.x);
-        acc.y = fmaf(-w[k], u.y, acc.y);
-        acc.z = fmaf(-w[k], u.z, acc.z);
-        acc.w = fmaf(-w[k], u.w, acc.w);
+        const float ek = W_AT(wp, k);
+        const float2 ne = make_float2(-ek, -ek);
+        lo = __ffma2_rn(ne, make_float2(u.x, u.y), lo);
+        hi = __ffma2_rn(ne, make_float2(u.z, u.w), hi);
       }
-      *reinterpret_cast<float4 *>(my + c) = acc;
+      *reinterpret_cast<float4 *>(my + c) = make_float4(lo.x, lo.y, hi.x, hi.y);
     }
   }
   __syncthreads();
@@ -263,12 +274,27 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
           make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
     }
   }
-  // codes: staged as bytes, stored coalesced
-  const uint8_t *cb = (const uint8_t *)cstage;
-  for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
-    const int r = e / SB, j = e % SB;
-    const int64_t gr = r0 + r;
-    if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
+  // codes: staged as words (4 codes each), stored coalesced; whole words when the block
+  // starts on a 4-column boundary, bytes otherwise
+  if ((b0 % 4) == 0 && (ldc % 4) == 0) {
+#pragma unroll 4
+    for (int it = 0; it < SB / 4; ++it) {
+      const int e = it * SW_ROWS + tid;
+      const int r = e / (SB / 4), wq = e % (SB / 4);
+      const int64_t gr = r0 + r;
+      if (gr < m && 4 * wq < nb) {
+        uint32_t v = cstage[r * (SB / 4 + 1) + wq];
+        if (4 * wq + 4 > nb) v &= (1u << (8 * (nb - 4 * wq))) - 1u;  // ragged block end
+        *reinterpret_cast<uint32_t *>(codes + gr * ldc + b0 + 4 * wq) = v;
+      }
+    }
+  } else {
+    const uint8_t *cb = (const uint8_t *)cstage;
+    for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
+      const int r = e / SB, j = e % SB;
+      const int64_t gr = r0 + r;
+      if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
+    }
   }
 }
 
