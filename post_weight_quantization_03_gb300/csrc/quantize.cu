@@ -159,10 +159,23 @@ struct SweepStep<SUB> {
 };
 
 // ---------------------------------------------------------------------------------------
-// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA.  The packed U
-// block arrives by one bulk copy while the threads stage the working-weight tile.
+// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA, two threads per row:
+//   chain  (warps 0-1): quantizes one 32-column sub-block at a time, its working weights
+//                       in registers, and leaves the sub-block's scaled errors in the row
+//   update (warps 2-3): applies those errors to the later sub-blocks of the row: the next
+//                       sub-block first (then signals it ready), the farther ones while the
+//                       chain thread already works on the next sub-block
+// Hand-offs are named barriers (1: errors of a sub-block ready, 2: a sub-block fully
+// updated), each an arrive on one side and a sync on the other.  The packed U block
+// arrives by one bulk copy while the threads stage the working-weight tile.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(SW_ROWS)
+constexpr int SW_THREADS = 2 * SW_ROWS;
+
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__global__ void __launch_bounds__(SW_THREADS)
 sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, int nb,
              const float *__restrict__ Ud, const float *__restrict__ scale,
              const int32_t *__restrict__ zero, float maxq, float *__restrict__ Ehi,
@@ -172,6 +185,7 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   float *Us = sm;                        // SB x LDU, then SB reciprocals
   float *rdiag = sm + SB * LDU;
   float *stage = sm + UD_FLOATS;         // SW_ROWS x LDW
+  uint32_t *cstage = (uint32_t *)(stage + SW_ROWS * LDW);  // SW_ROWS x (SB/4 + 1) words
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
@@ -187,8 +201,8 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   // working weights, coalesced; float4 when the tile rows are 16-byte aligned
   if ((b0 % 4) == 0 && (ldwf % 4) == 0) {
 #pragma unroll 8
-    for (int it = 0; it < SB / 4; ++it) {
-      const int e = it * SW_ROWS + tid;      // float4 index in the tile
+    for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
+      const int e = it * SW_THREADS + tid;   // float4 index in the tile
       const int r = e / (SB / 4), q = e % (SB / 4);
       const int64_t gr = r0 + r;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -203,8 +217,8 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
     }
   } else {
 #pragma unroll 16
-    for (int it = 0; it < SB; ++it) {
-      const int e = it * SW_ROWS + tid;
+    for (int it = 0; it < SW_ROWS * SB / SW_THREADS; ++it) {
+      const int e = it * SW_THREADS + tid;
       const int r = e / SB, j = e % SB;
       const int64_t gr = r0 + r;
       stage[r * LDW + j] = (gr < m && j < nb) ? Wf[gr * ldwf + b0 + j] : 0.f;
@@ -212,54 +226,71 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   }
   const int got = tc::mbar_wait(&bar, 0, st) ? 1 : 0;
   if (!__syncthreads_and(got)) return;  // CTA-uniform: later barriers stay matched
-  const int64_t row = r0 + tid;
-  const float s = row < m ? scale[row] : 1.f;
-  const float z = row < m ? (float)zero[row] : 0.f;
-  float *my = stage + tid * LDW;           // this thread's row of the block
-  uint32_t *cstage = (uint32_t *)(stage + SW_ROWS * LDW);  // SW_ROWS x (SB/4 + 1) words
+  const int role = tid / SW_ROWS, rl = tid % SW_ROWS;
+  float *my = stage + rl * LDW;         // this row of the block
+  if (role == 0) {
+    // ---------------- chain ----------------
+    const int64_t row = r0 + rl;
+    const float s = row < m ? scale[row] : 1.f;
+    const float z = row < m ? (float)zero[row] : 0.f;
 #pragma unroll 1
-  for (int sb = 0; sb < SB / SUB; ++sb) {
-    const int c0 = sb * SUB;
-    float2 wp[SUB / 2];
+    for (int sb = 0; sb < SB / SUB; ++sb) {
+      const int c0 = sb * SUB;
+      if (sb > 0) tc::named_barrier(2, SW_THREADS);  // sub-block sb fully updated
+      float2 wp[SUB / 2];
 #pragma unroll
-    for (int q = 0; q < SUB / 4; ++q) {
-      const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
-      wp[2 * q] = make_float2(v.x, v.y);
-      wp[2 * q + 1] = make_float2(v.z, v.w);
-    }
-    uint32_t cw[SUB / 4];
-#pragma unroll
-    for (int i = 0; i < SUB / 4; ++i) cw[i] = 0u;
-    SweepStep<0>::run(wp, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
-    // errors replace the consumed weights; codes go to their own staging area
-#pragma unroll
-    for (int q = 0; q < SUB / 4; ++q)
-      *reinterpret_cast<float4 *>(my + c0 + 4 * q) =
-          make_float4(wp[2 * q].x, wp[2 * q].y, wp[2 * q + 1].x, wp[2 * q + 1].y);
-#pragma unroll
-    for (int i = 0; i < SUB / 4; ++i) cstage[tid * (SB / 4 + 1) + sb * (SUB / 4) + i] = cw[i];
-    // the sub-block's errors update the later columns of the block:
-    //   w_c -= sum_k e_k U[c0 + k][c]     (paired fp32 FMAs, each rounded as fmaf)
-#pragma unroll 1
-    for (int c = c0 + SUB; c < SB; c += 4) {
-      const float4 a = *reinterpret_cast<const float4 *>(my + c);
-      float2 lo = make_float2(a.x, a.y), hi = make_float2(a.z, a.w);
-#pragma unroll
-      for (int k = 0; k < SUB; ++k) {
-        const float4 u = *reinterpret_cast<const float4 *>(Us + (c0 + k) * LDU + c);
-        const float ek = W_AT(wp, k);
-        const float2 ne = make_float2(-ek, -ek);
-        lo = __ffma2_rn(ne, make_float2(u.x, u.y), lo);
-        hi = __ffma2_rn(ne, make_float2(u.z, u.w), hi);
+      for (int q = 0; q < SUB / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
+        wp[2 * q] = make_float2(v.x, v.y);
+        wp[2 * q + 1] = make_float2(v.z, v.w);
       }
-      *reinterpret_cast<float4 *>(my + c) = make_float4(lo.x, lo.y, hi.x, hi.y);
+      uint32_t cw[SUB / 4];
+#pragma unroll
+      for (int i = 0; i < SUB / 4; ++i) cw[i] = 0u;
+      SweepStep<0>::run(wp, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
+#pragma unroll
+      for (int q = 0; q < SUB / 4; ++q)
+        *reinterpret_cast<float4 *>(my + c0 + 4 * q) =
+            make_float4(wp[2 * q].x, wp[2 * q].y, wp[2 * q + 1].x, wp[2 * q + 1].y);
+#pragma unroll
+      for (int i = 0; i < SUB / 4; ++i) cstage[rl * (SB / 4 + 1) + sb * (SUB / 4) + i] = cw[i];
+      bar_arrive(1, SW_THREADS);                   // errors of sub-block sb ready
+    }
+  } else {
+    // ---------------- update ----------------
+#pragma unroll 1
+    for (int sb = 0; sb < SB / SUB; ++sb) {
+      tc::named_barrier(1, SW_THREADS);            // errors of sub-block sb
+      if (sb == SB / SUB - 1) break;
+      const int c0 = sb * SUB;
+      float e[SUB];
+#pragma unroll
+      for (int q = 0; q < SUB / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
+        e[4 * q] = v.x; e[4 * q + 1] = v.y; e[4 * q + 2] = v.z; e[4 * q + 3] = v.w;
+      }
+      //   w_c -= sum_k e_k U[c0 + k][c], next sub-block first (paired fp32 FMAs)
+#pragma unroll 1
+      for (int c = c0 + SUB; c < SB; c += 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(my + c);
+        float2 lo = make_float2(a.x, a.y), hi = make_float2(a.z, a.w);
+#pragma unroll
+        for (int k = 0; k < SUB; ++k) {
+          const float4 u = *reinterpret_cast<const float4 *>(Us + (c0 + k) * LDU + c);
+          const float2 ne = make_float2(-e[k], -e[k]);
+          lo = __ffma2_rn(ne, make_float2(u.x, u.y), lo);
+          hi = __ffma2_rn(ne, make_float2(u.z, u.w), hi);
+        }
+        *reinterpret_cast<float4 *>(my + c) = make_float4(lo.x, lo.y, hi.x, hi.y);
+        if (c + 4 == c0 + 2 * SUB) bar_arrive(2, SW_THREADS);  // sub-block sb + 1 ready
+      }
     }
   }
   __syncthreads();
   // E (now in the stage rows) -> global as a TF32 head/tail pair, coalesced
-#pragma unroll 8
-  for (int it = 0; it < SB / 4; ++it) {
-    const int e = it * SW_ROWS + tid;
+#pragma unroll 4
+  for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
+    const int e = it * SW_THREADS + tid;
     const int r = e / (SB / 4), q = e % (SB / 4);
     const int64_t gr = r0 + r;
     if (gr < m) {
@@ -278,8 +309,8 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   // starts on a 4-column boundary, bytes otherwise
   if ((b0 % 4) == 0 && (ldc % 4) == 0) {
 #pragma unroll 4
-    for (int it = 0; it < SB / 4; ++it) {
-      const int e = it * SW_ROWS + tid;
+    for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
+      const int e = it * SW_THREADS + tid;
       const int r = e / (SB / 4), wq = e % (SB / 4);
       const int64_t gr = r0 + r;
       if (gr < m && 4 * wq < nb) {
@@ -290,7 +321,7 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
     }
   } else {
     const uint8_t *cb = (const uint8_t *)cstage;
-    for (int e = tid; e < SW_ROWS * SB; e += blockDim.x) {
+    for (int e = tid; e < SW_ROWS * SB; e += SW_THREADS) {
       const int r = e / SB, j = e % SB;
       const int64_t gr = r0 + r;
       if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
@@ -420,7 +451,7 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
   for (int64_t b0 = 0; b0 < d; b0 += block) {
     const int nb = (int)((d - b0) < block ? (d - b0) : block);
     const int64_t b1 = b0 + nb;
-    sweep_kernel<<<sweep_grid, SW_ROWS, sweep_smem, s>>>(
+    sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
         q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
         q.Elo, q.codes, q.ldc, q.st);
     GPTQ_LAUNCH_CHECK();
