@@ -110,13 +110,14 @@ __global__ void identity_kernel(float *Y, int64_t d) {
 //   phase 2: A_il -= L_ip L_lp^T                  R0 <= l <= i      (syrk)
 //            Bt_cr -= Yt_cp L_rp^T                c < R0 <= r       (inverse, step b)
 // Every product is C(m, n) = sum_k A(m, k) B(n, k) over 32 k; a warp takes a group of 4
-// rows and 32 lanes x 4 columns, so A reads are broadcasts and B reads are conflict free
-// (row stride 129); each phase is exactly 32 row groups, two per warp.
+// rows and 32 lanes x NQ columns (NQ = the 32-column blocks the group needs), reading A
+// by broadcast and B conflict free as float4 along k (row stride 132: eight consecutive
+// rows fall in distinct bank groups); each phase is exactly 32 row groups, two per warp.
 // A non-positive pivot records NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
 constexpr int PF_THREADS = 512;
 constexpr int PT = 32;             // leaf tile
-constexpr int PL = NB + 1;         // smem leading dimension
+constexpr int PL = NB + 4;         // smem leading dimension (16-byte rows)
 
 // Column J of the leaf factorization (lane i holds row i of the tile in a[]):
 //   L_JJ = sqrt(a_JJ);  L_iJ = a_iJ / L_JJ;  a_il -= L_iJ L_lJ  for l in (J, i]
@@ -145,15 +146,19 @@ struct LeafChol<PT> {
 };
 
 // Row I of the tile inverse for column c = lane:  x_I = (delta_Ic - sum_{l<I} L_Il x_l) / L_II
+// (row I of L read as float4; even and odd l summed apart)
 template <int I>
 struct LeafInv {
   static __device__ __forceinline__ void run(float (&x)[PT], const float *Lt, const float *rd,
                                              int lane) {
     float a0 = (I == lane) ? 1.0f : 0.0f, a1 = 0.0f;
 #pragma unroll
-    for (int l = 0; l < I; ++l) {
-      if (l & 1) a1 = fmaf(-Lt[I * PL + l], x[l], a1);
-      else a0 = fmaf(-Lt[I * PL + l], x[l], a0);
+    for (int l4 = 0; l4 < (I + 3) / 4; ++l4) {
+      const float4 v = *reinterpret_cast<const float4 *>(Lt + I * PL + 4 * l4);
+      if (4 * l4 + 0 < I) a0 = fmaf(-v.x, x[4 * l4 + 0], a0);
+      if (4 * l4 + 1 < I) a1 = fmaf(-v.y, x[4 * l4 + 1], a1);
+      if (4 * l4 + 2 < I) a0 = fmaf(-v.z, x[4 * l4 + 2], a0);
+      if (4 * l4 + 3 < I) a1 = fmaf(-v.w, x[4 * l4 + 3], a1);
     }
     x[I] = (I < lane) ? 0.0f : (a0 + a1) * rd[I];
     LeafInv<I + 1>::run(x, Lt, rd, lane);
@@ -169,12 +174,22 @@ struct LeafInv<PT> {
 __device__ __forceinline__ void leaf_factor(float *S, float *Li, float *rd, int t0, int lane,
                                             int &bad) {
   float a[PT];
+  float *row = S + (t0 + lane) * PL + t0;
 #pragma unroll
-  for (int l = 0; l < PT; ++l) a[l] = (l <= lane) ? S[(t0 + lane) * PL + t0 + l] : 0.0f;
+  for (int q = 0; q < PT / 4; ++q) {
+    const float4 v = *reinterpret_cast<const float4 *>(row + 4 * q);
+    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+  }
+#pragma unroll
+  for (int l = 0; l < PT; ++l)
+    if (l > lane) a[l] = 0.0f;
   float rdl = 0.0f;
   LeafChol<0>::run(a, rdl, lane, t0, bad);
 #pragma unroll
-  for (int l = 0; l < PT; ++l) S[(t0 + lane) * PL + t0 + l] = (l <= lane) ? a[l] : 0.0f;
+  for (int q = 0; q < PT / 4; ++q)
+    *reinterpret_cast<float4 *>(row + 4 * q) =
+        make_float4(4 * q + 0 <= lane ? a[4 * q + 0] : 0.0f, 4 * q + 1 <= lane ? a[4 * q + 1] : 0.0f,
+                    4 * q + 2 <= lane ? a[4 * q + 2] : 0.0f, 4 * q + 3 <= lane ? a[4 * q + 3] : 0.0f);
   rd[lane] = rdl;
   __syncwarp();
   float x[PT];
@@ -183,31 +198,68 @@ __device__ __forceinline__ void leaf_factor(float *S, float *Li, float *rd, int 
   for (int i = 0; i < PT; ++i) Li[(t0 + i) * PL + t0 + lane] = x[i];
 }
 
-// 4 rows (A rows m0..m0+3) x columns n = nb + lane + 32q (q < nq) of sum_k A(m,k) B(n,k),
+// 4 rows (A rows m0..m0+3) x columns n = nb + lane + 32q (q < NQ) of sum_k A(m,k) B(n,k),
 // k < 32.  A(m, k) = Am[m * PL + k], B(n, k) = Bm[n * PL + k].
+template <int NQ>
 __device__ __forceinline__ void group_nt(const float *Am, const float *Bm, int m0, int nb,
-                                         int nq, int lane, float (&acc)[4][4]) {
+                                         int lane, float (&acc)[4][NQ]) {
+  float2 c2[4][NQ];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < PT; ++k) {
-    float a[4], b[4];
+    for (int q = 0; q < NQ; ++q) c2[i][q] = make_float2(0.f, 0.f);
+#pragma unroll 2
+  for (int k = 0; k < PT; k += 4) {
+    float4 a[4], b[NQ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = Am[(m0 + i) * PL + k];
+    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Am + (m0 + i) * PL + k);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) b[q] = (q < nq) ? Bm[(nb + lane + 32 * q) * PL + k] : 0.f;
+    for (int q = 0; q < NQ; ++q)
+      b[q] = *reinterpret_cast<const float4 *>(Bm + (nb + lane + 32 * q) * PL + k);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(a[i], b[q], acc[i][q]);
+      for (int q = 0; q < NQ; ++q) {
+        c2[i][q] = __ffma2_rn(make_float2(a[i].x, a[i].y), make_float2(b[q].x, b[q].y), c2[i][q]);
+        c2[i][q] = __ffma2_rn(make_float2(a[i].z, a[i].w), make_float2(b[q].z, b[q].w), c2[i][q]);
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) acc[i][q] = c2[i][q].x + c2[i][q].y;
+}
+
+// Cm[m][n] -= (Am Bm^T)[m][n] for the group's 4 rows and NQ column blocks from nb; with
+// `lower` only columns n <= m.
+template <int NQ>
+__device__ __forceinline__ void update_group(float *Cm, const float *Am, const float *Bm,
+                                             int m0, int nb, int lane, bool lower) {
+  float acc[4][NQ];
+  group_nt<NQ>(Am, Bm, m0, nb, lane, acc);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const int col = nb + lane + 32 * q;
+      if (!lower || col <= m0 + i) Cm[(m0 + i) * PL + col] -= acc[i][q];
+    }
+}
+
+__device__ __forceinline__ void update_group_n(int nq, float *Cm, const float *Am,
+                                               const float *Bm, int m0, int nb, int lane,
+                                               bool lower) {
+  switch (nq) {
+    case 1: update_group<1>(Cm, Am, Bm, m0, nb, lane, lower); break;
+    case 2: update_group<2>(Cm, Am, Bm, m0, nb, lane, lower); break;
+    case 3: update_group<3>(Cm, Am, Bm, m0, nb, lane, lower); break;
+    default: break;
   }
 }
 
 __global__ void __launch_bounds__(PF_THREADS, 1)
 potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatus *st) {
-  extern __shared__ float psm[];
+  extern __shared__ __align__(16) float psm[];
   float *S = psm;                // NB x PL: working block, becomes L (lower)
   float *Bt = psm + NB * PL;     // NB x PL: transposed right-hand side -> Linv^T
   float *Li = Bt + NB * PL;      // PT x PL: current leaf's tile inverse (rows P0.., cols 0..)
@@ -227,79 +279,52 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
 #pragma unroll
       for (int q = 0; q < 4; ++q) v[q] = (i < n && l4 + q < n) ? A[(k0 + i) * d + k0 + l4 + q] : 0.f;
     }
+    float sv[4], bv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int l = l4 + q;
-      S[i * PL + l] = (i < n && l < n) ? v[q] : (i == l ? 1.0f : 0.0f);
-      Bt[i * PL + l] = (i == l) ? 1.0f : 0.0f;
+      sv[q] = (i < n && l < n) ? v[q] : (i == l ? 1.0f : 0.0f);
+      bv[q] = (i == l) ? 1.0f : 0.0f;
     }
+    *reinterpret_cast<float4 *>(S + i * PL + l4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    *reinterpret_cast<float4 *>(Bt + i * PL + l4) = make_float4(bv[0], bv[1], bv[2], bv[3]);
   }
   __syncthreads();
   int bad = -1;
 #pragma unroll 1
   for (int p = 0; p < NB / PT; ++p) {
     const int P0 = p * PT, R0 = P0 + PT;
+    const int ns = (NB - R0) / 4;  // row groups of S below the sub-panel
     if (warp == 0) {
       // the leaf writes its tile inverse at rows P0.. of a PT x PL scratch (shifted)
       leaf_factor(S, Li - P0 * PL - P0, rd, P0, lane, bad);
       if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
     }
     __syncthreads();
-    // phase 1: 32 row groups of 4 rows: groups g < (NB-R0)/4 are rows R0 + 4g of S (trsm),
-    // the rest rows 4(g - (NB-R0)/4) of Bt (inverse step a); 32 output columns each.
-    const float *LiT = Li;  // Linv_pp rows (B operand): LiT[j * PL + t]
-    float res[2][4];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int g = warp + 16 * r;
-      const int ns = (NB - R0) / 4;
-      float acc[4][4];
-      const float *Am = (g < ns) ? (S + P0) : (Bt + P0);
-      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
-      group_nt(Am, LiT, m0, 0, 1, lane, acc);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) res[r][i] = acc[i][0];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int g = warp + 16 * r;
-      const int ns = (NB - R0) / 4;
-      float *Cm = (g < ns) ? (S + P0) : (Bt + P0);
-      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
-#pragma unroll
-      for (int i = 0; i < 4; ++i) Cm[(m0 + i) * PL + lane] = res[r][i];
-    }
-    __syncthreads();
-    // phase 2: syrk on S rows >= R0 (columns R0..row), inverse step b on Bt rows < R0
-    // (columns R0..NB-1)
+    // phase 1: groups g < ns are rows R0 + 4g of S (trsm), the rest rows 4(g - ns) of Bt
+    // (inverse step a); 32 output columns each, in place (a group reads only its rows)
 #pragma unroll 1
     for (int r = 0; r < 2; ++r) {
       const int g = warp + 16 * r;
-      const int ns = (NB - R0) / 4;
-      float acc[4][4];
+      float *Cm = (g < ns) ? (S + P0) : (Bt + P0);
+      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
+      float acc[4][1];
+      group_nt<1>(Cm, Li, m0, 0, lane, acc);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) Cm[(m0 + i) * PL + lane] = acc[i][0];
+    }
+    __syncthreads();
+    // phase 2: syrk on S rows >= R0 (columns R0..row), inverse step b on Bt rows < R0
+    // (columns R0..NB-1); both read only columns P0..R0-1
+#pragma unroll 1
+    for (int r = 0; r < 2; ++r) {
+      const int g = warp + 16 * r;
       if (g < ns) {
         const int m0 = R0 + 4 * g;
-        const int nq = (m0 + 3 - R0) / 32 + 1;   // column blocks reaching the diagonal
-        group_nt(S + P0, S + P0, m0, R0, nq, lane, acc);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int col = R0 + lane + 32 * q;
-            if (q < nq && col <= m0 + i) S[(m0 + i) * PL + col] -= acc[i][q];
-          }
+        update_group_n((m0 + 3 - R0) / 32 + 1, S, S + P0, S + P0, m0, R0, lane, true);
       } else {
-        const int m0 = 4 * (g - ns);
-        const int nq = (NB - R0) / 32;
-        if (nq > 0) {
-          group_nt(Bt + P0, S + P0, m0, R0, nq, lane, acc);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (q < nq) Bt[(m0 + i) * PL + R0 + lane + 32 * q] -= acc[i][q];
-        }
+        update_group_n((NB - R0) / 32, Bt, Bt + P0, S + P0, 4 * (g - ns), R0, lane, false);
       }
     }
     __syncthreads();
@@ -310,9 +335,14 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
     return;
   }
   // Linv[i][c] = Yt[c][i]
-  for (int e = tid; e < NB * NB; e += PF_THREADS) {
-    const int i = e / NB, c = e % NB;
-    Linv[e] = (i < n && c < n) ? Bt[c * PL + i] : 0.0f;
+  for (int e = tid; e < NB * NB / 4; e += PF_THREADS) {
+    const int i4 = 4 * (e / NB), c = e % NB;
+    const float4 v = *reinterpret_cast<const float4 *>(Bt + c * PL + i4);
+    const bool cc = c < n;
+    Linv[(i4 + 0) * NB + c] = (cc && i4 + 0 < n) ? v.x : 0.0f;
+    Linv[(i4 + 1) * NB + c] = (cc && i4 + 1 < n) ? v.y : 0.0f;
+    Linv[(i4 + 2) * NB + c] = (cc && i4 + 2 < n) ? v.z : 0.0f;
+    Linv[(i4 + 3) * NB + c] = (cc && i4 + 3 < n) ? v.w : 0.0f;
   }
 }
 
