@@ -99,162 +99,149 @@ __global__ void identity_kernel(float *Y, int64_t d) {
 // inverse Linv.  Only Linv leaves the kernel (NB x NB, lower, zero padded): the panel below
 // is L_ik = A_ik Linv^T and the inversion needs Linv only.
 //
-// Recursive over four 32-column sub-panels p (P0 = 32p, R0 = P0 + 32), in shared memory,
+// Recursive over eight PW-column sub-panels p (P0 = PW p, R0 = P0 + PW), in shared memory,
 // with the inverse built alongside in transposed form (Bt = right-hand side of L Y = I,
 // transposed, which becomes Yt = Linv^T), exactly like the panel loop of the whole
 // factorization:
-//   leaf   : one warp factors the 32 x 32 tile (lane i holds row i; pivots and multipliers
-//            travel by shuffles) and inverts it (lane c solves column c)
-//   phase 1: L_ip  = A_ip Linv_pp^T              rows i >= R0      (trsm)
-//            Yt_cp = Bt_cp Linv_pp^T              rows c <  R0      (inverse, step a)
+//   leaf   : one warp factors the PW x PW tile (lane i holds row i; the next pivot is
+//            issued before the current column's updates) and writes the scaled transpose
+//            M[j][i] = L_ij / L_jj and the reciprocal pivots rd
+//   phase 1: L_ip  L_pp^T = A_ip                  rows i >= R0      (trsm)
+//            Yt_cp L_pp^T = Bt_cp                  rows c <  R0      (inverse, step a)
+//            one thread per row, forward substitution against M
 //   phase 2: A_il -= L_ip L_lp^T                  R0 <= l <= i      (syrk)
 //            Bt_cr -= Yt_cp L_rp^T                c < R0 <= r       (inverse, step b)
-// Every product is C(m, n) = sum_k A(m, k) B(n, k) over 32 k; a warp takes a group of 4
-// rows and 32 lanes x NQ columns (NQ = the 32-column blocks the group needs), reading A
-// by broadcast and B conflict free as float4 along k (row stride 132: eight consecutive
-// rows fall in distinct bank groups); each phase is exactly 32 row groups, two per warp.
-// A non-positive pivot records NOT_PD with its global index.
+// Phase 2 is a product over PW k in tiles of 8 rows x 64 columns per warp (A read by
+// broadcast, B as float4 along k at row stride 132: eight consecutive rows fall in distinct
+// bank groups).  Rows P0..R0-1 of Bt (identity rows, untouched until then) are written
+// while the leaf runs, and the rows of Linv that phase 1 finishes are stored during
+// phase 2.  A non-positive pivot records NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
 constexpr int PF_THREADS = 512;
-constexpr int PT = 32;             // leaf tile
+constexpr int PF_WARPS = PF_THREADS / 32;
+constexpr int PW = 16;             // sub-panel width
 constexpr int PL = NB + 4;         // smem leading dimension (16-byte rows)
 
-// Column J of the leaf factorization (lane i holds row i of the tile in a[]):
-//   L_JJ = sqrt(a_JJ);  L_iJ = a_iJ / L_JJ;  a_il -= L_iJ L_lJ  for l in (J, i]
+// Column J of the leaf, rl = 1/sqrt(pivot J) already known.  Lane i holds row i of the
+// tile in a[] and its running diagonal in dg.  The updates run on every lane and every
+// later column: what lands above the diagonal is never read and is cleared at the end.
 template <int J>
-struct LeafChol {
-  static __device__ __forceinline__ void run(float (&a)[PT], float &rdl, int lane, int t0,
-                                             int &bad) {
-    const float piv = __shfl_sync(0xffffffffu, a[J], J);
-    const bool okp = piv > 0.0f;
-    if (!okp && bad < 0) bad = t0 + J;
-    const float rl = okp ? rsqrtf(piv) : 0.0f;
-    if (lane == J) rdl = rl;      // 1 / L_JJ, kept by the lane owning row J
-    const float lij = a[J] * rl;  // L[i][J] (lane J: sqrt(piv); lanes above: 0)
+struct LeafCol {
+  static __device__ __forceinline__ void run(float (&a)[PW], float &dg, float rl, float &rdl,
+                                             float *cb, float *M, int lane) {
+    if (lane == J) rdl = rl;
+    const float lij = (lane == J ? dg : a[J]) * rl;  // L[i][J]
     a[J] = lij;
-#pragma unroll
-    for (int l = J + 1; l < PT; ++l) {
-      const float llj = __shfl_sync(0xffffffffu, lij, l);
-      if (lane >= l) a[l] = fmaf(-lij, llj, a[l]);
+    dg = fmaf(-lij, lij, dg);
+    float rn = 0.0f;
+    if (J + 1 < PW) {                                // next pivot, off the update path
+      const float pn = __shfl_sync(0xffffffffu, dg, J + 1);
+      rn = pn > 0.0f ? rsqrtf(pn) : 0.0f;
     }
-    LeafChol<J + 1>::run(a, rdl, lane, t0, bad);
+    M[J * PL + lane] = lij * rl;                     // L[i][J] / L[J][J]
+    if (J + 1 < PW) {
+      float *c = cb + (J & 1) * 32;
+      c[lane] = lij;
+      __syncwarp();
+#pragma unroll
+      for (int l4 = (J + 1) / 4; l4 < PW / 4; ++l4) {
+        const float4 v = *reinterpret_cast<const float4 *>(c + 4 * l4);
+        if (4 * l4 + 0 > J) a[4 * l4 + 0] = fmaf(-lij, v.x, a[4 * l4 + 0]);
+        if (4 * l4 + 1 > J) a[4 * l4 + 1] = fmaf(-lij, v.y, a[4 * l4 + 1]);
+        if (4 * l4 + 2 > J) a[4 * l4 + 2] = fmaf(-lij, v.z, a[4 * l4 + 2]);
+        if (4 * l4 + 3 > J) a[4 * l4 + 3] = fmaf(-lij, v.w, a[4 * l4 + 3]);
+      }
+    }
+    LeafCol<J + 1>::run(a, dg, rn, rdl, cb, M, lane);
   }
 };
 template <>
-struct LeafChol<PT> {
-  static __device__ __forceinline__ void run(float (&)[PT], float &, int, int, int &) {}
+struct LeafCol<PW> {
+  static __device__ __forceinline__ void run(float (&)[PW], float &, float, float &, float *,
+                                             float *, int) {}
 };
 
-// Row I of the tile inverse for column c = lane:  x_I = (delta_Ic - sum_{l<I} L_Il x_l) / L_II
-// (row I of L read as float4; even and odd l summed apart)
-template <int I>
-struct LeafInv {
-  static __device__ __forceinline__ void run(float (&x)[PT], const float *Lt, const float *rd,
-                                             int lane) {
-    float a0 = (I == lane) ? 1.0f : 0.0f, a1 = 0.0f;
+// Factor the PW x PW tile at (t0, t0) of S in place (lower part; lanes >= PW carry zeros).
+// Returns the first column with a non-positive (or NaN) pivot, or -1.
+__device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float *cb, int t0,
+                                           int lane) {
+  const bool own = lane < PW;
+  float *row = S + (t0 + (own ? lane : 0)) * PL + t0;
+  float a[PW];
 #pragma unroll
-    for (int l4 = 0; l4 < (I + 3) / 4; ++l4) {
-      const float4 v = *reinterpret_cast<const float4 *>(Lt + I * PL + 4 * l4);
-      if (4 * l4 + 0 < I) a0 = fmaf(-v.x, x[4 * l4 + 0], a0);
-      if (4 * l4 + 1 < I) a1 = fmaf(-v.y, x[4 * l4 + 1], a1);
-      if (4 * l4 + 2 < I) a0 = fmaf(-v.z, x[4 * l4 + 2], a0);
-      if (4 * l4 + 3 < I) a1 = fmaf(-v.w, x[4 * l4 + 3], a1);
-    }
-    x[I] = (I < lane) ? 0.0f : (a0 + a1) * rd[I];
-    LeafInv<I + 1>::run(x, Lt, rd, lane);
-  }
-};
-template <>
-struct LeafInv<PT> {
-  static __device__ __forceinline__ void run(float (&)[PT], const float *, const float *, int) {}
-};
-
-// Factor + invert the 32 x 32 tile at (t0, t0) of S (lower part) into S and Li (tile
-// inverse, lower, at (t0, t0)), one warp.
-__device__ __forceinline__ void leaf_factor(float *S, float *Li, float *rd, int t0, int lane,
-                                            int &bad) {
-  float a[PT];
-  float *row = S + (t0 + lane) * PL + t0;
-#pragma unroll
-  for (int q = 0; q < PT / 4; ++q) {
+  for (int q = 0; q < PW / 4; ++q) {
     const float4 v = *reinterpret_cast<const float4 *>(row + 4 * q);
     a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
   }
 #pragma unroll
-  for (int l = 0; l < PT; ++l)
-    if (l > lane) a[l] = 0.0f;
+  for (int l = 0; l < PW; ++l)
+    if (l > lane || !own) a[l] = 0.0f;
+  float dg = own ? row[lane] : 1.0f;
+  const float p0 = __shfl_sync(0xffffffffu, dg, 0);
   float rdl = 0.0f;
-  LeafChol<0>::run(a, rdl, lane, t0, bad);
+  LeafCol<0>::run(a, dg, p0 > 0.0f ? rsqrtf(p0) : 0.0f, rdl, cb, M, lane);
+  if (own) {
 #pragma unroll
-  for (int q = 0; q < PT / 4; ++q)
-    *reinterpret_cast<float4 *>(row + 4 * q) =
-        make_float4(4 * q + 0 <= lane ? a[4 * q + 0] : 0.0f, 4 * q + 1 <= lane ? a[4 * q + 1] : 0.0f,
-                    4 * q + 2 <= lane ? a[4 * q + 2] : 0.0f, 4 * q + 3 <= lane ? a[4 * q + 3] : 0.0f);
-  rd[lane] = rdl;
-  __syncwarp();
-  float x[PT];
-  LeafInv<0>::run(x, S + t0 * PL + t0, rd, lane);
-#pragma unroll
-  for (int i = 0; i < PT; ++i) Li[(t0 + i) * PL + t0 + lane] = x[i];
-}
-
-// 4 rows (A rows m0..m0+3) x columns n = nb + lane + 32q (q < NQ) of sum_k A(m,k) B(n,k),
-// k < 32.  A(m, k) = Am[m * PL + k], B(n, k) = Bm[n * PL + k].
-template <int NQ>
-__device__ __forceinline__ void group_nt(const float *Am, const float *Bm, int m0, int nb,
-                                         int lane, float (&acc)[4][NQ]) {
-  float2 c2[4][NQ];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) c2[i][q] = make_float2(0.f, 0.f);
-#pragma unroll 2
-  for (int k = 0; k < PT; k += 4) {
-    float4 a[4], b[NQ];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Am + (m0 + i) * PL + k);
-#pragma unroll
-    for (int q = 0; q < NQ; ++q)
-      b[q] = *reinterpret_cast<const float4 *>(Bm + (nb + lane + 32 * q) * PL + k);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        c2[i][q] = __ffma2_rn(make_float2(a[i].x, a[i].y), make_float2(b[q].x, b[q].y), c2[i][q]);
-        c2[i][q] = __ffma2_rn(make_float2(a[i].z, a[i].w), make_float2(b[q].z, b[q].w), c2[i][q]);
-      }
+    for (int q = 0; q < PW / 4; ++q)
+      *reinterpret_cast<float4 *>(row + 4 * q) =
+          make_float4(4 * q + 0 <= lane ? a[4 * q + 0] : 0.0f, 4 * q + 1 <= lane ? a[4 * q + 1] : 0.0f,
+                      4 * q + 2 <= lane ? a[4 * q + 2] : 0.0f, 4 * q + 3 <= lane ? a[4 * q + 3] : 0.0f);
+    rd[lane] = rdl;
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) acc[i][q] = c2[i][q].x + c2[i][q].y;
+  // a failed pivot left rl = 0 in its lane
+  const unsigned badm = __ballot_sync(0xffffffffu, own && !(rdl > 0.0f));
+  return badm ? t0 + __ffs((int)badm) - 1 : -1;
 }
 
-// Cm[m][n] -= (Am Bm^T)[m][n] for the group's 4 rows and NQ column blocks from nb; with
-// `lower` only columns n <= m.
-template <int NQ>
-__device__ __forceinline__ void update_group(float *Cm, const float *Am, const float *Bm,
-                                             int m0, int nb, int lane, bool lower) {
-  float acc[4][NQ];
-  group_nt<NQ>(Am, Bm, m0, nb, lane, acc);
+// x L_pp^T = c for one row, in place: z_l -= z_j M[j][l] (l > j), then x_j = z_j / L_jj.
+template <int J>
+struct RowSolve {
+  static __device__ __forceinline__ void run(float (&x)[PW], const float *M) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      const int col = nb + lane + 32 * q;
-      if (!lower || col <= m0 + i) Cm[(m0 + i) * PL + col] -= acc[i][q];
+    for (int l4 = (J + 1) / 4; l4 < PW / 4; ++l4) {
+      const float4 v = *reinterpret_cast<const float4 *>(M + J * PL + 4 * l4);
+      if (4 * l4 + 0 > J) x[4 * l4 + 0] = fmaf(-x[J], v.x, x[4 * l4 + 0]);
+      if (4 * l4 + 1 > J) x[4 * l4 + 1] = fmaf(-x[J], v.y, x[4 * l4 + 1]);
+      if (4 * l4 + 2 > J) x[4 * l4 + 2] = fmaf(-x[J], v.z, x[4 * l4 + 2]);
+      if (4 * l4 + 3 > J) x[4 * l4 + 3] = fmaf(-x[J], v.w, x[4 * l4 + 3]);
     }
-}
-
-__device__ __forceinline__ void update_group_n(int nq, float *Cm, const float *Am,
-                                               const float *Bm, int m0, int nb, int lane,
-                                               bool lower) {
-  switch (nq) {
-    case 1: update_group<1>(Cm, Am, Bm, m0, nb, lane, lower); break;
-    case 2: update_group<2>(Cm, Am, Bm, m0, nb, lane, lower); break;
-    case 3: update_group<3>(Cm, Am, Bm, m0, nb, lane, lower); break;
-    default: break;
+    RowSolve<J + 1>::run(x, M);
   }
+};
+template <>
+struct RowSolve<PW> {
+  static __device__ __forceinline__ void run(float (&)[PW], const float *) {}
+};
+
+// Phase-2 tile: C rows m0..m0+7 (Cm), columns n0 + lane + 32q (q < 2), minus
+// sum_{k < PW} A(m, k) B(n, k) with A(m, k) = Am[m * PL + k], B(n, k) = Bm[n * PL + k];
+// columns >= NB skipped, and with `lower` also columns above the row.
+__device__ __forceinline__ void update_tile(float *Cm, const float *Am, const float *Bm,
+                                            int m0, int n0, int lane, bool lower) {
+  float2 c2[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c2[i][0] = c2[i][1] = make_float2(0.f, 0.f);
+  const int nb0 = min(n0 + lane, NB - 1), nb1 = min(n0 + 32 + lane, NB - 1);
+#pragma unroll
+  for (int k = 0; k < PW; k += 4) {
+    const float4 b0 = *reinterpret_cast<const float4 *>(Bm + nb0 * PL + k);
+    const float4 b1 = *reinterpret_cast<const float4 *>(Bm + nb1 * PL + k);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 a = *reinterpret_cast<const float4 *>(Am + (m0 + i) * PL + k);
+      c2[i][0] = __ffma2_rn(make_float2(a.x, a.y), make_float2(b0.x, b0.y), c2[i][0]);
+      c2[i][0] = __ffma2_rn(make_float2(a.z, a.w), make_float2(b0.z, b0.w), c2[i][0]);
+      c2[i][1] = __ffma2_rn(make_float2(a.x, a.y), make_float2(b1.x, b1.y), c2[i][1]);
+      c2[i][1] = __ffma2_rn(make_float2(a.z, a.w), make_float2(b1.z, b1.w), c2[i][1]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int col = n0 + lane + 32 * q;
+      if (col < NB && (!lower || col <= m0 + i)) Cm[(m0 + i) * PL + col] -= c2[i][q].x + c2[i][q].y;
+    }
 }
 
 __global__ void __launch_bounds__(PF_THREADS, 1)
@@ -262,14 +249,17 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
   extern __shared__ __align__(16) float psm[];
   float *S = psm;                // NB x PL: working block, becomes L (lower)
   float *Bt = psm + NB * PL;     // NB x PL: transposed right-hand side -> Linv^T
-  float *Li = Bt + NB * PL;      // PT x PL: current leaf's tile inverse (rows P0.., cols 0..)
-  float *rd = Li + PT * PL;      // PT reciprocal pivots of the current leaf
+  float *M = Bt + NB * PL;       // PW x PL: scaled transpose of the current leaf
+  float *rd = M + PW * PL;       // PW reciprocal pivots of the current leaf
+  __shared__ __align__(16) float cb[64];
   __shared__ int s_skip, s_bad;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   if (tid == 0) { s_skip = st->status != 0; s_bad = -1; }
   __syncthreads();
   if (s_skip) return;
-  for (int e = tid; e < NB * NB / 4; e += PF_THREADS) {
+#pragma unroll
+  for (int it = 0; it < NB * NB / 4 / PF_THREADS; ++it) {
+    const int e = it * PF_THREADS + tid;
     const int i = e / (NB / 4), l4 = 4 * (e % (NB / 4));
     float v[4];
     if (i < n && (d % 4) == 0 && l4 + 4 <= n) {
@@ -279,71 +269,76 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
 #pragma unroll
       for (int q = 0; q < 4; ++q) v[q] = (i < n && l4 + q < n) ? A[(k0 + i) * d + k0 + l4 + q] : 0.f;
     }
-    float sv[4], bv[4];
+    float sv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int l = l4 + q;
       sv[q] = (i < n && l < n) ? v[q] : (i == l ? 1.0f : 0.0f);
-      bv[q] = (i == l) ? 1.0f : 0.0f;
     }
     *reinterpret_cast<float4 *>(S + i * PL + l4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
-    *reinterpret_cast<float4 *>(Bt + i * PL + l4) = make_float4(bv[0], bv[1], bv[2], bv[3]);
   }
   __syncthreads();
-  int bad = -1;
 #pragma unroll 1
-  for (int p = 0; p < NB / PT; ++p) {
-    const int P0 = p * PT, R0 = P0 + PT;
-    const int ns = (NB - R0) / 4;  // row groups of S below the sub-panel
+  for (int p = 0; p < NB / PW; ++p) {
+    const int P0 = p * PW, R0 = P0 + PW;
     if (warp == 0) {
-      // the leaf writes its tile inverse at rows P0.. of a PT x PL scratch (shifted)
-      leaf_factor(S, Li - P0 * PL - P0, rd, P0, lane, bad);
+      const int bad = leaf_factor(S, M, rd, cb, P0, lane);
       if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
+    } else {
+      // identity rows P0..R0-1 of Bt, first read by this sub-panel's phase 1
+      for (int e = tid - 32; e < PW * NB / 4; e += PF_THREADS - 32) {
+        const int r = P0 + e / (NB / 4), c4 = 4 * (e % (NB / 4));
+        *reinterpret_cast<float4 *>(Bt + r * PL + c4) =
+            make_float4(r == c4 ? 1.f : 0.f, r == c4 + 1 ? 1.f : 0.f, r == c4 + 2 ? 1.f : 0.f,
+                        r == c4 + 3 ? 1.f : 0.f);
+      }
     }
     __syncthreads();
-    // phase 1: groups g < ns are rows R0 + 4g of S (trsm), the rest rows 4(g - ns) of Bt
-    // (inverse step a); 32 output columns each, in place (a group reads only its rows)
-#pragma unroll 1
-    for (int r = 0; r < 2; ++r) {
-      const int g = warp + 16 * r;
-      float *Cm = (g < ns) ? (S + P0) : (Bt + P0);
-      const int m0 = (g < ns) ? (R0 + 4 * g) : (4 * (g - ns));
-      float acc[4][1];
-      group_nt<1>(Cm, Li, m0, 0, lane, acc);
-      __syncwarp();
+    // phase 1: row r < R0 of Bt or row r >= R0 of S, columns P0..R0-1, one thread each
+    if (tid < NB) {
+      float *xr = (tid < R0 ? Bt : S) + tid * PL + P0;
+      float x[PW];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) Cm[(m0 + i) * PL + lane] = acc[i][0];
+      for (int q = 0; q < PW / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(xr + 4 * q);
+        x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+      }
+      RowSolve<0>::run(x, M);
+#pragma unroll
+      for (int q = 0; q < PW / 4; ++q) {
+        const float4 r = *reinterpret_cast<const float4 *>(rd + 4 * q);
+        *reinterpret_cast<float4 *>(xr + 4 * q) =
+            make_float4(x[4 * q] * r.x, x[4 * q + 1] * r.y, x[4 * q + 2] * r.z, x[4 * q + 3] * r.w);
+      }
     }
     __syncthreads();
-    // phase 2: syrk on S rows >= R0 (columns R0..row), inverse step b on Bt rows < R0
-    // (columns R0..NB-1); both read only columns P0..R0-1
+    // rows P0..R0-1 of Linv are final: Linv[i][c] = Yt[c][i] for c < R0, zero beyond
+    {
+      const int i4 = P0 + 4 * (tid / NB), c = tid % NB;   // PW * NB / 4 == PF_THREADS
+      const float4 v = c < R0 ? *reinterpret_cast<const float4 *>(Bt + c * PL + i4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+      const bool cc = c < n;
+      Linv[(i4 + 0) * NB + c] = (cc && i4 + 0 < n) ? v.x : 0.0f;
+      Linv[(i4 + 1) * NB + c] = (cc && i4 + 1 < n) ? v.y : 0.0f;
+      Linv[(i4 + 2) * NB + c] = (cc && i4 + 2 < n) ? v.z : 0.0f;
+      Linv[(i4 + 3) * NB + c] = (cc && i4 + 3 < n) ? v.w : 0.0f;
+    }
+    // phase 2 over 8-row tiles of [Bt rows < R0 ; S rows >= R0] x 64-column tiles from R0
+    const int nct = (NB - R0 + 63) / 64;
 #pragma unroll 1
-    for (int r = 0; r < 2; ++r) {
-      const int g = warp + 16 * r;
-      if (g < ns) {
-        const int m0 = R0 + 4 * g;
-        update_group_n((m0 + 3 - R0) / 32 + 1, S, S + P0, S + P0, m0, R0, lane, true);
-      } else {
-        update_group_n((NB - R0) / 32, Bt, Bt + P0, S + P0, 4 * (g - ns), R0, lane, false);
+    for (int t = warp; t < (NB / 8) * nct; t += PF_WARPS) {
+      const int m0 = 8 * (t / nct), n0 = R0 + 64 * (t % nct);
+      if (m0 < R0) {
+        update_tile(Bt, Bt + P0, S + P0, m0, n0, lane, false);
+      } else if (n0 <= m0 + 7) {
+        update_tile(S, S + P0, S + P0, m0, n0, lane, true);
       }
     }
     __syncthreads();
   }
-  if (s_bad >= 0) {
-    if (tid == 0 && s_bad < n && atomicCAS(&st->status, 0, (int)GPTQ_ERR_NOT_PD) == 0)
-      st->info = (int)(k0 + s_bad) + 1;
-    return;
-  }
-  // Linv[i][c] = Yt[c][i]
-  for (int e = tid; e < NB * NB / 4; e += PF_THREADS) {
-    const int i4 = 4 * (e / NB), c = e % NB;
-    const float4 v = *reinterpret_cast<const float4 *>(Bt + c * PL + i4);
-    const bool cc = c < n;
-    Linv[(i4 + 0) * NB + c] = (cc && i4 + 0 < n) ? v.x : 0.0f;
-    Linv[(i4 + 1) * NB + c] = (cc && i4 + 1 < n) ? v.y : 0.0f;
-    Linv[(i4 + 2) * NB + c] = (cc && i4 + 2 < n) ? v.z : 0.0f;
-    Linv[(i4 + 3) * NB + c] = (cc && i4 + 3 < n) ? v.w : 0.0f;
-  }
+  if (s_bad >= 0 && tid == 0 && s_bad < n &&
+      atomicCAS(&st->status, 0, (int)GPTQ_ERR_NOT_PD) == 0)
+    st->info = (int)(k0 + s_bad) + 1;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -524,7 +519,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
                            void *ws, cudaStream_t s) {
   static bool attr_done = false;
   const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);
-  const size_t potrf_smem = (2 * NB * PL + PT * PL + PT) * sizeof(float);
+  const size_t potrf_smem = (2 * NB * PL + PW * PL + PW) * sizeof(float);
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
