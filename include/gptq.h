@@ -90,6 +90,50 @@ gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, in
                                     gptq_stream_t stream);
 
 /*
+ * gptq_hessian_host_workspace_bytes: device staging workspace that
+ * gptq_hessian_accumulate_host needs for inputs of d_in channels streamed in chunks of
+ * chunk_tok tokens (0 = the default chunk: about 64 MiB of X, a multiple of 512 tokens).
+ * Returns 0 for an unknown dtype, d_in < 1 or chunk_tok < 0.
+ */
+size_t gptq_hessian_host_workspace_bytes(int xdtype, int64_t d_in, int64_t chunk_tok);
+
+/*
+ * gptq_hessian_accumulate_host: gptq_hessian_accumulate with X in HOST memory.
+ *
+ * Source: as gptq_hessian_accumulate ("tm_gptq_math", "Why it is second-order: the
+ * Hessian"); the pages accumulate the Gram matrix over the calibration set, which is what
+ * the chunks below do.  The pages have no counterpart to the host staging itself: it
+ * exists so that the calibration activations need not be resident on the GPU, and so that
+ * their transfer overlaps the Gram products.
+ *
+ * X is copied to the device in chunks of chunk_tok tokens through two staging buffers in
+ * `ws`; the copy of chunk c + 1 runs on a copy stream this library keeps per device while
+ * chunk c is accumulated into H on `stream`.  Chunks are accumulated in token order, each
+ * exactly as one gptq_hessian_accumulate call over that chunk would (so the fp32 sums are
+ * grouped by chunk; the result can differ in the last bits from one call over all tokens).
+ *
+ *   X_host     HOST [n_tok, ldx] elements of xdtype, first d_in columns used.  Page-locked
+ *              memory (cudaHostAlloc / cudaHostRegister) lets the copies overlap; pageable
+ *              memory gives the same result, but each copy then blocks the calling thread.
+ *              Must stay valid and unchanged until the work on `stream` has completed.
+ *   xdtype     GPTQ_F16, GPTQ_BF16 or GPTQ_F32;  d_in * sizeof(elem) a multiple of 16 bytes.
+ *   n_tok      >= 0;  ldx >= d_in (host rows may be strided; no alignment needed).
+ *   H          as gptq_hessian_accumulate (DEVICE, 16-byte aligned); `accumulate` applies
+ *              to the first chunk, later chunks always accumulate.
+ *   chunk_tok  tokens per chunk (0 = default); the same value as in the size query.
+ *   ws         DEVICE workspace, 256-byte aligned, of ws_bytes >=
+ *              gptq_hessian_host_workspace_bytes(xdtype, d_in, chunk_tok).
+ * Returns once everything is enqueued (for page-locked X); every copy and product is
+ * ordered before later work on `stream`, and the copies start only after earlier work on
+ * `stream` (which may still use `ws`) has finished.  Calls from several host threads are
+ * serialized while they enqueue.  Errors: INVALID_ARG, WORKSPACE, CUDA.
+ */
+gptq_status gptq_hessian_accumulate_host(const void *X_host, int xdtype, int64_t n_tok,
+                                         int64_t d_in, int64_t ldx, float *H, int accumulate,
+                                         int64_t chunk_tok, void *ws, size_t ws_bytes,
+                                         gptq_stream_t stream);
+
+/*
  * gptq_prepare_workspace_bytes: workspace size gptq_prepare needs for this d_in.
  */
 size_t gptq_prepare_workspace_bytes(int64_t d_in);

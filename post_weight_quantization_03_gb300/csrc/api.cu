@@ -56,6 +56,28 @@ gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, in
                         (cudaStream_t)stream);
 }
 
+size_t gptq_hessian_host_workspace_bytes(int xdtype, int64_t d_in, int64_t chunk_tok) {
+  const size_t es = elem_size(xdtype);
+  if (es == 0 || d_in < 1 || chunk_tok < 0) return 0;
+  return hessian_host_ws_bytes(d_in, es, chunk_tok);
+}
+
+gptq_status gptq_hessian_accumulate_host(const void *X_host, int xdtype, int64_t n_tok,
+                                         int64_t d_in, int64_t ldx, float *H, int accumulate,
+                                         int64_t chunk_tok, void *ws, size_t ws_bytes,
+                                         gptq_stream_t stream) {
+  const size_t es = elem_size(xdtype);
+  if (es == 0 || n_tok < 0 || d_in < 1 || ldx < d_in || chunk_tok < 0 || !H)
+    return GPTQ_ERR_INVALID_ARG;
+  if (n_tok > 0 && !X_host) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(H, 16) || (d_in * (int64_t)es) % 16 != 0) return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 20) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < hessian_host_ws_bytes(d_in, es, chunk_tok))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_hessian_host(X_host, xdtype, es, n_tok, d_in, ldx, H, accumulate ? 1 : 0,
+                             chunk_tok, ws, (cudaStream_t)stream);
+}
+
 size_t gptq_prepare_workspace_bytes(int64_t d_in) {
   if (d_in < 1) return 0;
   return prepare_ws_bytes(d_in);

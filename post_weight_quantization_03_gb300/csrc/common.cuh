@@ -84,6 +84,12 @@ __device__ __forceinline__ float tf32_head(float x) {
 gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
                            float *H, int accumulate, DevStatus *st, cudaStream_t s);
 
+// host_stream.cu: X streamed from host memory in chunks (see gptq_hessian_accumulate_host)
+size_t hessian_host_ws_bytes(int64_t d, size_t es, int64_t chunk_tok);
+gptq_status launch_hessian_host(const void *X_host, int xdtype, size_t es, int64_t n_tok,
+                                int64_t d, int64_t ldx, float *H, int accumulate,
+                                int64_t chunk_tok, void *ws, cudaStream_t s);
+
 // gemm.cu: C[m, n] (+)= alpha * sum_k A[m, k] * B[n, k], operands given as a TF32 head
 // and tail pair each (tail may be null = 0).  lower_only skips tiles strictly above the
 // diagonal of C (C square, row/col offsets equal).  trans_c stores C(m, n) at

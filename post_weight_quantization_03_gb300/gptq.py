@@ -30,6 +30,10 @@ _SIGS = {
     "gptq_kernel_launches": (_c.c_ulonglong, []),
     "gptq_hessian_accumulate": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
                                            _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
+    "gptq_hessian_host_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int64, _c.c_int64]),
+    "gptq_hessian_accumulate_host": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+                                                _c.c_int64, _c.c_void_p, _c.c_int, _c.c_int64,
+                                                _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_prepare_workspace_bytes": (_c.c_size_t, [_c.c_int64]),
     "gptq_prepare": (_c.c_int, [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_void_p, _c.c_void_p,
                                 _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
@@ -104,6 +108,16 @@ def gptq_kernel_launches():
 
 def gptq_hessian_accumulate(X, xdtype, n_tok, d_in, ldx, H, accumulate, stream):
     return load().gptq_hessian_accumulate(X, xdtype, n_tok, d_in, ldx, H, accumulate, stream)
+
+
+def gptq_hessian_host_workspace_bytes(xdtype, d_in, chunk_tok):
+    return load().gptq_hessian_host_workspace_bytes(xdtype, d_in, chunk_tok)
+
+
+def gptq_hessian_accumulate_host(X_host, xdtype, n_tok, d_in, ldx, H, accumulate, chunk_tok, ws,
+                                 ws_bytes, stream):
+    return load().gptq_hessian_accumulate_host(X_host, xdtype, n_tok, d_in, ldx, H, accumulate,
+                                               chunk_tok, ws, ws_bytes, stream)
 
 
 def gptq_prepare_workspace_bytes(d_in):
@@ -186,6 +200,28 @@ def hessian(X, H=None, accumulate=False, stream=None):
     _check(gptq_hessian_accumulate(_ptr(X), _dtype_code(X), n, d, X.stride(0), _ptr(H),
                                    1 if accumulate else 0, _stream(stream)),
            "gptq_hessian_accumulate")
+    return H
+
+
+def hessian_host(Xh, H=None, accumulate=False, chunk_tok=0, ws=None, device=None, stream=None):
+    """``H (+)= 2 X^T X`` for a token-major HOST matrix ``Xh`` (CPU tensor, pinned for the
+    copies to overlap), streamed to the device in chunks of ``chunk_tok`` tokens."""
+    torch = _torch()
+    if Xh.device.type != "cpu" or Xh.dim() != 2 or Xh.stride(1) != 1:
+        raise ValueError("Xh must be a row-major [n_tok, d_in] CPU matrix")
+    n, d = Xh.shape
+    dev = torch.device(device) if device is not None else (
+        H.device if H is not None else torch.device("cuda", torch.cuda.current_device()))
+    if H is None:
+        H = torch.empty(d, d, dtype=torch.float32, device=dev)
+        accumulate = False
+    need = gptq_hessian_host_workspace_bytes(_dtype_code(Xh), d, chunk_tok)
+    if ws is None:
+        ws = workspace(need, H.device)
+    _check(gptq_hessian_accumulate_host(ctypes.c_void_p(Xh.data_ptr()), _dtype_code(Xh), n, d,
+                                        Xh.stride(0), _ptr(H), 1 if accumulate else 0, chunk_tok,
+                                        _ptr(ws), ws.numel(), _stream(stream)),
+           "gptq_hessian_accumulate_host")
     return H
 
 

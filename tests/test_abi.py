@@ -39,6 +39,13 @@ def test_workspace_sizes(lib):
     q = gptq.gptq_quantize_workspace_bytes(4096, 4096, 4, 128)
     assert q >= 4096 * 4096 * 4 * 3  # fp32 working copy + split U^T
     assert gptq.gptq_quantize_workspace_bytes(0, 10, 4, 128) == 0
+    # host-streamed Hessian: two staging buffers of chunk_tok rows (default ~64 MiB each,
+    # a multiple of 512 tokens), 256-byte rounded
+    assert gptq.gptq_hessian_host_workspace_bytes(0, 4096, 0) == 2 * 8192 * 4096 * 2
+    assert gptq.gptq_hessian_host_workspace_bytes(0, 300, 1000) == 2 * 600064
+    assert gptq.gptq_hessian_host_workspace_bytes(9, 4096, 0) == 0
+    assert gptq.gptq_hessian_host_workspace_bytes(0, 0, 0) == 0
+    assert gptq.gptq_hessian_host_workspace_bytes(0, 64, -1) == 0
 
 
 P = ctypes.c_void_p
@@ -54,6 +61,13 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert gptq.gptq_hessian_accumulate(fake, 0, 10, 8, 8, None, 0, None) == INV
     # misaligned X row stride (f16, ldx = 9 -> 18 bytes)
     assert gptq.gptq_hessian_accumulate(fake, 0, 10, 8, 9, fake, 0, None) == INV
+    # host-streamed Hessian: bad chunk size, d_in pitch not 16 bytes, workspace
+    hh = gptq.gptq_hessian_accumulate_host
+    assert hh(fake, 0, 10, 8, 8, fake, 0, -1, fake, 1 << 30, None) == INV
+    assert hh(fake, 0, 10, 9, 9, fake, 0, 0, fake, 1 << 30, None) == INV
+    assert hh(None, 0, 10, 8, 8, fake, 0, 0, fake, 1 << 30, None) == INV
+    assert hh(fake, 0, 10, 8, 8, fake, 0, 64, fake, 16, None) == WS
+    assert hh(fake, 0, 10, 8, 8, fake, 0, 64, P(256 * 1024 + 8), 1 << 30, None) == WS
     # prepare: negative damp, missing or short workspace
     assert gptq.gptq_prepare(fake, 8, -1.0, fake, None, None, fake, 1 << 20, None) == INV
     assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, None, 0, None) == WS

@@ -106,6 +106,45 @@ def test_hessian_zero_tokens():
     assert torch.all(H == 0.0)
 
 
+@pytest.mark.parametrize("d,n,dtype,chunk,ld_pad", [
+    (384, 5000, "f16", 1024, 0),     # five chunks, ragged last one
+    (256, 3000, "bf16", 512, 5),     # strided host rows
+    (128, 700, "f32", 0, 0),         # default chunk: a single copy
+    (1024, 4096, "f16", 1536, 0),    # chunks not a multiple of the drain segment
+])
+def test_hessian_host_streamed(d, n, dtype, chunk, ld_pad):
+    spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=3, n_outlier=2, seed=d + n + 5)
+    X = _x(spec)
+    Xh = torch.zeros(n, d + ld_pad, dtype=X.dtype).pin_memory()
+    Xh[:, :d] = X
+    Hg = gptq.hessian_host(Xh[:, :d], chunk_tok=chunk, device=DEV)
+    torch.cuda.synchronize()
+    Hr = O.hessian(X.float().numpy() if dtype != "f32" else X.numpy())
+    Hg = Hg.cpu().numpy()
+    assert PT.rel_fro(Hg, Hr) <= PT.TOL_H
+    assert np.array_equal(Hg, Hg.T)
+    # one chunk holding every token is the device-resident call, bit for bit
+    if chunk == 0:
+        Hd = gptq.hessian(_padded(X)).cpu().numpy()
+        assert np.array_equal(Hg, Hd)
+
+
+def test_hessian_host_accumulates_and_reuses_workspace():
+    spec = S.ActivationSpec(d_in=320, n_tok=4000, dtype="f16", n_dead=1, seed=33)
+    X = _x(spec).pin_memory()
+    ws = gptq.workspace(gptq.gptq_hessian_host_workspace_bytes(0, 320, 768), DEV)
+    H = gptq.hessian_host(X[:1500], chunk_tok=768, ws=ws, device=DEV)
+    gptq.hessian_host(X[1500:], H, accumulate=True, chunk_tok=768, ws=ws)
+    Hr = O.hessian(X.float().numpy())
+    assert PT.rel_fro(H.cpu().numpy(), Hr) <= PT.TOL_H
+    # zero tokens: accumulate keeps H, otherwise H is cleared
+    H2 = torch.full((320, 320), 3.0, device=DEV)
+    gptq.hessian_host(X[:0], H2, accumulate=True, chunk_tok=768, ws=ws)
+    assert torch.all(H2 == 3.0)
+    gptq.hessian_host(X[:0], H2, accumulate=False, chunk_tok=768, ws=ws)
+    assert torch.all(H2 == 0.0)
+
+
 # ---------------------------------------------------------------------------------------
 # Steps 2-3: dead columns, damping, U
 # ---------------------------------------------------------------------------------------
