@@ -45,6 +45,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--n-tok", type=int, default=None, help="override token count (smaller runs)")
+    p.add_argument("--block", type=int, default=None,
+                   help="lazy-batch width B (default: the workload's, 128); 1 = eager "
+                        "column-at-a-time trailing updates")
     return p.parse_args()
 
 
@@ -218,7 +221,7 @@ def main():
 
     wl = S.WORKLOADS[args.workload]
     layer = wl.layers[0]
-    bits, block, damp = wl.bits[-1], wl.block, wl.damp
+    bits, block, damp = wl.bits[-1], args.block or wl.block, wl.damp
     act = layer.act
     if args.n_tok:
         from dataclasses import replace
@@ -292,6 +295,9 @@ def main():
     value = whole_job_value(weights, world, ms_step)
 
     peaks, peak_src = measured_peaks()
+    # trailing-update traffic of the sweep: each block reads and writes the fp32 working copy
+    # of every later column once (the per-block rank-B update); other traffic not counted
+    q_bytes = float(sum(m * (d - min(b0 + block, d)) * 8 for b0 in range(0, d, block)))
     h_flops = float(d) * (d + 1) * n
     h_tflops = h_flops / (st_h / 1e3) / 1e12
     peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -303,6 +309,17 @@ def main():
                 "algorithmic": f"d(d+1)N = {h_flops:.4e} flop per launch (lower triangle of "
                                f"2 X^T X incl. diagonal)",
                 "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"}
+    if st_q > st_h:
+        # the sweep dominates (small B): report it against HBM, from its trailing-update bytes
+        q_gbs = q_bytes / (st_q / 1e3) / 1e9
+        roofline = {"kernel": "quantize stage (gptq_quantize_layer: sweeps + trailing updates)",
+                    "bound": "hbm", "achieved": round(q_gbs, 1), "peak": float(peaks["hbm_gbs"]),
+                    "unit": "GB/s", "frac": round(q_gbs / float(peaks["hbm_gbs"]), 4),
+                    "traffic": None,
+                    "algorithmic": f"sum over blocks of d_out*(d_in - block end)*8 bytes = "
+                                   f"{q_bytes:.4e} per layer (fp32 read + write of the later "
+                                   f"columns per block)",
+                    "peak_source": f"{peak_src} copy bandwidth"}
 
     # ---- end to end through the C ABI from host buffers --------------------------------
     e2e = None
@@ -403,7 +420,7 @@ def run_reference(args, rank, world):
 
     wl = S.WORKLOADS[args.workload]
     layer = wl.layers[0]
-    bits, block, damp = wl.bits[-1], wl.block, wl.damp
+    bits, block, damp = wl.bits[-1], args.block or wl.block, wl.damp
     m, d, n = layer.d_out, layer.act.d_in, layer.act.n_tok
     X = S.activations(layer.act, device="cpu", n_tok=2048).float().numpy()
     W = S.layer_weights(layer).float().numpy()

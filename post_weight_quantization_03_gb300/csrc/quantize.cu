@@ -330,6 +330,57 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
 }
 
 // ---------------------------------------------------------------------------------------
+// Eager sweep (B = 1, "tm_gptq_math", "GPTQ's speedups: fixed order and lazy batches": the
+// column-at-a-time form whose per-column update of every later column the pages call
+// memory-bandwidth-bound).  One launch per column j: each CTA takes ER rows x EC later
+// columns; every thread quantizes its row's column j itself (the threads of a row reach
+// the same code) and applies w_k -= e U_jk to its four columns, so the later columns
+// stream through memory once per column.  Same arithmetic as the blocked sweep.
+// ---------------------------------------------------------------------------------------
+constexpr int EC = 256, ER = 32, E_THREADS = 256;  // 64 column threads (float4) x 4 rows
+
+__global__ void __launch_bounds__(E_THREADS)
+eager_column_kernel(float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t d, int64_t j,
+                    const float *__restrict__ U, const float *__restrict__ scale,
+                    const int32_t *__restrict__ zero, float maxq, uint8_t *__restrict__ codes,
+                    int64_t ldc) {
+  const int tx = threadIdx.x % 64, ty = threadIdx.x / 64;
+  const int64_t c = (((j + 1) >> 2) << 2) + (int64_t)blockIdx.x * EC + 4 * tx;
+  const float rd = 1.0f / U[j * d + j];
+  float u[4];
+  if ((d % 4) == 0 && c + 4 <= d) {
+    const float4 v = *reinterpret_cast<const float4 *>(U + j * d + c);
+    u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) u[q] = (c + q < d) ? U[j * d + c + q] : 0.0f;
+  }
+#pragma unroll 2
+  for (int rr = ty; rr < ER; rr += E_THREADS / 64) {
+    const int64_t r = (int64_t)blockIdx.y * ER + rr;
+    if (r >= m) break;
+    float *wr = Wf + r * ldwf;
+    const float wj = wr[j];
+    const float s = scale[r], z = (float)zero[r];
+    const float cd = fminf(fmaxf(rintf(__fdiv_rn(wj, s)) + z, 0.0f), maxq);
+    const float e = (wj - s * (cd - z)) * rd;
+    if (blockIdx.x == 0 && tx == 0) codes[r * ldc + j] = (uint8_t)cd;
+    if (c > j && c + 4 <= d) {
+      float4 w = *reinterpret_cast<float4 *>(wr + c);
+      w.x = fmaf(-e, u[0], w.x);
+      w.y = fmaf(-e, u[1], w.y);
+      w.z = fmaf(-e, u[2], w.z);
+      w.w = fmaf(-e, u[3], w.w);
+      *reinterpret_cast<float4 *>(wr + c) = w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)   // the float4 holding column j (never written) or the end
+        if (c + q > j && c + q < d) wr[c + q] = fmaf(-e, u[q], wr[c + q]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Pack codes into the row bitstream; write W_hat = scale * (code - zero).
 // One thread per output word.
 // ---------------------------------------------------------------------------------------
@@ -400,7 +451,7 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
   return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * SB * 4, 256) +
          2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
-         nblk * UD_FLOATS * 4;
+         (block > 1 ? nblk * UD_FLOATS * 4 : 0);   // B = 1 needs no packed diagonal blocks
 }
 
 gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
@@ -440,29 +491,42 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
     }
     GPTQ_LAUNCH_CHECK();
   }
-  {
-    dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
-    lt_split_kernel<<<tg, dim3(32, 8), 0, s>>>(U, d, q.Lhi, q.Llo, q.ldl);
-    GPTQ_LAUNCH_CHECK();
-    diag_blocks_kernel<<<(unsigned)ceil_div(d, block), 256, 0, s>>>(U, d, block, q.Ud);
-    GPTQ_LAUNCH_CHECK();
-  }
-  const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
-  for (int64_t b0 = 0; b0 < d; b0 += block) {
-    const int nb = (int)((d - b0) < block ? (d - b0) : block);
-    const int64_t b1 = b0 + nb;
-    sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
-        q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
-        q.Elo, q.codes, q.ldc, q.st);
-    GPTQ_LAUNCH_CHECK();
-    if (b1 < d) {
-      GemmArgs g{};
-      g.a_hi = q.Ehi; g.a_lo = q.Elo; g.lda = SB;
-      g.b_hi = q.Lhi + b1 * q.ldl + b0; g.b_lo = q.Llo + b1 * q.ldl + b0; g.ldb = q.ldl;
-      g.c = q.Wf + b1; g.ldc = q.ldwf;
-      g.M = m; g.N = d - b1; g.K = nb;
-      g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0;
-      GPTQ_TRY(launch_gemm_nt(g, q.st, s));
+  if (block == 1) {
+    // eager: one launch per column, U read in place
+    for (int64_t j = 0; j < d; ++j) {
+      const int64_t first = ((j + 1) >> 2) << 2;
+      dim3 eg((unsigned)(ceil_div(d - first, EC) > 0 ? ceil_div(d - first, EC) : 1),
+              (unsigned)ceil_div(m, ER));
+      eager_column_kernel<<<eg, E_THREADS, 0, s>>>(q.Wf, q.ldwf, m, d, j, U, scale, zero, maxq,
+                                                   q.codes, q.ldc);
+      GPTQ_LAUNCH_CHECK();
+    }
+  } else {
+    // blocked: in-block sweep, then one rank-B trailing update per block
+    {
+      dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
+      lt_split_kernel<<<tg, dim3(32, 8), 0, s>>>(U, d, q.Lhi, q.Llo, q.ldl);
+      GPTQ_LAUNCH_CHECK();
+      diag_blocks_kernel<<<(unsigned)ceil_div(d, block), 256, 0, s>>>(U, d, block, q.Ud);
+      GPTQ_LAUNCH_CHECK();
+    }
+    const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
+    for (int64_t b0 = 0; b0 < d; b0 += block) {
+      const int nb = (int)((d - b0) < block ? (d - b0) : block);
+      const int64_t b1 = b0 + nb;
+      sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
+          q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
+          q.Elo, q.codes, q.ldc, q.st);
+      GPTQ_LAUNCH_CHECK();
+      if (b1 < d) {
+        GemmArgs g{};
+        g.a_hi = q.Ehi; g.a_lo = q.Elo; g.lda = SB;
+        g.b_hi = q.Lhi + b1 * q.ldl + b0; g.b_lo = q.Llo + b1 * q.ldl + b0; g.ldb = q.ldl;
+        g.c = q.Wf + b1; g.ldc = q.ldwf;
+        g.M = m; g.N = d - b1; g.K = nb;
+        g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0;
+        GPTQ_TRY(launch_gemm_nt(g, q.st, s));
+      }
     }
   }
   {

@@ -8,7 +8,8 @@ oracle can afford:
     (pinned in the oracle tests), so it is checked against the oracle's factor of that
     block, damped with lambda from the full exact diagonal;
   * sweep: the oracle's U (at d_in = 4096, from a token prefix) or a seeded synthetic upper
-    factor (d_in = 11008, 28672) as the shared input, the oracle sweeping sampled rows;
+    factor (d_in = 11008, 28672) as the shared input, the oracle sweeping sampled rows (at
+    d_in = 4096 also with B = 1, the eager column-at-a-time variant);
   * shared-Hessian batching: rows of q/k/v (and gate/up) quantized in one call equal the
     separate calls bit for bit (rows decouple: "GPTQ Hessian").
 """
@@ -113,6 +114,10 @@ def test_layer4096_n262144():
     W = S.layer_weights(layer, DEV)
     st = _quantize_and_check(W, U32, dead_p, bits, np.arange(layer.d_out))
     assert st["entries"] == 4096 * 4096
+    # the eager variant (B = 1: a rank-1 update of every later column after each column),
+    # sampled rows against the oracle's column-at-a-time sweep
+    rows = np.sort(np.random.default_rng(5).choice(layer.d_out, 48, replace=False))
+    _quantize_and_check(W, U32, dead_p, bits, rows, block=1)
     # the whole path on the prefix: reconstruction error within 0.1 % of the oracle's
     Hg = gptq.hessian(Xg[:16384])
     U, dm, _ = gptq.prepare(Hg, wl.damp)
