@@ -216,6 +216,52 @@ gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_
                                 gptq_stream_t stream);
 
 /*
+ * GPTQ_MAX_SHARED_LAYERS: most layers one gptq_quantize_layers_shared call takes.
+ */
+#define GPTQ_MAX_SHARED_LAYERS 64
+
+/*
+ * gptq_quantize_shared_workspace_bytes: workspace size gptq_quantize_layers_shared needs
+ * for n_layers layers of d_out[i] rows (HOST array) and d_in columns.  0 for bad arguments.
+ */
+size_t gptq_quantize_shared_workspace_bytes(int n_layers, const int64_t *d_out, int64_t d_in,
+                                            int bits, int block);
+
+/*
+ * gptq_quantize_layers_shared: the column sweep of several layers that read the same
+ * inputs, sharing one U.
+ *
+ * Source: "GPTQ Hessian" -- H depends on the layer inputs only and every row of W shares
+ * it, and the rows are quantized independently of one another.  Layers fed by the same
+ * inputs (the query, key and value projections of an attention block; the gate and up
+ * projections of an MLP) therefore share H, its damping and U, and their rows can be swept
+ * as one stack.  The pages have no multi-layer call; this one avoids concatenating the
+ * weights on the caller's side and runs one sweep and one trailing update per block over
+ * all rows.
+ *
+ * Each layer's outputs are exactly those of gptq_quantize_layer on that layer alone (same
+ * codes, scales, zeros and W_hat, bit for bit).
+ *
+ *   n_layers   1 .. GPTQ_MAX_SHARED_LAYERS.
+ *   W, wdtype, d_out, ldw, qpacked, scale, zero
+ *              HOST arrays of n_layers entries; entry i describes layer i exactly as the
+ *              same-named argument of gptq_quantize_layer (the pointers are DEVICE pointers).
+ *   W_hat      HOST array of n_layers DEVICE pointers (entries may be NULL), or NULL.
+ *   d_in, U, dead_mask, bits, block: shared by all layers, as in gptq_quantize_layer.
+ *   ws         workspace of ws_bytes >= gptq_quantize_shared_workspace_bytes(...).
+ * The host arrays are read during the call only.  Asynchronous.  Errors: INVALID_ARG,
+ * WORKSPACE, UNSUPPORTED, CUDA; non-finite weights are flagged in the workspace
+ * (gptq_workspace_status).
+ */
+gptq_status gptq_quantize_layers_shared(int n_layers, const void *const *W, const int *wdtype,
+                                        const int64_t *d_out, const int64_t *ldw, int64_t d_in,
+                                        const float *U, const uint8_t *dead_mask, int bits,
+                                        int block, uint32_t *const *qpacked,
+                                        float *const *scale, int32_t *const *zero,
+                                        float *const *W_hat, void *ws, size_t ws_bytes,
+                                        gptq_stream_t stream);
+
+/*
  * GPTQ_NOALLOC_SCRATCH_BYTES: size of the fixed scratch array behind
  * gptq_quantize_layer_noalloc (32 MiB, held on every GPU that loads this library until the
  * process exits).  A layer fits when

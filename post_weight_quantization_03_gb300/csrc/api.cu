@@ -123,6 +123,47 @@ gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_
                          scale, zero, W_hat, ws, (cudaStream_t)stream);
 }
 
+size_t gptq_quantize_shared_workspace_bytes(int n_layers, const int64_t *d_out, int64_t d_in,
+                                            int bits, int block) {
+  if (n_layers < 1 || n_layers > GPTQ_MAX_SHARED_LAYERS || !d_out || d_in < 1) return 0;
+  for (int i = 0; i < n_layers; ++i)
+    if (d_out[i] < 1) return 0;
+  return quantize_layers_ws_bytes(d_out, n_layers, d_in, bits, block);
+}
+
+gptq_status gptq_quantize_layers_shared(int n_layers, const void *const *W, const int *wdtype,
+                                        const int64_t *d_out, const int64_t *ldw, int64_t d_in,
+                                        const float *U, const uint8_t *dead_mask, int bits,
+                                        int block, uint32_t *const *qpacked,
+                                        float *const *scale, int32_t *const *zero,
+                                        float *const *W_hat, void *ws, size_t ws_bytes,
+                                        gptq_stream_t stream) {
+  if (n_layers < 1 || n_layers > GPTQ_MAX_SHARED_LAYERS) return GPTQ_ERR_INVALID_ARG;
+  if (!W || !wdtype || !d_out || !ldw || !qpacked || !scale || !zero || !U || d_in < 1)
+    return GPTQ_ERR_INVALID_ARG;
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
+  if (block < 1 || block > 128 || !aligned(U, 16)) return GPTQ_ERR_INVALID_ARG;
+  QLayer L[GPTQ_MAX_SHARED_LAYERS];
+  int64_t rows = 0;
+  for (int i = 0; i < n_layers; ++i) {
+    const size_t es = elem_size(wdtype[i]);
+    float *wh = W_hat ? W_hat[i] : nullptr;
+    if (es == 0 || !W[i] || !qpacked[i] || !scale[i] || !zero[i]) return GPTQ_ERR_INVALID_ARG;
+    if (d_out[i] < 1 || ldw[i] < d_in) return GPTQ_ERR_INVALID_ARG;
+    if (!aligned(W[i], es) || !aligned(qpacked[i], 4) || !aligned(scale[i], 4) ||
+        !aligned(zero[i], 4) || (wh && !aligned(wh, 4)))
+      return GPTQ_ERR_INVALID_ARG;
+    rows += d_out[i];
+    L[i] = QLayer{W[i], wdtype[i], d_out[i], ldw[i], qpacked[i], scale[i], zero[i], wh};
+  }
+  if (d_in > (int64_t)1 << 17 || rows > (int64_t)1 << 24) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) ||
+      ws_bytes < quantize_layers_ws_bytes(d_out, n_layers, d_in, bits, block))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_quantize_layers(L, n_layers, d_in, U, dead_mask, bits, block, ws,
+                                (cudaStream_t)stream);
+}
+
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {
   if (!ws || !aligned(ws, 256)) return GPTQ_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

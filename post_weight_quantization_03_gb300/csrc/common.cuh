@@ -119,5 +119,14 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
                             uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
                             void *ws, cudaStream_t s);
 size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block);
+// Several layers sharing U, swept as one stack of rows (gptq_quantize_layers_shared).
+struct QLayer {
+  const void *W; int wdtype; int64_t m; int64_t ldw;
+  uint32_t *qpacked; float *scale; int32_t *zero; float *W_hat;
+};
+gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
+                                   const uint8_t *dead_mask, int bits, int block, void *ws,
+                                   cudaStream_t s);
+size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, int block);
 
 }  // namespace gptq

@@ -454,10 +454,50 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
          (block > 1 ? nblk * UD_FLOATS * 4 : 0);   // B = 1 needs no packed diagonal blocks
 }
 
-gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
-                            const float *U, const uint8_t *dead_mask, int bits, int block,
-                            uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
-                            void *ws, cudaStream_t s) {
+namespace {
+
+gptq_status launch_grid(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                        const uint8_t *dead_mask, float maxq, float *scale, int32_t *zero,
+                        float *Wf, int64_t ldwf, DevStatus *st, cudaStream_t s) {
+  const int warps = 8;
+  const unsigned g = (unsigned)ceil_div(m, warps);
+  switch (wdtype) {
+    case GPTQ_F32:
+      grid_kernel<float><<<g, warps * 32, 0, s>>>((const float *)W, m, d, ldw, dead_mask, maxq,
+                                                  scale, zero, Wf, ldwf, st);
+      break;
+    case GPTQ_F16:
+      grid_kernel<__half><<<g, warps * 32, 0, s>>>((const __half *)W, m, d, ldw, dead_mask,
+                                                   maxq, scale, zero, Wf, ldwf, st);
+      break;
+    case GPTQ_BF16:
+      grid_kernel<__nv_bfloat16><<<g, warps * 32, 0, s>>>((const __nv_bfloat16 *)W, m, d, ldw,
+                                                          dead_mask, maxq, scale, zero, Wf, ldwf,
+                                                          st);
+      break;
+    default:
+      return GPTQ_ERR_INVALID_ARG;
+  }
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+}  // namespace
+
+size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, int block) {
+  int64_t mt = 0;
+  for (int i = 0; i < n; ++i) mt += m[i];
+  const size_t base = quantize_ws_bytes(mt, d, bits, block);
+  return n == 1 ? base : base + 2 * round_up((size_t)mt * 4, 256);
+}
+
+// Layers that share U are swept as one matrix of their stacked rows (rows decouple:
+// "GPTQ Hessian"): one grid pass per layer into the shared fp32 working copy, one sweep and
+// one trailing update per block over all rows, then each layer's rows packed into its own
+// outputs.  With one layer the per-row scale and zero are written in place.
+gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
+                                   const uint8_t *dead_mask, int bits, int block, void *ws,
+                                   cudaStream_t s) {
   static bool attr_done = false;
   const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
   if (!attr_done) {
@@ -466,31 +506,21 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
                                          (int)sweep_smem));
     attr_done = true;
   }
+  int64_t m = 0;
+  for (int i = 0; i < n; ++i) m += L[i].m;
   QuantWs q = carve_quantize(ws, m, d);
+  float *scale = L[0].scale;
+  int32_t *zero = L[0].zero;
+  if (n > 1) {
+    char *p = (char *)ws + quantize_ws_bytes(m, d, bits, block);
+    scale = (float *)p;
+    zero = (int32_t *)(p + round_up((size_t)m * 4, 256));
+  }
   const float maxq = (float)((1 << bits) - 1);
   GPTQ_CUDA_CHECK(cudaMemsetAsync(q.st, 0, sizeof(DevStatus), s));
-  {
-    const int warps = 8;
-    const unsigned g = (unsigned)ceil_div(m, warps);
-    switch (wdtype) {
-      case GPTQ_F32:
-        grid_kernel<float><<<g, warps * 32, 0, s>>>((const float *)W, m, d, ldw, dead_mask,
-                                                    maxq, scale, zero, q.Wf, q.ldwf, q.st);
-        break;
-      case GPTQ_F16:
-        grid_kernel<__half><<<g, warps * 32, 0, s>>>((const __half *)W, m, d, ldw, dead_mask,
-                                                     maxq, scale, zero, q.Wf, q.ldwf, q.st);
-        break;
-      case GPTQ_BF16:
-        grid_kernel<__nv_bfloat16><<<g, warps * 32, 0, s>>>(
-            (const __nv_bfloat16 *)W, m, d, ldw, dead_mask, maxq, scale, zero, q.Wf, q.ldwf,
-            q.st);
-        break;
-      default:
-        return GPTQ_ERR_INVALID_ARG;
-    }
-    GPTQ_LAUNCH_CHECK();
-  }
+  for (int64_t i = 0, off = 0; i < n; off += L[i].m, ++i)
+    GPTQ_TRY(launch_grid(L[i].W, L[i].wdtype, L[i].m, d, L[i].ldw, dead_mask, maxq,
+                         scale + off, zero + off, q.Wf + off * q.ldwf, q.ldwf, q.st, s));
   if (block == 1) {
     // eager: one launch per column, U read in place
     for (int64_t j = 0; j < d; ++j) {
@@ -529,16 +559,32 @@ gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int
       }
     }
   }
-  {
-    const int64_t words = ceil_div(d, 32) * bits;
-    pack_kernel<<<2048, 256, 0, s>>>(q.codes, q.ldc, m, d, bits, words, qpacked);
+  const int64_t words = ceil_div(d, 32) * bits;
+  for (int64_t i = 0, off = 0; i < n; off += L[i].m, ++i) {
+    const uint8_t *codes = q.codes + off * q.ldc;
+    pack_kernel<<<2048, 256, 0, s>>>(codes, q.ldc, L[i].m, d, bits, words, L[i].qpacked);
     GPTQ_LAUNCH_CHECK();
-    if (W_hat) {
-      dequant_kernel<<<2048, 256, 0, s>>>(q.codes, q.ldc, m, d, scale, zero, W_hat);
+    if (L[i].W_hat) {
+      dequant_kernel<<<2048, 256, 0, s>>>(codes, q.ldc, L[i].m, d, scale + off, zero + off,
+                                          L[i].W_hat);
       GPTQ_LAUNCH_CHECK();
+    }
+    if (n > 1) {
+      GPTQ_CUDA_CHECK(cudaMemcpyAsync(L[i].scale, scale + off, L[i].m * 4,
+                                      cudaMemcpyDeviceToDevice, s));
+      GPTQ_CUDA_CHECK(cudaMemcpyAsync(L[i].zero, zero + off, L[i].m * 4,
+                                      cudaMemcpyDeviceToDevice, s));
     }
   }
   return GPTQ_OK;
+}
+
+gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                            const float *U, const uint8_t *dead_mask, int bits, int block,
+                            uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                            void *ws, cudaStream_t s) {
+  const QLayer one{W, wdtype, m, ldw, qpacked, scale, zero, W_hat};
+  return launch_quantize_layers(&one, 1, d, U, dead_mask, bits, block, ws, s);
 }
 
 

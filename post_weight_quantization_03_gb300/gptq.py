@@ -43,12 +43,20 @@ _SIGS = {
                                        _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                        _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_workspace_status": (_c.c_int, [_c.c_void_p, _c.c_void_p]),
+    "gptq_quantize_shared_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_void_p, _c.c_int64,
+                                                           _c.c_int, _c.c_int]),
+    "gptq_quantize_layers_shared": (_c.c_int, [_c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                               _c.c_void_p, _c.c_int64, _c.c_void_p,
+                                               _c.c_void_p, _c.c_int, _c.c_int, _c.c_void_p,
+                                               _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                               _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_quantize_layer_noalloc": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
                                                _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_int,
                                                _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                                _c.c_void_p, _c.c_void_p]),
 }
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GPTQ_NOALLOC_SCRATCH_BYTES in include/gptq.h
+MAX_SHARED_LAYERS = 64            # GPTQ_MAX_SHARED_LAYERS in include/gptq.h
 
 _lib = None
 
@@ -140,6 +148,17 @@ def gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, 
 
 def gptq_workspace_status(ws, stream):
     return load().gptq_workspace_status(ws, stream)
+
+
+def gptq_quantize_shared_workspace_bytes(n_layers, d_out, d_in, bits, block):
+    return load().gptq_quantize_shared_workspace_bytes(n_layers, d_out, d_in, bits, block)
+
+
+def gptq_quantize_layers_shared(n_layers, W, wdtype, d_out, ldw, d_in, U, dead_mask, bits, block,
+                                qpacked, scale, zero, W_hat, ws, ws_bytes, stream):
+    return load().gptq_quantize_layers_shared(n_layers, W, wdtype, d_out, ldw, d_in, U,
+                                              dead_mask, bits, block, qpacked, scale, zero,
+                                              W_hat, ws, ws_bytes, stream)
 
 
 def gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
@@ -274,3 +293,103 @@ def quantize(W, U, bits=4, block=128, dead_mask=None, want_w_hat=True, ws=None, 
                                _ptr(zero), _ptr(W_hat), _ptr(ws), ws.numel(), _stream(stream)),
            "gptq_quantize_layer")
     return qpacked, scale, zero, W_hat
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() if t is not None else None for t in ts])
+
+
+def quantize_shared(Ws, U, bits=4, block=128, dead_mask=None, want_w_hat=False, ws=None,
+                    stream=None):
+    """The sweep of several layers sharing U (one stack of rows).  Returns one
+    ``(qpacked, scale, zero, W_hat or None)`` tuple per layer."""
+    torch = _torch()
+    n = len(Ws)
+    d = Ws[0].shape[1]
+    for W in Ws:
+        if W.dim() != 2 or W.stride(1) != 1 or W.shape[1] != d:
+            raise ValueError("every W must be a row-major [d_out, d_in] matrix with one d_in")
+    dev = Ws[0].device
+    outs = []
+    for W in Ws:
+        m = W.shape[0]
+        outs.append((torch.empty(m, packed_words(d, bits), dtype=torch.int32, device=dev),
+                     torch.empty(m, dtype=torch.float32, device=dev),
+                     torch.empty(m, dtype=torch.int32, device=dev),
+                     torch.empty(m, d, dtype=torch.float32, device=dev) if want_w_hat else None))
+    d_out = (ctypes.c_int64 * n)(*[W.shape[0] for W in Ws])
+    if ws is None:
+        ws = workspace(gptq_quantize_shared_workspace_bytes(n, d_out, d, bits, block), dev)
+    _check(gptq_quantize_layers_shared(
+        n, _ptr_array(Ws), (ctypes.c_int * n)(*[_dtype_code(W) for W in Ws]), d_out,
+        (ctypes.c_int64 * n)(*[W.stride(0) for W in Ws]), d, _ptr(U), _ptr(dead_mask), bits,
+        block, _ptr_array([o[0] for o in outs]), _ptr_array([o[1] for o in outs]),
+        _ptr_array([o[2] for o in outs]),
+        _ptr_array([o[3] for o in outs]) if want_w_hat else None, _ptr(ws), ws.numel(),
+        _stream(stream)), "gptq_quantize_layers_shared")
+    return outs
+
+
+def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, overlap=True,
+                   stage_events=None):
+    """GPTQ over a block of layers grouped by their shared inputs.
+
+    ``groups`` is a list of ``(X, [W, ...])``: X the token-major inputs of the group (on the
+    device) and the weights of every layer that reads them.  Per group: H from X, one
+    prepare, then one shared sweep of all its layers per bit width.  With ``overlap`` the
+    Hessians are accumulated (in chunks of ``chunk_tok`` tokens, or in one call when None) on
+    a producer stream, ahead of the prepares and sweeps, which run on a higher-priority
+    stream; every step is a call of this library.  Returns ``[{bits: [(qpacked, scale, zero, None) per layer]}, ...]`` and
+    the dead-column counts, in group order."""
+    torch = _torch()
+    dev = groups[0][1][0].device
+    caller = torch.cuda.current_stream(dev)
+    lo, hi = torch.cuda.Stream.priority_range()
+    cons = torch.cuda.Stream(dev, priority=hi) if overlap else caller
+    prod = torch.cuda.Stream(dev, priority=lo) if overlap else caller
+    if overlap:
+        prod.wait_stream(caller)
+        cons.wait_stream(caller)
+    Hs, ready = [], []
+    for X, _ in groups:
+        d = X.shape[1]
+        H = torch.empty(d, d, dtype=torch.float32, device=dev)
+        if stage_events is not None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(prod)
+        step = chunk_tok or max(X.shape[0], 1)
+        for t0 in range(0, X.shape[0], step):
+            hessian(X[t0:t0 + step], H, accumulate=t0 > 0, stream=prod)
+        e = torch.cuda.Event(enable_timing=stage_events is not None)
+        e.record(prod)
+        if stage_events is not None:
+            stage_events.append(("hessian", e0, e))
+        Hs.append(H)
+        ready.append(e)
+    results, n_dead, keep = [], [], []
+    for (X, Ws), H, e in zip(groups, Hs, ready):
+        cons.wait_event(e)
+        d = X.shape[1]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(cons)
+        U, dm, nd = prepare(H, damp, stream=cons)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(cons)
+        m_rows = (ctypes.c_int64 * len(Ws))(*[W.shape[0] for W in Ws])
+        ws = workspace(max(gptq_quantize_shared_workspace_bytes(len(Ws), m_rows, d, b, block)
+                           for b in bits), dev)
+        res = {}
+        for b in bits:
+            res[b] = quantize_shared(Ws, U, b, block, dm, ws=ws, stream=cons)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e2.record(cons)
+        if stage_events is not None:
+            stage_events.append(("prepare", e0, e1))
+            stage_events.append(("quantize", e1, e2))
+        results.append(res)
+        n_dead.append(nd)
+        keep += [U, dm, ws]     # in use on the consumer stream until the waits below
+    if overlap:
+        caller.wait_stream(cons)
+        caller.wait_stream(prod)
+    return results, n_dead

@@ -46,6 +46,15 @@ def test_workspace_sizes(lib):
     assert gptq.gptq_hessian_host_workspace_bytes(9, 4096, 0) == 0
     assert gptq.gptq_hessian_host_workspace_bytes(0, 0, 0) == 0
     assert gptq.gptq_hessian_host_workspace_bytes(0, 64, -1) == 0
+    # shared sweep: the stacked rows' workspace plus the stacked scales and zeros
+    rows = (ctypes.c_int64 * 3)(4096, 4096, 4096)
+    assert gptq.gptq_quantize_shared_workspace_bytes(3, rows, 4096, 4, 128) == \
+        gptq.gptq_quantize_workspace_bytes(12288, 4096, 4, 128) + 2 * 12288 * 4
+    one = (ctypes.c_int64 * 1)(300)
+    assert gptq.gptq_quantize_shared_workspace_bytes(1, one, 200, 3, 128) == \
+        gptq.gptq_quantize_workspace_bytes(300, 200, 3, 128)
+    assert gptq.gptq_quantize_shared_workspace_bytes(0, rows, 4096, 4, 128) == 0
+    assert gptq.gptq_quantize_shared_workspace_bytes(65, rows, 4096, 4, 128) == 0
 
 
 P = ctypes.c_void_p
@@ -68,6 +77,25 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert hh(None, 0, 10, 8, 8, fake, 0, 0, fake, 1 << 30, None) == INV
     assert hh(fake, 0, 10, 8, 8, fake, 0, 64, fake, 16, None) == WS
     assert hh(fake, 0, 10, 8, 8, fake, 0, 64, P(256 * 1024 + 8), 1 << 30, None) == WS
+    # shared multi-layer sweep: layer count, null arrays, bits, workspace
+    import ctypes as C
+    n1 = (C.c_int64 * 1)(4)
+    arr = (C.c_void_p * 1)(256 * 1024)
+    dts = (C.c_int * 1)(1)
+    lds = (C.c_int64 * 1)(8)
+    sh = gptq.gptq_quantize_layers_shared
+    assert sh(0, arr, dts, n1, lds, 8, fake, None, 4, 128, arr, arr, arr, None, fake, 1 << 30,
+              None) == INV
+    assert sh(65, arr, dts, n1, lds, 8, fake, None, 4, 128, arr, arr, arr, None, fake, 1 << 30,
+              None) == INV
+    assert sh(1, None, dts, n1, lds, 8, fake, None, 4, 128, arr, arr, arr, None, fake, 1 << 30,
+              None) == INV
+    assert sh(1, arr, dts, n1, lds, 8, fake, None, 5, 128, arr, arr, arr, None, fake, 1 << 30,
+              None) == INV
+    assert sh(1, arr, dts, n1, (C.c_int64 * 1)(7), 8, fake, None, 4, 128, arr, arr, arr, None,
+              fake, 1 << 30, None) == INV
+    assert sh(1, arr, dts, n1, lds, 8, fake, None, 4, 128, arr, arr, arr, None, fake, 16,
+              None) == WS
     # prepare: negative damp, missing or short workspace
     assert gptq.gptq_prepare(fake, 8, -1.0, fake, None, None, fake, 1 << 20, None) == INV
     assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, None, 0, None) == WS

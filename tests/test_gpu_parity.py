@@ -277,3 +277,47 @@ def test_layer_end_to_end_small(bits):
     _, q_rtn = O.rtn_quantize(W.numpy(), ref["scale"], ref["zero"], bits)
     assert e_gpu < O.reconstruction_error(W.numpy(), q_rtn, ref["H"])
     assert nd == 0
+
+
+# ---------------------------------------------------------------------------------------
+# Layers sharing one Hessian: the shared sweep and the block driver
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("block", [128, 32, 1])
+def test_quantize_shared_equals_separate_calls(block):
+    d = 384
+    _, U32, dmask = _quant_case(8, d, 4, block, "f32", seed=17, dead=3, outl=1)
+    U = torch.from_numpy(U32).to(DEV)
+    dm = torch.from_numpy(dmask.astype(np.uint8)).to(DEV)
+    Ws = [S.weights(96, d, 0.02, "bf16", 1).to(DEV), S.weights(130, d, 0.02, "f16", 2).to(DEV),
+          _padded(S.weights(64, d, 0.02, "f32", 3)), S.weights(1, d, 0.02, "bf16", 4).to(DEV)]
+    for bits in (3, 4):
+        shared = gptq.quantize_shared(Ws, U, bits, block, dm, want_w_hat=True)
+        sep = [gptq.quantize(W, U, bits, block, dm) for W in Ws]
+        torch.cuda.synchronize()
+        for a, b in zip(shared, sep):
+            for x, y in zip(a, b):
+                assert torch.equal(x, y)
+
+
+def test_quantize_block_driver_matches_per_layer_path():
+    # two input streams: a 3-layer group and a 2-layer group, 3- and 4-bit
+    specs = [S.ActivationSpec(d_in=256, n_tok=3000, dtype="f16", n_dead=2, n_outlier=1, seed=41),
+             S.ActivationSpec(d_in=320, n_tok=2500, dtype="f16", n_dead=1, n_outlier=2, seed=42)]
+    groups = []
+    for i, sp in enumerate(specs):
+        X = S.activations(sp, device=DEV)
+        Ws = [S.weights(64 + 16 * j, sp.d_in, 0.02, "bf16", 10 * i + j).to(DEV)
+              for j in range(3 - i)]
+        groups.append((X, Ws))
+    for overlap in (True, False):
+        res, nd = gptq.quantize_block(groups, bits=(3, 4), overlap=overlap)
+        torch.cuda.synchronize()
+        for (X, Ws), r, n_dead in zip(groups, res, nd):
+            U, dm, nd_ref = gptq.prepare(gptq.hessian(X), 0.01)
+            assert n_dead == nd_ref
+            for bits in (3, 4):
+                for W, got in zip(Ws, r[bits]):
+                    ref = gptq.quantize(W, U, bits, 128, dm, want_w_hat=False)
+                    for x, y in zip(got[:3], ref[:3]):
+                        assert torch.equal(x, y)

@@ -10,8 +10,9 @@ oracle can afford:
   * sweep: the oracle's U (at d_in = 4096, from a token prefix) or a seeded synthetic upper
     factor (d_in = 11008, 28672) as the shared input, the oracle sweeping sampled rows (at
     d_in = 4096 also with B = 1, the eager column-at-a-time variant);
-  * shared-Hessian batching: rows of q/k/v (and gate/up) quantized in one call equal the
-    separate calls bit for bit (rows decouple: "GPTQ Hessian").
+  * shared-Hessian batching: rows of q/k/v (and gate/up) quantized in one call (stacked
+    rows, or the shared multi-layer call) equal the separate calls bit for bit (rows
+    decouple: "GPTQ Hessian").
 """
 
 import numpy as np
@@ -182,9 +183,11 @@ def test_block7b_n131072():
         for bits in wl.bits:
             sep = [gptq.quantize(w, U, bits, 128, dm, want_w_hat=False) for w in Ws]
             cat = gptq.quantize(torch.cat(Ws), U, bits, 128, dm, want_w_hat=False)
+            shared = gptq.quantize_shared(Ws, U, bits, 128, dm)
             torch.cuda.synchronize()
             for k in range(3):
                 assert torch.equal(cat[k], torch.cat([s[k] for s in sep]))
+                assert torch.equal(cat[k], torch.cat([s[k] for s in shared]))
         del U, Ws
         _free()
     # o_proj at 3 and 4 bits against the oracle (U from an 8192-token prefix), sampled rows
