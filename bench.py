@@ -45,6 +45,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--n-tok", type=int, default=None, help="override token count (smaller runs)")
+    p.add_argument("--recon", action="store_true",
+                   help="time the consumer instead: per-row ||(W - W_hat) X^T||^2 from the "
+                        "packed codes, on X (gptq_recon_error)")
     p.add_argument("--block", type=int, default=None,
                    help="lazy-batch width B (default: the workload's, 128); 1 = eager "
                         "column-at-a-time trailing updates")
@@ -250,6 +253,9 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    if args.recon:
+        return run_recon(args, wl, layer, X, W, H, U, dm, qp, sc, zr, ws_p, ws_q, bits, block,
+                         damp, stream, dev, rank, world)
 
     def step(record=None):
         e = [ev() for _ in range(4)] if record is not None else None
@@ -409,6 +415,61 @@ def main():
         print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_recon(args, wl, layer, X, W, H, U, dm, qp, sc, zr, ws_p, ws_q, bits, block, damp,
+              stream, dev, rank, world):
+    """The consumer of the quantized layer, timed alone: per-row output error on X from the
+    packed codes (one dequant-difference pass, one tcgen05 product, one reduction)."""
+    import torch
+    from post_weight_quantization_03_gb300 import gptq
+    gptq.hessian(X, H, stream=stream)
+    gptq.prepare(H, damp, U=U, dead_mask=dm, ws=ws_p, stream=stream)
+    gptq.quantize(W, U, bits, block, dm, ws=ws_q, stream=stream, out=(qp, sc, zr, None))
+    m, d, n = W.shape[0], W.shape[1], X.shape[0]
+    ws_r = gptq.workspace(gptq.gptq_recon_error_workspace_bytes(gptq._dtype_code(X), m, d, n),
+                          dev)
+    for _ in range(max(3, args.warmup)):
+        err = gptq.recon_error(X, W, qp, bits, sc, zr, ws=ws_r, stream=stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.4)
+    launches0 = gptq.gptq_kernel_launches()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        err = gptq.recon_error(X, W, qp, bits, sc, zr, ws=ws_r, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    launches = gptq.gptq_kernel_launches() - launches0
+    clk = clocks.stop()
+    ms = a.elapsed_time(b) / args.steps
+    flops = 2.0 * m * d * n
+    peaks, peak_src = measured_peaks()
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    tf = flops / (ms / 1e3) / 1e12
+    out = {
+        "metric": "ms per layer & tokens/sec evaluating ||(W - W_hat) X^T||^2 per row from the "
+                  "packed codes (4096x4096 int4)",
+        "value": n / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": wl.name, "d_out": m, "d_in": d, "n_tok": n, "bits": bits,
+                   "x_dtype": layer.act.dtype,
+                   "l2": f"inputs exceed L2: X is {X.numel() * X.element_size() / 1e9:.2f} GB"},
+        "total_error": float(err.double().sum().item()),
+        "roofline": {"kernel": "recon_tc_kernel (tcgen05 kind::f16, (W - W_hat) X^T with the "
+                               "row sums of squares in the epilogue)",
+                     "bound": "tensor", "achieved": round(tf, 3), "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": round(tf / peak_t, 4), "traffic": None,
+                     "algorithmic": f"2 d_out d_in N = {flops:.4e} flop per call (the whole "
+                                    f"call timed: difference pass + product + reduction)",
+                     "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
 
 
 def run_block(args, wl, dev, rank, world):

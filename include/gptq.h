@@ -262,6 +262,41 @@ gptq_status gptq_quantize_layers_shared(int n_layers, const void *const *W, cons
                                         gptq_stream_t stream);
 
 /*
+ * gptq_recon_error_workspace_bytes: workspace size gptq_recon_error needs.  0 for bad
+ * arguments.
+ */
+size_t gptq_recon_error_workspace_bytes(int xdtype, int64_t d_out, int64_t d_in,
+                                        int64_t n_tok);
+
+/*
+ * gptq_recon_error: per-row output error of a quantized layer on its inputs,
+ *   err[i] = sum_t ( (W_i - W_hat_i) . x_t )^2 ,   W_hat = scale * (code - zero),
+ * so that sum_i err[i] = ||W X^T - W_hat X^T||_F^2 with X token-major.
+ *
+ * Source: "tm_gptq_math", "The reconstruction objective, written out" -- GPTQ minimizes
+ * this squared output error, one row at a time, over the calibration inputs.  The codes are
+ * read from the packed form gptq_quantize_layer writes, so this is the consumer of the
+ * quantized layer; it evaluates the objective on X directly rather than through H.
+ *
+ *   X          [n_tok, ldx] of xdtype: GPTQ_F16 / GPTQ_BF16 (tensor cores: W - W_hat is
+ *              rounded to the same type, fp32 accumulation) or GPTQ_F32 (CUDA cores);
+ *              16-byte aligned, ldx * sizeof(elem) a multiple of 16 bytes.
+ *   W          [d_out, ldw] of wdtype, the layer's original weights.
+ *   qpacked, bits, scale, zero
+ *              as written by gptq_quantize_layer for this W (packed rows of
+ *              ceil(d_in/32) * bits words).
+ *   err        [d_out] fp32 out.
+ *   ws         workspace of ws_bytes >= gptq_recon_error_workspace_bytes(...).
+ * The row sums are combined in a fixed order: repeated calls give identical results.
+ * Asynchronous.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+gptq_status gptq_recon_error(const void *X, int xdtype, int64_t n_tok, int64_t d_in,
+                             int64_t ldx, const void *W, int wdtype, int64_t d_out, int64_t ldw,
+                             const uint32_t *qpacked, int bits, const float *scale,
+                             const int32_t *zero, float *err, void *ws, size_t ws_bytes,
+                             gptq_stream_t stream);
+
+/*
  * GPTQ_NOALLOC_SCRATCH_BYTES: size of the fixed scratch array behind
  * gptq_quantize_layer_noalloc (32 MiB, held on every GPU that loads this library until the
  * process exits).  A layer fits when

@@ -378,6 +378,22 @@ def reconstruction_error_direct(W, W_hat, X):
     return float(np.sum(Y * Y))
 
 
+def reconstruction_error_rows(W, W_hat, X):
+    """Per-row terms of ``||W X^T - W_hat X^T||_F^2``: ``err_i = sum_t ((W_i - W_hat_i) . x_t)^2``.
+
+    [TGM "The reconstruction objective, written out"]: the objective is a sum of independent
+    per-row output errors over the calibration tokens.  X may be given as a list of token
+    chunks (summed in order).
+    """
+    D = np.asarray(W, dtype=np.float64) - np.asarray(W_hat, dtype=np.float64)
+    chunks = X if isinstance(X, (list, tuple)) else [X]
+    err = np.zeros(D.shape[0])
+    for Xc in chunks:
+        Y = D @ np.asarray(Xc, dtype=np.float64).T
+        err += np.sum(Y * Y, axis=1)
+    return err
+
+
 # ---------------------------------------------------------------------------------------
 # The whole per-layer path
 # ---------------------------------------------------------------------------------------

@@ -164,6 +164,35 @@ gptq_status gptq_quantize_layers_shared(int n_layers, const void *const *W, cons
                                 (cudaStream_t)stream);
 }
 
+size_t gptq_recon_error_workspace_bytes(int xdtype, int64_t d_out, int64_t d_in,
+                                        int64_t n_tok) {
+  if (elem_size(xdtype) == 0 || d_out < 1 || d_in < 1 || n_tok < 0) return 0;
+  return recon_ws_bytes(xdtype, d_out, d_in, n_tok);
+}
+
+gptq_status gptq_recon_error(const void *X, int xdtype, int64_t n_tok, int64_t d_in,
+                             int64_t ldx, const void *W, int wdtype, int64_t d_out, int64_t ldw,
+                             const uint32_t *qpacked, int bits, const float *scale,
+                             const int32_t *zero, float *err, void *ws, size_t ws_bytes,
+                             gptq_stream_t stream) {
+  const size_t xes = elem_size(xdtype), wes = elem_size(wdtype);
+  if (xes == 0 || wes == 0 || n_tok < 0 || d_in < 1 || d_out < 1 || ldx < d_in ||
+      ldw < d_in || !W || !qpacked || !scale || !zero || !err)
+    return GPTQ_ERR_INVALID_ARG;
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
+  if (n_tok > 0 && (!X || !aligned(X, 16) || (ldx * (int64_t)xes) % 16 != 0))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, wes) || !aligned(qpacked, 4) || !aligned(scale, 4) || !aligned(zero, 4) ||
+      !aligned(err, 4))
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 20 || d_out > (int64_t)1 << 24 || n_tok > (int64_t)1 << 31)
+    return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < recon_ws_bytes(xdtype, d_out, d_in, n_tok))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_recon(X, xdtype, n_tok, d_in, ldx, W, wdtype, d_out, ldw, qpacked, bits, scale,
+                      zero, err, ws, (cudaStream_t)stream);
+}
+
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {
   if (!ws || !aligned(ws, 256)) return GPTQ_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

@@ -90,6 +90,13 @@ gptq_status launch_hessian_host(const void *X_host, int xdtype, size_t es, int64
                                 int64_t d, int64_t ldx, float *H, int accumulate,
                                 int64_t chunk_tok, void *ws, cudaStream_t s);
 
+// recon.cu: per-row ||(W - W_hat) X^T||^2 on X (gptq_recon_error)
+size_t recon_ws_bytes(int xdtype, int64_t m, int64_t d, int64_t n);
+gptq_status launch_recon(const void *X, int xdtype, int64_t n, int64_t d, int64_t ldx,
+                         const void *W, int wdtype, int64_t m, int64_t ldw, const uint32_t *qp,
+                         int bits, const float *scale, const int32_t *zero, float *err,
+                         void *ws, cudaStream_t s);
+
 // gemm.cu: C[m, n] (+)= alpha * sum_k A[m, k] * B[n, k], operands given as a TF32 head
 // and tail pair each (tail may be null = 0).  lower_only skips tiles strictly above the
 // diagonal of C (C square, row/col offsets equal).  trans_c stores C(m, n) at

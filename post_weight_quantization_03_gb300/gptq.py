@@ -43,6 +43,12 @@ _SIGS = {
                                        _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                        _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_workspace_status": (_c.c_int, [_c.c_void_p, _c.c_void_p]),
+    "gptq_recon_error_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_int64, _c.c_int64,
+                                                       _c.c_int64]),
+    "gptq_recon_error": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+                                    _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_void_p,
+                                    _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                    _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_quantize_shared_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_void_p, _c.c_int64,
                                                            _c.c_int, _c.c_int]),
     "gptq_quantize_layers_shared": (_c.c_int, [_c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
@@ -148,6 +154,16 @@ def gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, 
 
 def gptq_workspace_status(ws, stream):
     return load().gptq_workspace_status(ws, stream)
+
+
+def gptq_recon_error_workspace_bytes(xdtype, d_out, d_in, n_tok):
+    return load().gptq_recon_error_workspace_bytes(xdtype, d_out, d_in, n_tok)
+
+
+def gptq_recon_error(X, xdtype, n_tok, d_in, ldx, W, wdtype, d_out, ldw, qpacked, bits, scale,
+                     zero, err, ws, ws_bytes, stream):
+    return load().gptq_recon_error(X, xdtype, n_tok, d_in, ldx, W, wdtype, d_out, ldw, qpacked,
+                                   bits, scale, zero, err, ws, ws_bytes, stream)
 
 
 def gptq_quantize_shared_workspace_bytes(n_layers, d_out, d_in, bits, block):
@@ -393,3 +409,20 @@ def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, over
         caller.wait_stream(cons)
         caller.wait_stream(prod)
     return results, n_dead
+
+
+def recon_error(X, W, qpacked, bits, scale, zero, ws=None, stream=None):
+    """Per-row ``||(W - W_hat) X^T||^2`` from the packed codes (``[d_out]`` fp32)."""
+    torch = _torch()
+    n, d = X.shape
+    m = W.shape[0]
+    if X.stride(1) != 1 or W.stride(1) != 1 or W.shape[1] != d:
+        raise ValueError("X [n_tok, d_in] and W [d_out, d_in] must be row-major")
+    err = torch.empty(m, dtype=torch.float32, device=W.device)
+    if ws is None:
+        ws = workspace(gptq_recon_error_workspace_bytes(_dtype_code(X), m, d, n), W.device)
+    _check(gptq_recon_error(_ptr(X), _dtype_code(X), n, d, X.stride(0), _ptr(W), _dtype_code(W),
+                            m, d if W.stride(0) == d else W.stride(0), _ptr(qpacked), bits,
+                            _ptr(scale), _ptr(zero), _ptr(err), _ptr(ws), ws.numel(),
+                            _stream(stream)), "gptq_recon_error")
+    return err

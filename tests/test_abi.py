@@ -96,6 +96,21 @@ def test_invalid_arguments_rejected_before_launch(lib):
               fake, 1 << 30, None) == INV
     assert sh(1, arr, dts, n1, lds, 8, fake, None, 4, 128, arr, arr, arr, None, fake, 16,
               None) == WS
+    # reconstruction error: dtype, bits, X pitch, workspace
+    re = gptq.gptq_recon_error
+    assert re(fake, 9, 10, 8, 8, fake, 1, 4, 8, fake, 4, fake, fake, fake, fake, 1 << 30,
+              None) == INV
+    assert re(fake, 0, 10, 8, 8, fake, 1, 4, 8, fake, 5, fake, fake, fake, fake, 1 << 30,
+              None) == INV
+    assert re(fake, 0, 10, 8, 9, fake, 1, 4, 8, fake, 4, fake, fake, fake, fake, 1 << 30,
+              None) == INV
+    assert re(fake, 0, 10, 8, 8, fake, 1, 4, 8, fake, 4, fake, fake, None, fake, 1 << 30,
+              None) == INV
+    assert re(fake, 0, 10, 8, 8, fake, 1, 4, 8, fake, 4, fake, fake, fake, fake, 16,
+              None) == WS
+    assert gptq.gptq_recon_error_workspace_bytes(0, 4096, 4096, 262144) >= \
+        4096 * 4096 * 2 + 1024 * 4096 * 4
+    assert gptq.gptq_recon_error_workspace_bytes(9, 4, 8, 10) == 0
     # prepare: negative damp, missing or short workspace
     assert gptq.gptq_prepare(fake, 8, -1.0, fake, None, None, fake, 1 << 20, None) == INV
     assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, None, 0, None) == WS

@@ -321,3 +321,46 @@ def test_quantize_block_driver_matches_per_layer_path():
                     ref = gptq.quantize(W, U, bits, 128, dm, want_w_hat=False)
                     for x, y in zip(got[:3], ref[:3]):
                         assert torch.equal(x, y)
+
+
+# ---------------------------------------------------------------------------------------
+# The consumer: per-row ||(W - W_hat) X^T||^2 from the packed codes, on X
+# ---------------------------------------------------------------------------------------
+
+# W - W_hat is rounded to the activations' type before the tensor-core product (relative
+# error <= u = 2^-11 fp16, 2^-8 bf16 per entry).  With delta' = delta (1 + eps) the row
+# error moves by 2 delta H (delta o eps) + O(u^2), at most 2u of it: tolerance 2.5 u.
+REL_TOL = {"f16": 2.5 * 2.0 ** -11, "bf16": 2.5 * 2.0 ** -8, "f32": 1e-5}
+
+
+@pytest.mark.parametrize("m,d,n,bits,xdtype", [
+    (96, 384, 1000, 4, "f16"),
+    (130, 200, 777, 3, "f16"),      # ragged rows, tokens and K
+    (64, 256, 700, 3, "bf16"),
+    (256, 256, 512, 4, "f32"),      # the 256 x 256 fp32 layer
+    (300, 512, 3000, 2, "f16"),
+])
+def test_recon_error_parity(m, d, n, bits, xdtype):
+    spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=xdtype, n_dead=2, n_outlier=1, seed=m + d)
+    X = _x(spec)
+    Xn = X.float().numpy() if xdtype != "f32" else X.numpy()
+    W = S.weights(m, d, 0.02, "bf16", m + n)
+    U, dm, _ = gptq.prepare(gptq.hessian(_padded(X)), 0.01)
+    Wg = W.to(DEV)
+    qp, sc, zr, Wh = gptq.quantize(Wg, U, bits, 128, dm)
+    err = gptq.recon_error(_padded(X), Wg, qp, bits, sc, zr)
+    err2 = gptq.recon_error(_padded(X), Wg, qp, bits, sc, zr)
+    torch.cuda.synchronize()
+    ref = O.reconstruction_error_rows(W.float().numpy(), Wh.cpu().numpy(), Xn)
+    got = err.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - ref) / np.maximum(ref, 1e-30)) <= REL_TOL[xdtype]
+    assert torch.equal(err, err2)     # fixed-order reduction: repeatable
+
+
+def test_recon_error_zero_tokens():
+    d, m = 256, 64
+    X = torch.empty(0, d, dtype=torch.float16, device=DEV)
+    W = S.weights(m, d, 0.02, "bf16", 3).to(DEV)
+    U = torch.eye(d, device=DEV)
+    qp, sc, zr, _ = gptq.quantize(W, U, 4, 128)
+    assert torch.all(gptq.recon_error(X, W, qp, 4, sc, zr) == 0)

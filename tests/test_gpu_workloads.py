@@ -10,6 +10,8 @@ oracle can afford:
   * sweep: the oracle's U (at d_in = 4096, from a token prefix) or a seeded synthetic upper
     factor (d_in = 11008, 28672) as the shared input, the oracle sweeping sampled rows (at
     d_in = 4096 also with B = 1, the eager column-at-a-time variant);
+  * the consumer (per-row output error from the packed codes) over all tokens, sampled rows
+    against the oracle;
   * shared-Hessian batching: rows of q/k/v (and gate/up) quantized in one call (stacked
     rows, or the shared multi-layer call) equal the separate calls bit for bit (rows
     decouple: "GPTQ Hessian").
@@ -129,6 +131,12 @@ def test_layer4096_n262144():
     e_gpu = O.reconstruction_error(Wn, Wh.cpu().numpy(), Hp)
     e_ref = O.reconstruction_error(Wn, ref, Hp)
     assert abs(e_gpu - e_ref) <= PT.TOL_RECON * e_ref
+    # the consumer on all 262144 tokens, sampled rows against the oracle (token chunks)
+    err = gptq.recon_error(Xg, W, qp, bits, sc, zr).cpu().numpy().astype(np.float64)
+    rows = np.sort(np.random.default_rng(6).choice(layer.d_out, 24, replace=False))
+    chunks = [Xh[t:t + 32768] for t in range(0, Xh.shape[0], 32768)]
+    ref_rows = O.reconstruction_error_rows(Wn[rows], Wh.cpu().numpy()[rows], chunks)
+    assert np.max(np.abs(err[rows] - ref_rows) / ref_rows) <= 2.5 * 2.0 ** -11
 
 
 def test_mlp11008_n131072():

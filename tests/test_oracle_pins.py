@@ -197,6 +197,24 @@ def test_reconstruction_error_two_routes_agree():
     assert e1 == pytest.approx(e2, rel=1e-10)
 
 
+def test_reconstruction_error_rows_match_the_hessian_quadratic_forms():
+    # per row: sum_t (delta . x_t)^2 equals 1/2 delta H0 delta^T with H0 = 2 X^T X, over
+    # token chunks; one planted row with a single nonzero delta k reduces to 2 H0_kk / 2
+    X, W = correlated_problem(12, 20, 90, 3)
+    out = O.gptq_layer(X, W, 3)
+    rows = O.reconstruction_error_rows(W, out["W_hat"], [X[:40], X[40:]])
+    D = W.astype(np.float64) - out["W_hat"]
+    quad = 0.5 * np.einsum("ij,jk,ik->i", D, O.hessian(X), D)
+    np.testing.assert_allclose(rows, quad, rtol=1e-12)
+    assert rows.sum() == pytest.approx(O.reconstruction_error_direct(W, out["W_hat"], X),
+                                       rel=1e-12)
+    Wp = np.zeros((1, 20))
+    Wp[0, 7] = 0.5
+    one = O.reconstruction_error_rows(Wp, np.zeros((1, 20)), X)
+    assert one[0] == pytest.approx(0.25 * float(np.sum(X[:, 7].astype(np.float64) ** 2)),
+                                   rel=1e-13)
+
+
 # ---------------------------------------------------------------------------------------
 # P8: rows decouple ("GPTQ Hessian": every row has the same H); dead-column invariance
 # ---------------------------------------------------------------------------------------
