@@ -292,6 +292,78 @@ def obs_quantize_schur(W, Hd, scale, zero, bits, dead=None, maxq="bits"):
     return codes, W_hat
 
 
+def obq_greedy(W, Hd, scale, zero, bits, dead=None, forced=None, tie_tol=1e-3):
+    """OBQ: greedy per-row order with an explicit Schur downdate.
+
+    [TGM "Greedy quantization with error compensation"]: with F the free weights of a row
+    and H_F^-1 their inverse Hessian, quantizing weight q costs
+    ``(w_q - quant(w_q))^2 / [H_F^-1]_qq`` and the best correction of the others is
+    ``delta_F = -((w_q - quant(w_q)) / [H_F^-1]_qq) H_F^-1[:, q]``; OBQ quantizes the weight
+    of least cost first, row by row.  [MDU]: removing q from F is the rank-one downdate
+    ``H_F^-1 <- H_F^-1 - H_F^-1[:, q] H_F^-1[q, :] / [H_F^-1]_qq``.  Ties go to the lowest
+    index; codes as ``quantize_to_grid``.
+
+    ``forced = (order, codes)`` replays another implementation's decisions, row by row:
+    each forced column must be a least-cost column here up to ``slack`` (the cost gap
+    relative to the largest current cost, reported as ``max_slack``), and each forced code
+    must equal this rounding unless the pre-rounding value ``w/scale`` lies within
+    ``tie_tol`` of a rounding boundary (counted in ``tie_flips``; other differences in
+    ``bad_codes``).  Returns ``(codes, W_hat, order, info)``.
+    """
+    W = np.asarray(W, dtype=np.float64)
+    m, d = W.shape
+    maxq = 2 ** int(bits) - 1
+    Hinv0 = np.linalg.inv(np.asarray(Hd, dtype=np.float64))
+    s32 = np.asarray(scale, dtype=np.float32)
+    zr = np.asarray(zero, dtype=np.int64)
+    codes = np.zeros((m, d), dtype=np.int64)
+    W_hat = np.zeros((m, d), dtype=np.float64)
+    order = np.zeros((m, d), dtype=np.int64)
+    info = {"max_slack": 0.0, "tie_flips": 0, "bad_codes": 0, "bad_order": 0}
+    deadm = np.zeros(d, dtype=bool) if dead is None else np.asarray(dead, dtype=bool)
+    for i in range(m):
+        w = W[i].copy()
+        w[deadm] = 0.0
+        Hinv = Hinv0.copy()
+        free = np.ones(d, dtype=bool)
+        si, zi = s32[i:i + 1], zr[i:i + 1]
+        for step in range(d):
+            idx = np.flatnonzero(free)
+            c_all, q_all = quantize_to_grid(w[idx], np.repeat(si, idx.size),
+                                            np.repeat(zi, idx.size), maxq)
+            cost = (w[idx] - q_all) ** 2 / np.diag(Hinv)[idx]
+            k = int(np.argmin(cost))              # first minimum: lowest index
+            if forced is not None:
+                fq = int(forced[0][i, step])
+                pos = np.flatnonzero(idx == fq)
+                if pos.size != 1:
+                    info["bad_order"] += 1
+                    break
+                k = int(pos[0])
+                gap = (cost[k] - cost.min()) / max(cost.max(), 1e-300)
+                info["max_slack"] = max(info["max_slack"], float(gap))
+            q = int(idx[k])
+            c, qv = int(c_all[k]), float(q_all[k])
+            if forced is not None:
+                fc = int(forced[1][i, q])
+                if fc != c:
+                    x = float(np.float32(np.float32(w[q]) / si[0]))
+                    near = abs(abs(x - np.floor(x)) - 0.5) <= tie_tol
+                    if near and abs(fc - c) == 1:
+                        info["tie_flips"] += 1
+                    else:
+                        info["bad_codes"] += 1
+                    c = fc
+                    qv = float(si[0]) * float(c - zi[0])
+            e = (w[q] - qv) / Hinv[q, q]
+            w[free] -= e * Hinv[free, q]
+            w[q] = qv
+            codes[i, q], W_hat[i, q], order[i, step] = c, qv, q
+            Hinv = Hinv - np.outer(Hinv[:, q], Hinv[q, :]) / Hinv[q, q]
+            free[q] = False
+    return codes, W_hat, order, info
+
+
 def rtn_quantize(W, scale, zero, bits, dead=None):
     """Round-to-nearest on the same grid, every weight independently, no compensation.
 

@@ -367,3 +367,74 @@ def test_trailing_block_of_u_depends_only_on_trailing_block_of_h(t):
     U = O.inverse_cholesky_upper(Hd)
     Ut = O.inverse_cholesky_upper(Hd[t:, t:])
     np.testing.assert_allclose(U[t:, t:], Ut, rtol=0, atol=1e-12 * np.abs(U).max())
+
+
+# ---------------------------------------------------------------------------------------
+# OBQ greedy order (explicit Schur downdates)
+# ---------------------------------------------------------------------------------------
+
+def _obq_case(d=7, m=4, seed=5, bits=3):
+    X, W = correlated_problem(m, d, 60, seed)
+    Hd, dead, _ = O.damp_hessian(O.hessian(X))
+    s, z = O.row_grid(W, bits)
+    return W, Hd, s, z, dead
+
+
+def test_obq_first_choice_is_brute_force_least_increase():
+    # for every candidate q: fix w_q to its grid value, re-solve the other weights exactly,
+    # and measure the increase of 1/2 (v - w) H (v - w)^T; the least one is OBQ's first pick
+    W, Hd, s, z, _ = _obq_case()
+    bits, d = 3, W.shape[1]
+    codes, _, order, _ = O.obq_greedy(W, Hd, s, z, bits)
+    Hinv = np.linalg.inv(Hd)
+    for i in range(W.shape[0]):
+        inc = []
+        for q in range(d):
+            _, qv = O.quantize_to_grid(W[i, q:q + 1], s[i:i + 1], z[i:i + 1], 2 ** bits - 1)
+            F = [k for k in range(d) if k != q]
+            # v_F minimises (v - w) H (v - w)^T with v_q = qv
+            dq = qv[0] - W[i, q]
+            vF = W[i, F] - np.linalg.solve(Hd[np.ix_(F, F)], Hd[F, q] * dq)
+            v = W[i].astype(np.float64).copy()
+            v[q], v[F] = qv[0], vF
+            inc.append(0.5 * (v - W[i]) @ Hd @ (v - W[i]))
+            assert inc[-1] == pytest.approx(0.5 * dq * dq / Hinv[q, q], rel=1e-9)
+        assert order[i, 0] == int(np.argmin(inc))
+
+
+def test_obq_with_diagonal_hessian_is_rtn():
+    W, _, s, z, _ = _obq_case()
+    Hd = np.diag(np.linspace(0.5, 3.0, W.shape[1]))
+    codes, W_hat, _, _ = O.obq_greedy(W, Hd, s, z, 3)
+    c_rtn, q_rtn = O.rtn_quantize(W, s, z, 3)
+    assert np.array_equal(codes, c_rtn)
+    np.testing.assert_allclose(W_hat, q_rtn, rtol=0, atol=0)
+
+
+def test_obq_forced_left_to_right_is_the_fixed_order_sweep():
+    W, Hd, s, z, dead = _obq_case(d=9, m=5, seed=8, bits=4)
+    d = W.shape[1]
+    c_fix, q_fix = O.obs_quantize_schur(W, Hd, s, z, 4, dead=dead)
+    order = np.tile(np.arange(d), (W.shape[0], 1))
+    c, q, _, info = O.obq_greedy(W, Hd, s, z, 4, dead=dead, forced=(order, c_fix))
+    assert info["bad_codes"] == 0 and info["tie_flips"] == 0 and info["bad_order"] == 0
+    assert np.array_equal(c, c_fix)
+    np.testing.assert_allclose(q, q_fix, rtol=0, atol=1e-15)
+
+
+def test_obq_is_column_permutation_equivariant():
+    W, Hd, s, z, _ = _obq_case(d=8, m=3, seed=11)
+    p = np.random.default_rng(2).permutation(W.shape[1])
+    c, _, order, _ = O.obq_greedy(W, Hd, s, z, 3)
+    cp, _, order_p, _ = O.obq_greedy(W[:, p], Hd[np.ix_(p, p)], s, z, 3)
+    assert np.array_equal(cp, c[:, p])
+    assert np.array_equal(p[order_p], order)
+
+
+def test_obq_beats_rtn_on_correlated_inputs():
+    W, Hd, s, z, _ = _obq_case(d=10, m=6, seed=13, bits=3)
+    _, W_hat, order, _ = O.obq_greedy(W, Hd, s, z, 3)
+    _, q_rtn = O.rtn_quantize(W, s, z, 3)
+    for i in range(W.shape[0]):
+        assert sorted(order[i]) == list(range(W.shape[1]))
+    assert O.reconstruction_error(W, W_hat, Hd) < O.reconstruction_error(W, q_rtn, Hd)
