@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--recon", action="store_true",
                    help="time the consumer instead: per-row ||(W - W_hat) X^T||^2 from the "
                         "packed codes, on X (gptq_recon_error)")
+    p.add_argument("--obq", action="store_true",
+                   help="greedy-order OBQ against the fixed-order sweep on a 4096 x 128 layer "
+                        "(OBQ keeps a per-row inverse Hessian on chip: d_in <= 128)")
     p.add_argument("--block", type=int, default=None,
                    help="lazy-batch width B (default: the workload's, 128); 1 = eager "
                         "column-at-a-time trailing updates")
@@ -223,6 +226,8 @@ def main():
     gptq.load()
 
     wl = S.WORKLOADS[args.workload]
+    if args.obq:
+        return run_obq(args, dev, rank, world)
     if len(wl.layers) > 1:
         return run_block(args, wl, dev, rank, world)
     layer = wl.layers[0]
@@ -472,6 +477,85 @@ def run_recon(args, wl, layer, X, W, H, U, dm, qp, sc, zr, ws_p, ws_q, bits, blo
         print(json.dumps(out), flush=True)
 
 
+def run_obq(args, dev, rank, world):
+    """OBQ (greedy order, per-row Schur downdates) and the fixed-order sweep on one narrow
+    layer: time per call, and the output error of each (and of round-to-nearest) on X
+    through the packed codes."""
+    import torch
+    from post_weight_quantization_03_gb300 import gptq
+    from post_weight_quantization_03_gb300 import synthetic as S
+    m, d, n, bits = 4096, 128, args.n_tok or 65536, 4
+    act = S.ActivationSpec(d_in=d, n_tok=n, dtype="f16", n_dead=2, n_outlier=2, seed=77)
+    X = S.activations(act, device=dev)
+    W = S.weights(m, d, 0.02, "bf16", 78).to(dev)
+    U, dm, _ = gptq.prepare(gptq.hessian(X), 0.01)
+    ws_o = gptq.workspace(gptq.gptq_quantize_obq_workspace_bytes(m, d), dev)
+    ws_g = gptq.workspace(gptq.gptq_quantize_workspace_bytes(m, d, bits, 128), dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            out = fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            out = fn()
+        b.record()
+        torch.cuda.synchronize()
+        return out, a.elapsed_time(b) / args.steps
+
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    time.sleep(0.4)
+    launches0 = gptq.gptq_kernel_launches()
+    obq, ms_obq = timed(lambda: gptq.quantize_obq(W, U, bits, dm, ws=ws_o))
+    launches = (gptq.gptq_kernel_launches() - launches0) // (args.steps + max(3, args.warmup))
+    clk = clocks.stop()
+    gq, ms_gptq = timed(lambda: gptq.quantize(W, U, bits, 128, dm, ws=ws_g))
+
+    def errors(X, U, dm):
+        outs = (("obq", gptq.quantize_obq(W, U, bits, dm)),
+                ("gptq", gptq.quantize(W, U, bits, 128, dm)),
+                ("rtn", gptq.quantize(W, torch.eye(d, device=dev), bits, 128, dm)))
+        return {k: float(gptq.recon_error(X, W, o[0], bits, o[1], o[2]).double().sum().item())
+                for k, o in outs}
+
+    errs = {"2_outlier_channels": errors(X, U, dm)}
+    # the same layer on inputs without outlier channels
+    X0 = S.activations(S.ActivationSpec(d_in=d, n_tok=n, dtype="f16", n_dead=2, n_outlier=0,
+                                        seed=77), device=dev)
+    U0, dm0, _ = gptq.prepare(gptq.hessian(X0), 0.01)
+    errs["no_outlier_channels"] = errors(X0, U0, dm0)
+    peaks, _ = measured_peaks()
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_alu = nsm * 128 * 2 * sm_mhz * 1e6 / 1e12      # fp32 FMA lanes x 2 flop x clock
+    flops = 2.0 * m * sum(f * f for f in range(1, d + 1))  # Schur downdates of the free block
+    tf = flops / (ms_obq / 1e3) / 1e12
+    out = {
+        "metric": "ms per layer: OBQ greedy order vs fixed-order GPTQ (4096 x 128 int4)",
+        "value": m * d / (ms_obq / 1e3), "unit": "weights/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_obq,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "obq4096x128", "d_out": m, "d_in": d, "n_tok": n, "bits": bits,
+                   "x_dtype": "f16", "w_dtype": "bf16"},
+        "gptq_fixed_order_ms": ms_gptq,
+        "output_error_on_X": errs,
+        "roofline": {"kernel": "obq_kernel (one CTA per row, per-row inverse Hessian in shared "
+                               "memory)", "bound": "alu", "achieved": round(tf, 4),
+                     "peak": round(peak_alu, 2), "unit": "TFLOP/s",
+                     "frac": round(tf / peak_alu, 4), "traffic": None,
+                     "algorithmic": f"2 d_out sum_f f^2 = {flops:.4e} flop (rank-one downdates "
+                                    f"of the shrinking free block)",
+                     "peak_source": f"derived: {nsm} SMs x 128 fp32 lanes x 2 flop x "
+                                    f"{sm_mhz:.0f} MHz"},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_block(args, wl, dev, rank, world):
     """A block of layers grouped by shared inputs (one Hessian and one prepare per group,
     one shared sweep per group and bit width): overlapped producer/consumer schedule timed
@@ -559,6 +643,8 @@ def run_reference(args, rank, world):
     from post_weight_quantization_03_gb300 import synthetic as S
 
     wl = S.WORKLOADS[args.workload]
+    if args.obq:
+        return run_obq(args, dev, rank, world)
     if len(wl.layers) > 1:
         return run_block(args, wl, dev, rank, world)
     layer = wl.layers[0]

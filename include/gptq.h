@@ -297,6 +297,42 @@ gptq_status gptq_recon_error(const void *X, int xdtype, int64_t n_tok, int64_t d
                              gptq_stream_t stream);
 
 /*
+ * GPTQ_OBQ_MAX_D_IN: widest layer gptq_quantize_obq takes (its per-row inverse Hessian
+ * lives in on-chip shared memory).
+ */
+#define GPTQ_OBQ_MAX_D_IN 128
+
+/*
+ * gptq_quantize_obq_workspace_bytes: workspace size gptq_quantize_obq needs.  0 for bad
+ * arguments.
+ */
+size_t gptq_quantize_obq_workspace_bytes(int64_t d_out, int64_t d_in);
+
+/*
+ * gptq_quantize_obq: the greedy-order variant that GPTQ's fixed order replaces.
+ *
+ * Source: "tm_gptq_math", "Greedy quantization with error compensation" -- per row,
+ * quantize next the free weight whose rounding raises the output error least,
+ * (w_q - quant(w_q))^2 / [H_F^-1]_qq, and correct the other free weights by
+ * -((w_q - quant(w_q)) / [H_F^-1]_qq) H_F^-1[:, q]; "GPTQ › Mathematical Details of the
+ * Update" -- remove q from the free set by the rank-one Schur downdate of H_F^-1.  Every
+ * row follows its own order, so each row carries its own H_F^-1: O(d_in^3) per row, for
+ * small layers.  Costs are compared in fp32; ties go to the lowest column index.
+ *
+ * Same grid, dead-column handling and outputs as gptq_quantize_layer, plus:
+ *   U          [d_in, d_in] fp32 upper factor from gptq_prepare (H^-1 = U^T U is formed
+ *              from it).
+ *   d_in       1 .. GPTQ_OBQ_MAX_D_IN (else UNSUPPORTED).
+ *   order      [d_out, d_in] int32 out, or NULL: row i's columns in the order quantized.
+ *   ws         workspace of ws_bytes >= gptq_quantize_obq_workspace_bytes(d_out, d_in).
+ * Asynchronous.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+gptq_status gptq_quantize_obq(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                              int64_t ldw, const float *U, const uint8_t *dead_mask, int bits,
+                              uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                              int32_t *order, void *ws, size_t ws_bytes, gptq_stream_t stream);
+
+/*
  * GPTQ_NOALLOC_SCRATCH_BYTES: size of the fixed scratch array behind
  * gptq_quantize_layer_noalloc (32 MiB, held on every GPU that loads this library until the
  * process exits).  A layer fits when

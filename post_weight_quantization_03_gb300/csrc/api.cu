@@ -193,6 +193,29 @@ gptq_status gptq_recon_error(const void *X, int xdtype, int64_t n_tok, int64_t d
                       zero, err, ws, (cudaStream_t)stream);
 }
 
+size_t gptq_quantize_obq_workspace_bytes(int64_t d_out, int64_t d_in) {
+  if (d_out < 1 || d_in < 1) return 0;
+  return quantize_obq_ws_bytes(d_out, d_in);
+}
+
+gptq_status gptq_quantize_obq(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                              int64_t ldw, const float *U, const uint8_t *dead_mask, int bits,
+                              uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                              int32_t *order, void *ws, size_t ws_bytes, gptq_stream_t stream) {
+  const size_t es = elem_size(wdtype);
+  if (es == 0 || !W || !U || !qpacked || !scale || !zero) return GPTQ_ERR_INVALID_ARG;
+  if (d_out < 1 || d_in < 1 || ldw < d_in) return GPTQ_ERR_INVALID_ARG;
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, es) || !aligned(U, 4) || !aligned(qpacked, 4) || !aligned(scale, 4) ||
+      !aligned(zero, 4) || (W_hat && !aligned(W_hat, 4)) || (order && !aligned(order, 4)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_in > GPTQ_OBQ_MAX_D_IN || d_out > (int64_t)1 << 24) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < quantize_obq_ws_bytes(d_out, d_in))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_quantize_obq(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, qpacked, scale,
+                             zero, W_hat, order, ws, (cudaStream_t)stream);
+}
+
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {
   if (!ws || !aligned(ws, 256)) return GPTQ_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

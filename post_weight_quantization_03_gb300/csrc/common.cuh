@@ -135,5 +135,11 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
                                    const uint8_t *dead_mask, int bits, int block, void *ws,
                                    cudaStream_t s);
 size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, int block);
+// OBQ greedy order, d <= 128 (gptq_quantize_obq)
+gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                                const float *U, const uint8_t *dead_mask, int bits,
+                                uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                                int32_t *order, void *ws, cudaStream_t s);
+size_t quantize_obq_ws_bytes(int64_t m, int64_t d);
 
 }  // namespace gptq

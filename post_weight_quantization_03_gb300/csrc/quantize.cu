@@ -10,6 +10,8 @@
 //   trailing : W[:, b1:] -= E U[b0:b1, b1:]   (the deferred lazy-batch product, run as
 //              C -= A B^T with B = U^T rows, i.e. Lt = U^T split into head/tail)
 // then one pass packs the codes and writes W_hat.
+#include <cfloat>
+
 #include "tc.cuh"
 
 namespace gptq {
@@ -381,6 +383,92 @@ eager_column_kernel(float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t d, 
 }
 
 // ---------------------------------------------------------------------------------------
+// OBQ greedy order ("tm_gptq_math", "Greedy quantization with error compensation"; the
+// Schur downdate of "GPTQ › Mathematical Details of the Update"), for d_in <= OBQ_MAX_D:
+// one CTA per row, thread j owns column j; the row's inverse Hessian of the free weights
+// lives in shared memory.  Per step: every free column's cost (w - quant(w))^2 / [H_F^-1]_jj
+// in fp32, an argmin over the CTA (lowest index on ties), then the chosen thread stores its
+// code and scaled error, the free threads compensate their weights and downdate their own
+// column of H_F^-1.  Only uniform barriers; no waits on other CTAs.
+// ---------------------------------------------------------------------------------------
+constexpr int OBQ_MAX_D = 128;
+
+// Hinv = U^T U (U upper): Hinv[i][j] = sum_{k <= min(i, j)} U[k][i] U[k][j].
+__global__ void hinv_kernel(const float *__restrict__ U, int64_t d, float *__restrict__ Hinv) {
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < d * d;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = e / d, j = e % d, kmax = i < j ? i : j;
+    float acc = 0.f;
+    for (int64_t k = 0; k <= kmax; ++k) acc = fmaf(U[k * d + i], U[k * d + j], acc);
+    Hinv[e] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(OBQ_MAX_D)
+obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__restrict__ Hinv,
+           const float *__restrict__ scale, const int32_t *__restrict__ zero, float maxq,
+           uint8_t *__restrict__ codes, int64_t ldc, int32_t *__restrict__ order) {
+  extern __shared__ float Hs[];  // d x (d + 1)
+  __shared__ float s_val[OBQ_MAX_D / 32];
+  __shared__ int s_idx[OBQ_MAX_D / 32];
+  __shared__ float s_e;
+  __shared__ uint8_t s_free[OBQ_MAX_D];
+  const int j = threadIdx.x, lane = j % 32, wid = j / 32;
+  const int64_t row = blockIdx.x;
+  const int L = d + 1;
+  for (int e = j; e < d * d; e += OBQ_MAX_D) Hs[(e / d) * L + e % d] = Hinv[e];
+  bool free = j < d;
+  float w = free ? Wf[row * ldwf + j] : 0.f;
+  if (free) s_free[j] = 1;
+  const float sc_row = scale[row], z = (float)zero[row];
+  __syncthreads();
+#pragma unroll 1
+  for (int step = 0; step < d; ++step) {
+    float cd = 0.f, qv = 0.f, key = INFINITY;   // non-free columns never win
+    if (free) {
+      cd = fminf(fmaxf(rintf(__fdiv_rn(w, sc_row)) + z, 0.f), maxq);
+      qv = sc_row * (cd - z);
+      const float er = w - qv;
+      const float cost = __fdiv_rn(er * er, Hs[j * L + j]);
+      key = (cost >= 0.f && cost <= FLT_MAX) ? cost : FLT_MAX;  // NaN/inf: last among free
+    }
+    int idx = free ? j : OBQ_MAX_D;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, key, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      if (ov < key || (ov == key && oi < idx)) { key = ov; idx = oi; }
+    }
+    if (lane == 0) { s_val[wid] = key; s_idx[wid] = idx; }
+    __syncthreads();
+    float best = s_val[0];
+    int q = s_idx[0];
+#pragma unroll
+    for (int k = 1; k < OBQ_MAX_D / 32; ++k)
+      if (s_val[k] < best || (s_val[k] == best && s_idx[k] < q)) { best = s_val[k]; q = s_idx[k]; }
+    // a free column always exists while step < d, so q < d; the clamp only keeps every
+    // index inside the tile should that ever fail
+    q = q < d ? q : d - 1;
+    if (j == q) {
+      codes[row * ldc + q] = (uint8_t)cd;
+      if (order) order[row * d + step] = q;
+      s_e = __fdiv_rn(w - qv, Hs[q * L + q]);
+      s_free[q] = 0;
+      w = qv;
+      free = false;
+    }
+    __syncthreads();
+    if (free) {
+      w = fmaf(-s_e, Hs[j * L + q], w);
+      const float f = __fdiv_rn(Hs[q * L + j], Hs[q * L + q]);
+      for (int i = 0; i < d; ++i)
+        if (s_free[i]) Hs[i * L + j] = fmaf(-Hs[i * L + q], f, Hs[i * L + j]);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Pack codes into the row bitstream; write W_hat = scale * (code - zero).
 // One thread per output word.
 // ---------------------------------------------------------------------------------------
@@ -575,6 +663,45 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
       GPTQ_CUDA_CHECK(cudaMemcpyAsync(L[i].zero, zero + off, L[i].m * 4,
                                       cudaMemcpyDeviceToDevice, s));
     }
+  }
+  return GPTQ_OK;
+}
+
+size_t quantize_obq_ws_bytes(int64_t m, int64_t d) {
+  return 256 + round_up((size_t)m * round_up((size_t)d, 4) * 4, 256) +
+         round_up((size_t)m * round_up((size_t)d, 16), 256) + round_up((size_t)d * d * 4, 256);
+}
+
+gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
+                                const float *U, const uint8_t *dead_mask, int bits,
+                                uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
+                                int32_t *order, void *ws, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(obq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(OBQ_MAX_D * (OBQ_MAX_D + 1) * sizeof(float))));
+    attr_done = true;
+  }
+  char *p = (char *)ws;
+  DevStatus *st = (DevStatus *)p; p += 256;
+  const int64_t ldwf = (int64_t)round_up((size_t)d, 4), ldc = (int64_t)round_up((size_t)d, 16);
+  float *Wf = (float *)p; p += round_up((size_t)m * ldwf * 4, 256);
+  uint8_t *codes = (uint8_t *)p; p += round_up((size_t)m * ldc, 256);
+  float *Hinv = (float *)p;
+  const float maxq = (float)((1 << bits) - 1);
+  GPTQ_CUDA_CHECK(cudaMemsetAsync(st, 0, sizeof(DevStatus), s));
+  GPTQ_TRY(launch_grid(W, wdtype, m, d, ldw, dead_mask, maxq, scale, zero, Wf, ldwf, st, s));
+  hinv_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(U, d, Hinv);
+  GPTQ_LAUNCH_CHECK();
+  obq_kernel<<<(unsigned)m, OBQ_MAX_D, (size_t)d * (d + 1) * sizeof(float), s>>>(
+      Wf, ldwf, (int)d, Hinv, scale, zero, maxq, codes, ldc, order);
+  GPTQ_LAUNCH_CHECK();
+  const int64_t words = ceil_div(d, 32) * bits;
+  pack_kernel<<<2048, 256, 0, s>>>(codes, ldc, m, d, bits, words, qpacked);
+  GPTQ_LAUNCH_CHECK();
+  if (W_hat) {
+    dequant_kernel<<<2048, 256, 0, s>>>(codes, ldc, m, d, scale, zero, W_hat);
+    GPTQ_LAUNCH_CHECK();
   }
   return GPTQ_OK;
 }

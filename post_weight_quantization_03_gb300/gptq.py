@@ -49,6 +49,11 @@ _SIGS = {
                                     _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_void_p,
                                     _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                     _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "gptq_quantize_obq_workspace_bytes": (_c.c_size_t, [_c.c_int64, _c.c_int64]),
+    "gptq_quantize_obq": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+                                     _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p,
+                                     _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                     _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "gptq_quantize_shared_workspace_bytes": (_c.c_size_t, [_c.c_int, _c.c_void_p, _c.c_int64,
                                                            _c.c_int, _c.c_int]),
     "gptq_quantize_layers_shared": (_c.c_int, [_c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
@@ -62,6 +67,7 @@ _SIGS = {
                                                _c.c_void_p, _c.c_void_p]),
 }
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GPTQ_NOALLOC_SCRATCH_BYTES in include/gptq.h
+OBQ_MAX_D_IN = 128                # GPTQ_OBQ_MAX_D_IN in include/gptq.h
 MAX_SHARED_LAYERS = 64            # GPTQ_MAX_SHARED_LAYERS in include/gptq.h
 
 _lib = None
@@ -164,6 +170,16 @@ def gptq_recon_error(X, xdtype, n_tok, d_in, ldx, W, wdtype, d_out, ldw, qpacked
                      zero, err, ws, ws_bytes, stream):
     return load().gptq_recon_error(X, xdtype, n_tok, d_in, ldx, W, wdtype, d_out, ldw, qpacked,
                                    bits, scale, zero, err, ws, ws_bytes, stream)
+
+
+def gptq_quantize_obq_workspace_bytes(d_out, d_in):
+    return load().gptq_quantize_obq_workspace_bytes(d_out, d_in)
+
+
+def gptq_quantize_obq(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, qpacked, scale, zero,
+                      W_hat, order, ws, ws_bytes, stream):
+    return load().gptq_quantize_obq(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, qpacked,
+                                    scale, zero, W_hat, order, ws, ws_bytes, stream)
 
 
 def gptq_quantize_shared_workspace_bytes(n_layers, d_out, d_in, bits, block):
@@ -426,3 +442,23 @@ def recon_error(X, W, qpacked, bits, scale, zero, ws=None, stream=None):
                             _ptr(scale), _ptr(zero), _ptr(err), _ptr(ws), ws.numel(),
                             _stream(stream)), "gptq_recon_error")
     return err
+
+
+def quantize_obq(W, U, bits=4, dead_mask=None, ws=None, stream=None):
+    """OBQ greedy order per row (d_in <= 128).  Returns
+    ``(qpacked, scale, zero, W_hat, order)``."""
+    torch = _torch()
+    m, d = W.shape
+    dev = W.device
+    qpacked = torch.empty(m, packed_words(d, bits), dtype=torch.int32, device=dev)
+    scale = torch.empty(m, dtype=torch.float32, device=dev)
+    zero = torch.empty(m, dtype=torch.int32, device=dev)
+    W_hat = torch.empty(m, d, dtype=torch.float32, device=dev)
+    order = torch.empty(m, d, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(gptq_quantize_obq_workspace_bytes(m, d), dev)
+    _check(gptq_quantize_obq(_ptr(W), _dtype_code(W), m, d, W.stride(0), _ptr(U),
+                             _ptr(dead_mask), bits, _ptr(qpacked), _ptr(scale), _ptr(zero),
+                             _ptr(W_hat), _ptr(order), _ptr(ws), ws.numel(), _stream(stream)),
+           "gptq_quantize_obq")
+    return qpacked, scale, zero, W_hat, order

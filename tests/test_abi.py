@@ -111,6 +111,15 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert gptq.gptq_recon_error_workspace_bytes(0, 4096, 4096, 262144) >= \
         4096 * 4096 * 2 + 1024 * 4096 * 4
     assert gptq.gptq_recon_error_workspace_bytes(9, 4, 8, 10) == 0
+    # OBQ: too wide, bits, workspace
+    ob = gptq.gptq_quantize_obq
+    assert ob(fake, 1, 4, 129, 129, fake, None, 4, fake, fake, fake, None, None, fake, 1 << 30,
+              None) == 6
+    assert ob(fake, 1, 4, 64, 64, fake, None, 6, fake, fake, fake, None, None, fake, 1 << 30,
+              None) == INV
+    assert ob(fake, 1, 4, 64, 64, fake, None, 4, fake, fake, fake, None, None, fake, 16,
+              None) == WS
+    assert gptq.gptq_quantize_obq_workspace_bytes(0, 64) == 0
     # prepare: negative damp, missing or short workspace
     assert gptq.gptq_prepare(fake, 8, -1.0, fake, None, None, fake, 1 << 20, None) == INV
     assert gptq.gptq_prepare(fake, 8, 0.01, fake, None, None, None, 0, None) == WS

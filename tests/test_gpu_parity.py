@@ -364,3 +364,36 @@ def test_recon_error_zero_tokens():
     U = torch.eye(d, device=DEV)
     qp, sc, zr, _ = gptq.quantize(W, U, 4, 128)
     assert torch.all(gptq.recon_error(X, W, qp, 4, sc, zr) == 0)
+
+
+# ---------------------------------------------------------------------------------------
+# OBQ greedy order: the GPU's order and codes replayed through the oracle
+# ---------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("m,d,bits,wdtype,dead", [
+    (64, 64, 4, "bf16", 2),
+    (100, 128, 3, "f32", 3),
+    (33, 37, 2, "f16", 1),          # ragged width
+    (40, 1, 4, "f32", 0),           # a single column
+])
+def test_obq_parity(m, d, bits, wdtype, dead):
+    W, U32, dmask = _quant_case(m, d, bits, 128, wdtype, seed=m + 3 * d, dead=dead, outl=1)
+    Hd = np.linalg.inv(U32.astype(np.float64).T @ U32.astype(np.float64))
+    dm = torch.from_numpy(dmask.astype(np.uint8)).to(DEV)
+    Wg = W.to(DEV) if (d * W.element_size()) % 16 == 0 else _padded(W)
+    qp, sc, zr, Wh, order = gptq.quantize_obq(Wg, torch.from_numpy(U32).to(DEV), bits, dm)
+    torch.cuda.synchronize()
+    Wn = W.float().numpy()
+    s_ref, z_ref = O.row_grid(Wn, bits)
+    assert np.array_equal(sc.cpu().numpy(), s_ref)
+    assert np.array_equal(zr.cpu().numpy(), z_ref)
+    codes = _codes(qp, bits, d)
+    order = order.cpu().numpy().astype(np.int64)
+    for i in range(m):
+        assert sorted(order[i]) == list(range(d))
+    _, _, _, info = O.obq_greedy(Wn, Hd, s_ref, z_ref, bits, dead=dmask, forced=(order, codes))
+    assert info["bad_order"] == 0 and info["bad_codes"] == 0
+    assert info["max_slack"] <= 1e-4
+    assert info["tie_flips"] <= max(1, m * d // 5000)
+    Wh_ref = (s_ref[:, None] * (codes - z_ref[:, None]).astype(np.float32)).astype(np.float32)
+    assert np.array_equal(Wh.cpu().numpy(), Wh_ref)
