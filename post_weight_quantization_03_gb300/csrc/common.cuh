@@ -109,6 +109,8 @@ struct GemmArgs {
   float alpha;
   int lower_only;
   int trans_c;
+  int max_ctas;   // tensor-core path: at most this many persistent CTAs (0 = one per SM;
+                  // -1 = one CTA per tile, so SMs free up tile by tile for other streams)
 };
 gptq_status launch_gemm_nt(const GemmArgs &g, DevStatus *st, cudaStream_t s);
 // tc_gemm.cu: the tcgen05 3xTF32 kernel; UNSUPPORTED when the operands do not meet its

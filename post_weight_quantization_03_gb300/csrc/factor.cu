@@ -342,30 +342,47 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
 }
 
 // ---------------------------------------------------------------------------------------
-// Row-panel product: Out[r][j] = sum_{t<n} In[r][t] * Bm[j][t] for rows r in [r0, r1),
-// j < n.  Each CTA owns whole rows, so Out may alias In.  Optionally also writes the
-// TF32 head/tail split of Out into (hi, lo) panels (row r -> hi[r * NB + j]).
+// Row-panel product: P[r][j] = sum_{t<n} In[r][t] * Bm[j][t] for rows r in [r0, r1),
+// j < nj, with In and Bm optionally given as TF32 head + tail pairs (In_lo, Bm_lo summed on
+// load: the exact fp32 value).  Out[r][j] = P (sub = 0) or Out[r][j] -= P by atomic adds
+// (sub = 1: another stream may be adding into the same block).  Optionally also writes the
+// TF32 head/tail split of P into (hi, lo) panels (row r -> hi[r * NB + j]).  A CTA takes
+// RM_ROWS rows and NCQ of the four 32-column quarters of the output (blockIdx.y selects
+// which); with NCQ = 4 a CTA owns whole rows, stages its input rows before writing, and
+// Out may alias In.
 // ---------------------------------------------------------------------------------------
 constexpr int RM_ROWS = 32, RM_THREADS = 256;
 constexpr int RML = NB + 4;  // smem leading dimension: float4 rows of 8 consecutive
                              // threads fall in distinct bank groups
 
-// Thread (rg, cg) computes rows 4rg..4rg+3 x columns cg + 32q (q < 4) of the CTA's
-// 32 x 128 output block: per 4-wide K step, 8 float4 shared loads feed 64 FMAs.
+// Thread (rg, cg) computes rows 4rg..4rg+3 x columns 32(q0 + q) + cg (q < NCQ): per 4-wide
+// K step, 4 broadcast + NCQ float4 shared loads feed 8 NCQ paired FMAs.
+template <int NCQ>
 __global__ void __launch_bounds__(RM_THREADS)
-rowmul_kernel(const float *In, int64_t ldi, float *Out, int64_t ldo, int64_t r0, int64_t r1,
-              const float *Bm, int n, float *hi, float *lo, const DevStatus *st) {
+rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int64_t ldo,
+              int64_t r0, int64_t r1, const float *Bm, const float *Bm_lo, int64_t ldb, int n,
+              int nj, int sub, float *hi, float *lo, const DevStatus *st) {
   extern __shared__ __align__(16) float sm[];
-  float *Bs = sm;                 // NB x RML: Bm rows (output column index, K)
-  float *Is = sm + NB * RML;      // RM_ROWS x RML: the CTA's input rows
+  float *Bs = sm;                    // 32 NCQ x RML: the CTA's Bm rows (output columns, K)
+  float *Is = sm + 32 * NCQ * RML;   // RM_ROWS x RML: the CTA's input rows
   if (st->status != 0) return;
   const int tid = threadIdx.x;
   const int64_t rb = r0 + (int64_t)blockIdx.x * RM_ROWS;
+  const int q0 = blockIdx.y * NCQ;
 #pragma unroll 4
-  for (int it = 0; it < NB * NB / 4 / RM_THREADS; ++it) {
-    const int e = it * RM_THREADS + tid;  // float4 index
-    const float4 v = reinterpret_cast<const float4 *>(Bm)[e];
-    *reinterpret_cast<float4 *>(Bs + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = v;
+  for (int it = 0; it < 32 * NCQ * NB / 4 / RM_THREADS; ++it) {
+    const int e = it * RM_THREADS + tid;  // float4 index within the CTA's Bm rows
+    const int j = e / (NB / 4), t4 = 4 * (e % (NB / 4));
+    const int64_t bo = (int64_t)(32 * q0 + j) * ldb + t4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (32 * q0 + j < nj) {
+      v = *reinterpret_cast<const float4 *>(Bm + bo);
+      if (Bm_lo) {
+        const float4 u = *reinterpret_cast<const float4 *>(Bm_lo + bo);
+        v = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+      }
+    }
+    *reinterpret_cast<float4 *>(Bs + j * RML + t4) = v;
   }
   const bool vec = (ldi % 4) == 0 && (((uintptr_t)In) % 16) == 0;
 #pragma unroll 4
@@ -377,37 +394,38 @@ rowmul_kernel(const float *In, int64_t ldi, float *Out, int64_t ldo, int64_t r0,
     if (gr < r1) {
       if (vec && t4 + 4 <= n) {
         v = *reinterpret_cast<const float4 *>(In + gr * ldi + t4);
+        if (In_lo) {
+          const float4 u = *reinterpret_cast<const float4 *>(In_lo + gr * ldi + t4);
+          v = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+        }
       } else {
-        v.x = (t4 + 0 < n) ? In[gr * ldi + t4 + 0] : 0.f;
-        v.y = (t4 + 1 < n) ? In[gr * ldi + t4 + 1] : 0.f;
-        v.z = (t4 + 2 < n) ? In[gr * ldi + t4 + 2] : 0.f;
-        v.w = (t4 + 3 < n) ? In[gr * ldi + t4 + 3] : 0.f;
+#define RM_IN(q) ((t4 + q < n) ? In[gr * ldi + t4 + q] + (In_lo ? In_lo[gr * ldi + t4 + q] : 0.f) : 0.f)
+        v = make_float4(RM_IN(0), RM_IN(1), RM_IN(2), RM_IN(3));
+#undef RM_IN
       }
     }
     *reinterpret_cast<float4 *>(Is + r * RML + t4) = v;
   }
   __syncthreads();
   const int rg = tid / 32, cg = tid % 32;
-  float acc[4][4];
+  float2 acc[4][NCQ];   // even and odd k summed apart
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[i][q] = 0.f;
+    for (int q = 0; q < NCQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
 #pragma unroll 2
   for (int t = 0; t < NB; t += 4) {
-    float4 a[4], b[4];
+    float4 a[4], b[NCQ];
 #pragma unroll
     for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Is + (4 * rg + i) * RML + t);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) b[q] = *reinterpret_cast<const float4 *>(Bs + (cg + 32 * q) * RML + t);
+    for (int q = 0; q < NCQ; ++q) b[q] = *reinterpret_cast<const float4 *>(Bs + (32 * q + cg) * RML + t);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[i][q] = fmaf(a[i].x, b[q].x, acc[i][q]);
-        acc[i][q] = fmaf(a[i].y, b[q].y, acc[i][q]);
-        acc[i][q] = fmaf(a[i].z, b[q].z, acc[i][q]);
-        acc[i][q] = fmaf(a[i].w, b[q].w, acc[i][q]);
+      for (int q = 0; q < NCQ; ++q) {
+        acc[i][q] = __ffma2_rn(make_float2(a[i].x, a[i].y), make_float2(b[q].x, b[q].y), acc[i][q]);
+        acc[i][q] = __ffma2_rn(make_float2(a[i].z, a[i].w), make_float2(b[q].z, b[q].w), acc[i][q]);
       }
   }
 #pragma unroll
@@ -415,10 +433,13 @@ rowmul_kernel(const float *In, int64_t ldi, float *Out, int64_t ldo, int64_t r0,
     const int64_t gr = rb + 4 * rg + i;
     if (gr >= r1) continue;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = cg + 32 * q;
-      const float v = (j < n) ? acc[i][q] : 0.f;
-      if (Out && j < n) Out[gr * ldo + j] = v;
+    for (int q = 0; q < NCQ; ++q) {
+      const int j = 32 * (q0 + q) + cg;
+      const float v = (j < nj) ? acc[i][q].x + acc[i][q].y : 0.f;
+      if (Out && j < nj) {
+        if (sub) atomicAdd(Out + gr * ldo + j, -v);
+        else Out[gr * ldo + j] = v;
+      }
       if (hi) {
         const float h = tf32_head(v);
         hi[gr * NB + j] = h;
@@ -469,12 +490,15 @@ PrepWs carve_prepare(void *ws, int64_t d) {
   return w;
 }
 
-// A second stream and two event pairs per device, created once and kept for the process:
-// the panel loop runs its critical chain on the caller's stream and the rest beside it.
+// Two streams and their events per device, created once and kept for the process: the
+// panel loop runs its critical chain on `crit` (the device's highest stream priority, so its
+// blocks are dispatched first whenever an SM has room) and the rest beside it on `s`.
 struct SideStream {
   std::mutex enqueue;  // one panel loop at a time enqueues on these events
-  cudaStream_t s = nullptr;
-  cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr;
+  cudaStream_t s = nullptr, crit = nullptr;
+  cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr,
+              e1 = nullptr;
+  int num_sms = 0;
 };
 constexpr int kMaxDevices = 128;
 std::mutex g_side_mu;
@@ -487,12 +511,17 @@ gptq_status side_stream(SideStream **out) {
   std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream &ss = g_side[dev];
   if (!ss.s) {
-    GPTQ_CUDA_CHECK(cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking));
+    int lo = 0, hi = 0;
+    GPTQ_CUDA_CHECK(cudaDeviceGetStreamPriorityRange(&lo, &hi));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit, cudaStreamNonBlocking, hi));
+    GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&ss.num_sms, cudaDevAttrMultiProcessorCount, dev));
     for (int b = 0; b < 2; ++b) {
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ea[b], cudaEventDisableTiming));
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.eb[b], cudaEventDisableTiming));
     }
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e0, cudaEventDisableTiming));
+    GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e1, cudaEventDisableTiming));
   }
   *out = &ss;
   return GPTQ_OK;
@@ -505,26 +534,29 @@ size_t prepare_ws_bytes(int64_t d) {
          2 * round_up((size_t)NB * NB * 4, 256);
 }
 
-// Panel loop.  On the caller's stream `s` (the critical chain):
+// Panel loop.  On the critical stream (highest priority; the caller's stream when the
+// side stream cannot be used):
 //   potrf(k) -> trsm(k) for all rows below -> the next panel column's update
 //   (rows >= k1, columns [k1, k1 + NB)) -> potrf(k + 1) ...
-// On the side stream `b`, once panel k's factor and L panel exist:
+// On the side stream, once panel k's factor and L panel exist:
 //   inverse step a(k) -> the rest of the trailing update (the lower square from
 //   k1 + NB) -> inverse step b(k).
 // potrf(k) waits for the side stream's panel k - 2, which last wrote its diagonal block
 // and read the panel buffers it is about to overwrite.  Updates of one column block by
-// both streams are L2 reduce-adds (tensor-core epilogue); where C is not 16-byte aligned
-// the epilogue is a plain read-modify-write and everything runs on `s`.
+// both streams are atomic adds (L2 reduce-adds in the tensor-core epilogue, red.add in the
+// next-column update); where C is not 16-byte aligned everything runs on the caller's
+// stream.  The caller's stream waits for both at the end.
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                            void *ws, cudaStream_t s) {
   static bool attr_done = false;
-  const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);
+  const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);       // whole rows
+  const size_t rmq_smem = (32 + RM_ROWS) * RML * sizeof(float);       // one column quarter
   const size_t potrf_smem = (2 * NB * PL + PW * PL + PW) * sizeof(float);
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)potrf_smem));
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel,
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel<4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)rm_smem));
     attr_done = true;
@@ -536,6 +568,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   std::unique_lock<std::mutex> enqueue_lock;
   if (overlap) enqueue_lock = std::unique_lock<std::mutex>(ss->enqueue);
   cudaStream_t b = overlap ? ss->s : s;
+  const int side_ctas = 0;  // persistent: one CTA per SM
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
   dead_damp_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead_mask, w.st);
   GPTQ_LAUNCH_CHECK();
@@ -543,9 +576,11 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   GPTQ_LAUNCH_CHECK();
   identity_kernel<<<1024, 256, 0, s>>>(w.Yt, d);
   GPTQ_LAUNCH_CHECK();
+  cudaStream_t c = overlap ? ss->crit : s;  // the critical chain
   if (overlap) {
     GPTQ_CUDA_CHECK(cudaEventRecord(ss->e0, s));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->e0, 0));
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->e0, 0));
   }
   float *A = H;  // reversed, damped Hessian; lower triangle is the Cholesky workspace
   int k = 0;
@@ -553,33 +588,35 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
     const int par = k & 1;
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
-    if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[par], 0));
-    potrf_kernel<<<1, PF_THREADS, potrf_smem, s>>>(A, d, k0, n, w.Linv[par], w.st);
+    if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->eb[par], 0));
+    potrf_kernel<<<1, PF_THREADS, potrf_smem, c>>>(A, d, k0, n, w.Linv[par], w.st);
     GPTQ_LAUNCH_CHECK();
     if (k1 < d) {
       // trsm: rows [k1, d) of panel k -> L panel (hi/lo)
-      const unsigned g = (unsigned)ceil_div(d - k1, RM_ROWS);
-      rowmul_kernel<<<g, RM_THREADS, rm_smem, s>>>(A + k0, d, nullptr, 0, k1, d, w.Linv[par], n,
-                                                  w.Lhi[par], w.Llo[par], w.st);
+      dim3 g((unsigned)ceil_div(d - k1, RM_ROWS), 4);
+      rowmul_kernel<1><<<g, RM_THREADS, rmq_smem, c>>>(A + k0, nullptr, d, nullptr, 0, k1, d,
+                                                      w.Linv[par], nullptr, NB, n, n, 0,
+                                                      w.Lhi[par], w.Llo[par], w.st);
       GPTQ_LAUNCH_CHECK();
-      // next panel column: A[k1:, k1:k1+NB] -= L[k1:] L[k1:k1+NB]^T
-      GemmArgs g1{};
-      g1.a_hi = w.Lhi[par] + k1 * NB; g1.a_lo = w.Llo[par] + k1 * NB; g1.lda = NB;
-      g1.b_hi = w.Lhi[par] + k1 * NB; g1.b_lo = w.Llo[par] + k1 * NB; g1.ldb = NB;
-      g1.c = A + k1 * d + k1; g1.ldc = d;
-      g1.M = d - k1; g1.N = std::min<int64_t>(NB, d - k1); g1.K = n;
-      g1.alpha = -1.0f; g1.lower_only = 0; g1.trans_c = 0;
-      GPTQ_TRY(launch_gemm_nt(g1, w.st, s));
+      // next panel column: A[k1:, k1:k1+NB] -= L[k1:] L[k1:k1+NB]^T (fp32 from the head +
+      // tail panels; atomic adds: the side stream's previous trailing update adds here too)
+      const int nn = (int)std::min<int64_t>(NB, d - k1);
+      dim3 g2((unsigned)ceil_div(d - k1, RM_ROWS), (unsigned)ceil_div(nn, 32));
+      rowmul_kernel<1><<<g2, RM_THREADS, rmq_smem, c>>>(
+          w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, 0, d - k1,
+          w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
+      GPTQ_LAUNCH_CHECK();
     }
     if (overlap) {
-      GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], s));
+      GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
     }
     // inverse step a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
     {
       const unsigned g = (unsigned)ceil_div(k1, RM_ROWS);
-      rowmul_kernel<<<g, RM_THREADS, rm_smem, b>>>(w.Yt + k0, d, w.Yt + k0, d, 0, k1,
-                                                  w.Linv[par], n, w.Yhi, w.Ylo, w.st);
+      rowmul_kernel<4><<<g, RM_THREADS, rm_smem, b>>>(w.Yt + k0, nullptr, d, w.Yt + k0, d, 0,
+                                                      k1, w.Linv[par], nullptr, NB, n, n, 0,
+                                                      w.Yhi, w.Ylo, w.st);
       GPTQ_LAUNCH_CHECK();
     }
     if (k1 < d) {
@@ -591,7 +628,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
         g2.b_hi = w.Lhi[par] + r0 * NB; g2.b_lo = w.Llo[par] + r0 * NB; g2.ldb = NB;
         g2.c = A + r0 * d + r0; g2.ldc = d;
         g2.M = d - r0; g2.N = d - r0; g2.K = n;
-        g2.alpha = -1.0f; g2.lower_only = 1; g2.trans_c = 0;
+        g2.alpha = -1.0f; g2.lower_only = 1; g2.trans_c = 0; g2.max_ctas = side_ctas;
         GPTQ_TRY(launch_gemm_nt(g2, w.st, b));
       }
       // inverse step b: Bt[c][k1:] -= Yp[c] Lp[k1:]^T for c < k1
@@ -600,12 +637,14 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
       h.b_hi = w.Lhi[par] + k1 * NB; h.b_lo = w.Llo[par] + k1 * NB; h.ldb = NB;
       h.c = w.Yt + k1; h.ldc = d;
       h.M = k1; h.N = d - k1; h.K = n;
-      h.alpha = -1.0f; h.lower_only = 0; h.trans_c = 0;
+      h.alpha = -1.0f; h.lower_only = 0; h.trans_c = 0; h.max_ctas = side_ctas;
       GPTQ_TRY(launch_gemm_nt(h, w.st, b));
     }
     if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->eb[par], b));
   }
   if (overlap) {
+    GPTQ_CUDA_CHECK(cudaEventRecord(ss->e1, c));
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e1, 0));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[0], 0));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[1], 0));
   }

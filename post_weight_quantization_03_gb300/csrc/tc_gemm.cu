@@ -309,7 +309,9 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   p.n_n = (int)ceil_div(g.N, BN);
   p.lower_only = g.lower_only && g.M == g.N;
   p.n_tiles = p.lower_only ? p.n_n * (p.n_n + 1) / 2 : p.n_m * p.n_n;
-  const int grid = p.n_tiles < num_sms ? p.n_tiles : num_sms;
+  const int cap = g.max_ctas < 0 ? p.n_tiles
+                  : (g.max_ctas > 0 && g.max_ctas < num_sms) ? g.max_ctas : num_sms;
+  const int grid = p.n_tiles < cap ? p.n_tiles : cap;
   tc_gemm_3xtf32_kernel<<<grid, kThreads, kSmemBytes, s>>>(mah, mal, mbh, mbl, mc, p, st);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
