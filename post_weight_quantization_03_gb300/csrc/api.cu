@@ -19,6 +19,28 @@ static size_t elem_size(int dt) {
   }
 }
 
+
+gptq_status quantize_layer_checked(const void *W, int wdtype, int64_t d_out,
+                                         int64_t d_in, int64_t ldw, const float *U,
+                                         const uint8_t *dead_mask, int bits, int block,
+                                         uint32_t *qpacked, float *scale, int32_t *zero,
+                                         float *W_hat, void *ws, size_t ws_bytes,
+                                         gptq_stream_t stream, bool allow_overlap) {
+  const size_t es = elem_size(wdtype);
+  if (es == 0 || !W || !U || !qpacked || !scale || !zero) return GPTQ_ERR_INVALID_ARG;
+  if (d_out < 1 || d_in < 1 || ldw < d_in) return GPTQ_ERR_INVALID_ARG;
+  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
+  if (block < 1 || block > 128) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, es) || !aligned(U, 16) || !aligned(qpacked, 4) || !aligned(scale, 4) ||
+      !aligned(zero, 4) || (W_hat && !aligned(W_hat, 4)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_in > (int64_t)1 << 17 || d_out > (int64_t)1 << 24) return GPTQ_ERR_UNSUPPORTED;
+  if (!ws || !aligned(ws, 256) || ws_bytes < quantize_ws_bytes(d_out, d_in, bits, block))
+    return GPTQ_ERR_WORKSPACE;
+  return launch_quantize(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
+                         scale, zero, W_hat, ws, (cudaStream_t)stream, allow_overlap);
+}
+
 }  // namespace gptq
 
 using namespace gptq;
@@ -103,25 +125,6 @@ size_t gptq_quantize_workspace_bytes(int64_t d_out, int64_t d_in, int bits, int 
   return quantize_ws_bytes(d_out, d_in, bits, block);
 }
 
-gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_t d_in,
-                                int64_t ldw, const float *U, const uint8_t *dead_mask,
-                                int bits, int block, uint32_t *qpacked, float *scale,
-                                int32_t *zero, float *W_hat, void *ws, size_t ws_bytes,
-                                gptq_stream_t stream) {
-  const size_t es = elem_size(wdtype);
-  if (es == 0 || !W || !U || !qpacked || !scale || !zero) return GPTQ_ERR_INVALID_ARG;
-  if (d_out < 1 || d_in < 1 || ldw < d_in) return GPTQ_ERR_INVALID_ARG;
-  if (!(bits == 2 || bits == 3 || bits == 4 || bits == 8)) return GPTQ_ERR_INVALID_ARG;
-  if (block < 1 || block > 128) return GPTQ_ERR_INVALID_ARG;
-  if (!aligned(W, es) || !aligned(U, 16) || !aligned(qpacked, 4) || !aligned(scale, 4) ||
-      !aligned(zero, 4) || (W_hat && !aligned(W_hat, 4)))
-    return GPTQ_ERR_INVALID_ARG;
-  if (d_in > (int64_t)1 << 17 || d_out > (int64_t)1 << 24) return GPTQ_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, 256) || ws_bytes < quantize_ws_bytes(d_out, d_in, bits, block))
-    return GPTQ_ERR_WORKSPACE;
-  return launch_quantize(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
-                         scale, zero, W_hat, ws, (cudaStream_t)stream);
-}
 
 size_t gptq_quantize_shared_workspace_bytes(int n_layers, const int64_t *d_out, int64_t d_in,
                                             int bits, int block) {
@@ -161,7 +164,7 @@ gptq_status gptq_quantize_layers_shared(int n_layers, const void *const *W, cons
       ws_bytes < quantize_layers_ws_bytes(d_out, n_layers, d_in, bits, block))
     return GPTQ_ERR_WORKSPACE;
   return launch_quantize_layers(L, n_layers, d_in, U, dead_mask, bits, block, ws,
-                                (cudaStream_t)stream);
+                                (cudaStream_t)stream, true);
 }
 
 size_t gptq_recon_error_workspace_bytes(int xdtype, int64_t d_out, int64_t d_in,
@@ -214,6 +217,15 @@ gptq_status gptq_quantize_obq(const void *W, int wdtype, int64_t d_out, int64_t 
     return GPTQ_ERR_WORKSPACE;
   return launch_quantize_obq(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, qpacked, scale,
                              zero, W_hat, order, ws, (cudaStream_t)stream);
+}
+
+gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                                int64_t ldw, const float *U, const uint8_t *dead_mask,
+                                int bits, int block, uint32_t *qpacked, float *scale,
+                                int32_t *zero, float *W_hat, void *ws, size_t ws_bytes,
+                                gptq_stream_t stream) {
+  return gptq::quantize_layer_checked(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
+                                      qpacked, scale, zero, W_hat, ws, ws_bytes, stream, true);
 }
 
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {

@@ -123,11 +123,19 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
 size_t prepare_ws_bytes(int64_t d);
 
 // quantize.cu
+// allow_overlap: the blocked sweep may run the far part of each trailing update on a
+// second stream (same results bit for bit); false keeps every launch on `s`.
 gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
                             const float *U, const uint8_t *dead_mask, int bits, int block,
                             uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
-                            void *ws, cudaStream_t s);
+                            void *ws, cudaStream_t s, bool allow_overlap);
 size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block);
+// api.cu: gptq_quantize_layer's validation + launch; allow_overlap as launch_quantize.
+gptq_status quantize_layer_checked(const void *W, int wdtype, int64_t d_out, int64_t d_in,
+                                   int64_t ldw, const float *U, const uint8_t *dead_mask,
+                                   int bits, int block, uint32_t *qpacked, float *scale,
+                                   int32_t *zero, float *W_hat, void *ws, size_t ws_bytes,
+                                   gptq_stream_t stream, bool allow_overlap);
 // Several layers sharing U, swept as one stack of rows (gptq_quantize_layers_shared).
 struct QLayer {
   const void *W; int wdtype; int64_t m; int64_t ldw;
@@ -135,7 +143,7 @@ struct QLayer {
 };
 gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
                                    const uint8_t *dead_mask, int bits, int block, void *ws,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool allow_overlap);
 size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, int block);
 // OBQ greedy order, d <= 128 (gptq_quantize_obq)
 gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,

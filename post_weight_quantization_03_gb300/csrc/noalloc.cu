@@ -63,7 +63,8 @@ extern "C" gptq_status gptq_quantize_layer_noalloc(
   void *scratch = nullptr;
   const gptq_status st = gptq::scratch_address(&scratch);
   if (st != GPTQ_OK) return st;
-  return gptq_quantize_layer(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block, qpacked,
-                             scale, zero, W_hat, scratch, (size_t)GPTQ_NOALLOC_SCRATCH_BYTES,
-                             stream);
+  // one stream only: the two-stream schedule would create streams and events on first use
+  return gptq::quantize_layer_checked(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
+                                      qpacked, scale, zero, W_hat, scratch,
+                                      (size_t)GPTQ_NOALLOC_SCRATCH_BYTES, stream, false);
 }

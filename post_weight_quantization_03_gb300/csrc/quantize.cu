@@ -10,7 +10,9 @@
 //   trailing : W[:, b1:] -= E U[b0:b1, b1:]   (the deferred lazy-batch product, run as
 //              C -= A B^T with B = U^T rows, i.e. Lt = U^T split into head/tail)
 // then one pass packs the codes and writes W_hat.
+#include <algorithm>
 #include <cfloat>
+#include <mutex>
 
 #include "tc.cuh"
 
@@ -511,9 +513,10 @@ struct QuantWs {
   float *Lhi, *Llo; int64_t ldl;
   uint8_t *codes; int64_t ldc;
   float *Ud;
+  float *Ehi2, *Elo2;   // second E pair (blocks of odd index when the far update overlaps)
 };
 
-QuantWs carve_quantize(void *ws, int64_t m, int64_t d) {
+QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   QuantWs q;
   char *p = (char *)ws;
   q.st = (DevStatus *)p; p += 256;
@@ -527,6 +530,10 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d) {
   q.ldc = (int64_t)round_up((size_t)d, 16);
   q.codes = (uint8_t *)p; p += round_up((size_t)m * q.ldc, 256);
   q.Ud = (float *)p;
+  const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
+  p += block > 1 ? nblk * UD_FLOATS * 4 : 0;
+  q.Ehi2 = (float *)p; p += round_up((size_t)m * SB * 4, 256);
+  q.Elo2 = (float *)p;
   return q;
 }
 
@@ -539,10 +546,44 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
   return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * SB * 4, 256) +
          2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
-         (block > 1 ? nblk * UD_FLOATS * 4 : 0);   // B = 1 needs no packed diagonal blocks
+         (block > 1 ? nblk * UD_FLOATS * 4 + 2 * round_up((size_t)m * SB * 4, 256)
+                    : 0);   // B = 1 needs neither packed diagonal blocks nor a second E pair
 }
 
 namespace {
+
+// The blocked sweep's two streams per device, created once and kept for the process:
+// `crit` (highest priority) runs the sweeps and each block's update of the next block's
+// columns; `side` (lowest priority) runs the far part of each block's trailing update.
+struct QuantStreams {
+  std::mutex enqueue;  // one call at a time enqueues on these events
+  cudaStream_t crit = nullptr, side = nullptr;
+  cudaEvent_t start = nullptr, crit_done = nullptr, side_done = nullptr;
+  cudaEvent_t e_ready[2] = {nullptr, nullptr};   // E of a block written (by parity)
+  cudaEvent_t far_done[2] = {nullptr, nullptr};  // that block's far update finished
+};
+constexpr int kMaxDevices = 128;
+std::mutex g_qs_mu;
+QuantStreams g_qs[kMaxDevices];
+
+gptq_status quant_streams(QuantStreams **out) {
+  int dev = -1;
+  GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return GPTQ_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_qs_mu);
+  QuantStreams &q = g_qs[dev];
+  if (!q.crit) {
+    int lo = 0, hi = 0;
+    GPTQ_CUDA_CHECK(cudaDeviceGetStreamPriorityRange(&lo, &hi));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.crit, cudaStreamNonBlocking, hi));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.side, cudaStreamNonBlocking, lo));
+    cudaEvent_t *evs[] = {&q.start, &q.crit_done, &q.side_done, &q.e_ready[0], &q.e_ready[1],
+                          &q.far_done[0], &q.far_done[1]};
+    for (cudaEvent_t *e : evs) GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+  }
+  *out = &q;
+  return GPTQ_OK;
+}
 
 gptq_status launch_grid(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
                         const uint8_t *dead_mask, float maxq, float *scale, int32_t *zero,
@@ -585,7 +626,7 @@ size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, in
 // outputs.  With one layer the per-row scale and zero are written in place.
 gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
                                    const uint8_t *dead_mask, int bits, int block, void *ws,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, bool allow_overlap) {
   static bool attr_done = false;
   const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
   if (!attr_done) {
@@ -596,7 +637,7 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
   }
   int64_t m = 0;
   for (int i = 0; i < n; ++i) m += L[i].m;
-  QuantWs q = carve_quantize(ws, m, d);
+  QuantWs q = carve_quantize(ws, m, d, block);
   float *scale = L[0].scale;
   int32_t *zero = L[0].zero;
   if (n > 1) {
@@ -629,22 +670,73 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
       GPTQ_LAUNCH_CHECK();
     }
     const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
-    for (int64_t b0 = 0; b0 < d; b0 += block) {
-      const int nb = (int)((d - b0) < block ? (d - b0) : block);
-      const int64_t b1 = b0 + nb;
-      sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
-          q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
-          q.Elo, q.codes, q.ldc, q.st);
-      GPTQ_LAUNCH_CHECK();
-      if (b1 < d) {
-        GemmArgs g{};
-        g.a_hi = q.Ehi; g.a_lo = q.Elo; g.lda = SB;
-        g.b_hi = q.Lhi + b1 * q.ldl + b0; g.b_lo = q.Llo + b1 * q.ldl + b0; g.ldb = q.ldl;
-        g.c = q.Wf + b1; g.ldc = q.ldwf;
-        g.M = m; g.N = d - b1; g.K = nb;
-        g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0;
-        GPTQ_TRY(launch_gemm_nt(g, q.st, s));
+    // W[:, c0:c1] -= E U[b0:b1, c0:c1] with E from buffer pair e
+    auto update = [&](int e, int64_t b0, int nb, int64_t c0, int64_t c1, int max_ctas,
+                      cudaStream_t st) -> gptq_status {
+      GemmArgs g{};
+      g.a_hi = e ? q.Ehi2 : q.Ehi; g.a_lo = e ? q.Elo2 : q.Elo; g.lda = SB;
+      g.b_hi = q.Lhi + c0 * q.ldl + b0; g.b_lo = q.Llo + c0 * q.ldl + b0; g.ldb = q.ldl;
+      g.c = q.Wf + c0; g.ldc = q.ldwf;
+      g.M = m; g.N = c1 - c0; g.K = nb;
+      g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
+      return launch_gemm_nt(g, q.st, st);
+    };
+    QuantStreams *qs = nullptr;
+    const bool overlap = allow_overlap && d > 2 * (int64_t)block;
+    if (overlap) GPTQ_TRY(quant_streams(&qs));
+    if (!overlap) {
+      for (int64_t b0 = 0; b0 < d; b0 += block) {
+        const int nb = (int)((d - b0) < block ? (d - b0) : block);
+        const int64_t b1 = b0 + nb;
+        sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
+            q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
+            q.Elo, q.codes, q.ldc, q.st);
+        GPTQ_LAUNCH_CHECK();
+        if (b1 < d) GPTQ_TRY(update(0, b0, nb, b1, d, 0, s));
       }
+    } else {
+      // Block b's trailing update is split at b1 + B: the next block's columns on the
+      // critical stream right after the sweep, the far columns on the side stream beside
+      // the next sweep.  The next-block update of block b + 1 waits for block b's far
+      // update, so every column receives its blocks' contributions in block order, exactly
+      // as in the single-stream order above (the results are bit for bit the same).
+      std::lock_guard<std::mutex> lock(qs->enqueue);
+      cudaStream_t c = qs->crit, sd = qs->side;
+      int nsm = 0, dev = 0;
+      GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+      GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+      // the far update (persistent) leaves one SM per sweep CTA: measured better than
+      // sharing SMs two sweep CTAs each, and than one CTA per tile over all SMs
+      const int far_ctas = std::max(1, nsm - (int)std::min<unsigned>(sweep_grid, nsm / 2));
+      GPTQ_CUDA_CHECK(cudaEventRecord(qs->start, s));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->start, 0));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->start, 0));
+      int k = 0;
+      for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
+        const int e = k & 1;
+        const int nb = (int)((d - b0) < block ? (d - b0) : block);
+        const int64_t b1 = b0 + nb;
+        const int64_t f0 = b1 + block < d ? b1 + block : d;   // far columns [f0, d)
+        sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, c>>>(
+            q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq,
+            e ? q.Ehi2 : q.Ehi, e ? q.Elo2 : q.Elo, q.codes, q.ldc, q.st);
+        GPTQ_LAUNCH_CHECK();
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
+        // far part of this block (E stays untouched until the sweep two blocks on, which
+        // follows the next block's near update, which waits for this far update)
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
+        if (f0 < d) GPTQ_TRY(update(e, b0, nb, f0, d, far_ctas, sd));
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
+        // near part: the next block's columns, after the previous block's far update
+        if (b1 < d) {
+          if (k > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
+          GPTQ_TRY(update(e, b0, nb, b1, f0, 0, c));
+        }
+      }
+      GPTQ_CUDA_CHECK(cudaEventRecord(qs->crit_done, c));
+      GPTQ_CUDA_CHECK(cudaEventRecord(qs->side_done, sd));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, qs->crit_done, 0));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, qs->side_done, 0));
     }
   }
   const int64_t words = ceil_div(d, 32) * bits;
@@ -709,9 +801,9 @@ gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d,
 gptq_status launch_quantize(const void *W, int wdtype, int64_t m, int64_t d, int64_t ldw,
                             const float *U, const uint8_t *dead_mask, int bits, int block,
                             uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
-                            void *ws, cudaStream_t s) {
+                            void *ws, cudaStream_t s, bool allow_overlap) {
   const QLayer one{W, wdtype, m, ldw, qpacked, scale, zero, W_hat};
-  return launch_quantize_layers(&one, 1, d, U, dead_mask, bits, block, ws, s);
+  return launch_quantize_layers(&one, 1, d, U, dead_mask, bits, block, ws, s, allow_overlap);
 }
 
 
