@@ -497,8 +497,20 @@ struct SideStream {
   std::mutex enqueue;  // one panel loop at a time enqueues on these events
   cudaStream_t s = nullptr, crit = nullptr;
   cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr,
-              e1 = nullptr;
+              e1 = nullptr, e_in = nullptr, e_out = nullptr;
   int num_sms = 0;
+  // the most recent panel loops captured as graphs, and what each was captured for
+  struct Graph {
+    cudaGraphExec_t exec = nullptr;
+    const void *key_ptr[4] = {nullptr, nullptr, nullptr, nullptr};
+    int64_t key_d = -1;
+    float key_damp = 0.f;
+    unsigned kernels = 0;       // kernel launches in the graph
+    unsigned long long used = 0;
+  };
+  static constexpr int kGraphs = 8;
+  Graph graphs[kGraphs];
+  unsigned long long tick = 0;
 };
 constexpr int kMaxDevices = 128;
 std::mutex g_side_mu;
@@ -522,6 +534,8 @@ gptq_status side_stream(SideStream **out) {
     }
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e0, cudaEventDisableTiming));
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e1, cudaEventDisableTiming));
+    GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e_in, cudaEventDisableTiming));
+    GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e_out, cudaEventDisableTiming));
   }
   *out = &ss;
   return GPTQ_OK;
@@ -546,27 +560,17 @@ size_t prepare_ws_bytes(int64_t d) {
 // both streams are atomic adds (L2 reduce-adds in the tensor-core epilogue, red.add in the
 // next-column update); where C is not 16-byte aligned everything runs on the caller's
 // stream.  The caller's stream waits for both at the end.
-gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
-                           void *ws, cudaStream_t s) {
-  static bool attr_done = false;
+namespace {
+
+// The panel loop's launches (no set-up, no locking): on `s`, and with `ss` on its two
+// streams as well.
+gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
+                            void *ws, cudaStream_t s, SideStream *ss) {
   const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);       // whole rows
   const size_t rmq_smem = (32 + RM_ROWS) * RML * sizeof(float);       // one column quarter
   const size_t potrf_smem = (2 * NB * PL + PW * PL + PW) * sizeof(float);
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)potrf_smem));
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel<4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)rm_smem));
-    attr_done = true;
-  }
   PrepWs w = carve_prepare(ws, d);
-  const bool overlap = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0;
-  SideStream *ss = nullptr;
-  if (overlap) GPTQ_TRY(side_stream(&ss));
-  std::unique_lock<std::mutex> enqueue_lock;
-  if (overlap) enqueue_lock = std::unique_lock<std::mutex>(ss->enqueue);
+  const bool overlap = ss != nullptr;
   cudaStream_t b = overlap ? ss->s : s;
   const int side_ctas = 0;  // persistent: one CTA per SM
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
@@ -643,14 +647,87 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
     if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->eb[par], b));
   }
   if (overlap) {
+    // join only what this call recorded (one panel records eb[0] only): waiting on an event
+    // recorded elsewhere is not allowed inside a graph capture
     GPTQ_CUDA_CHECK(cudaEventRecord(ss->e1, c));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e1, 0));
-    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[0], 0));
-    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[1], 0));
+    for (int p = 0; p < std::min(k, 2); ++p) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[p], 0));
   }
   dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
   assemble_u_kernel<<<tg, dim3(32, 8), 0, s>>>(w.Yt, U, d);
   GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+}  // namespace
+
+gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
+                           void *ws, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((2 * NB * PL + PW * PL + PW) * sizeof(float))));
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel<4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((NB + RM_ROWS) * RML * sizeof(float))));
+    attr_done = true;
+  }
+  const bool overlap = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0;
+  if (!overlap) return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, nullptr);
+  SideStream *ss = nullptr;
+  GPTQ_TRY(side_stream(&ss));
+  std::lock_guard<std::mutex> lock(ss->enqueue);
+  // Graph replay: the loop is ~200 dependent launches on three streams; replaying it as one
+  // captured graph removes most of the per-launch latency between them.  The graph is
+  // captured and launched on the library's critical stream, joined to the caller's stream
+  // by an event on each side; inside a caller's own capture everything is launched directly.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);
+  }
+  GPTQ_CUDA_CHECK(cudaEventRecord(ss->e_in, s));
+  GPTQ_CUDA_CHECK(cudaStreamWaitEvent(ss->crit, ss->e_in, 0));
+  const cudaStream_t o = ss->crit;   // the graph's origin stream
+  const void *key[4] = {H, U, dead_mask, ws};
+  SideStream::Graph *gr = nullptr, *lru = &ss->graphs[0];
+  for (SideStream::Graph &c : ss->graphs) {
+    if (c.exec && c.key_d == d && c.key_damp == damp && std::equal(key, key + 4, c.key_ptr))
+      gr = &c;
+    if (c.used < lru->used) lru = &c;
+  }
+  if (!gr) {
+    // capture; any failure (e.g. a one-time set-up call not allowed while capturing)
+    // falls back to launching directly
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    const unsigned long long n0 = gptq_kernel_launches();
+    gptq_status st = GPTQ_ERR_CUDA;
+    if (cudaStreamBeginCapture(o, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+      st = enqueue_prepare(H, d, damp, U, dead_mask, ws, o, ss);
+      if (cudaStreamEndCapture(o, &g) != cudaSuccess) st = GPTQ_ERR_CUDA;
+    }
+    if (st != GPTQ_OK || !g || cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      if (g) cudaGraphDestroy(g);
+      return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);  // after the join above
+    }
+    cudaGraphDestroy(g);
+    gr = lru;
+    if (gr->exec) cudaGraphExecDestroy(gr->exec);
+    gr->exec = exec;
+    std::copy(key, key + 4, gr->key_ptr);
+    gr->key_d = d;
+    gr->key_damp = damp;
+    gr->kernels = (unsigned)(gptq_kernel_launches() - n0);  // counted while capturing
+  } else {
+    count_launch(gr->kernels);
+  }
+  gr->used = ++ss->tick;
+  GPTQ_CUDA_CHECK(cudaGraphLaunch(gr->exec, o));
+  GPTQ_CUDA_CHECK(cudaEventRecord(ss->e_out, o));
+  GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e_out, 0));
   return GPTQ_OK;
 }
 
