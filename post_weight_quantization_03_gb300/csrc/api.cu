@@ -7,6 +7,7 @@ namespace gptq {
 
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+unsigned long long launches_so_far() { return g_launches.load(); }
 
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 

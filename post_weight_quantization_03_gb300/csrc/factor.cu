@@ -16,9 +16,10 @@
 // where Bt is the transposed right-hand side of L Y = I, updated in place into Yt.
 // Finally U[i][j] = Yt[d-1-j][d-1-i] for i <= j.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
-#include "common.cuh"
+#include "graph_cache.cuh"
 
 namespace gptq {
 
@@ -499,18 +500,7 @@ struct SideStream {
   cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr,
               e1 = nullptr, e_in = nullptr, e_out = nullptr;
   int num_sms = 0;
-  // the most recent panel loops captured as graphs, and what each was captured for
-  struct Graph {
-    cudaGraphExec_t exec = nullptr;
-    const void *key_ptr[4] = {nullptr, nullptr, nullptr, nullptr};
-    int64_t key_d = -1;
-    float key_damp = 0.f;
-    unsigned kernels = 0;       // kernel launches in the graph
-    unsigned long long used = 0;
-  };
-  static constexpr int kGraphs = 8;
-  Graph graphs[kGraphs];
-  unsigned long long tick = 0;
+  GraphCache graphs;   // the panel loop captured per buffer set
 };
 constexpr int kMaxDevices = 128;
 std::mutex g_side_mu;
@@ -678,55 +668,20 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   SideStream *ss = nullptr;
   GPTQ_TRY(side_stream(&ss));
   std::lock_guard<std::mutex> lock(ss->enqueue);
-  // Graph replay: the loop is ~200 dependent launches on three streams; replaying it as one
-  // captured graph removes most of the per-launch latency between them.  The graph is
-  // captured and launched on the library's critical stream, joined to the caller's stream
-  // by an event on each side; inside a caller's own capture everything is launched directly.
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
-    (void)cudaGetLastError();
-    return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);
-  }
+  // Graph replay (graph_cache.cuh): the loop is ~200 dependent launches on three streams.
+  if (caller_capturing(s)) return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);
   GPTQ_CUDA_CHECK(cudaEventRecord(ss->e_in, s));
   GPTQ_CUDA_CHECK(cudaStreamWaitEvent(ss->crit, ss->e_in, 0));
-  const cudaStream_t o = ss->crit;   // the graph's origin stream
-  const void *key[4] = {H, U, dead_mask, ws};
-  SideStream::Graph *gr = nullptr, *lru = &ss->graphs[0];
-  for (SideStream::Graph &c : ss->graphs) {
-    if (c.exec && c.key_d == d && c.key_damp == damp && std::equal(key, key + 4, c.key_ptr))
-      gr = &c;
-    if (c.used < lru->used) lru = &c;
-  }
-  if (!gr) {
-    // capture; any failure (e.g. a one-time set-up call not allowed while capturing)
-    // falls back to launching directly
-    cudaGraph_t g = nullptr;
-    cudaGraphExec_t exec = nullptr;
-    const unsigned long long n0 = gptq_kernel_launches();
-    gptq_status st = GPTQ_ERR_CUDA;
-    if (cudaStreamBeginCapture(o, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
-      st = enqueue_prepare(H, d, damp, U, dead_mask, ws, o, ss);
-      if (cudaStreamEndCapture(o, &g) != cudaSuccess) st = GPTQ_ERR_CUDA;
-    }
-    if (st != GPTQ_OK || !g || cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
-      (void)cudaGetLastError();
-      if (g) cudaGraphDestroy(g);
-      return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);  // after the join above
-    }
-    cudaGraphDestroy(g);
-    gr = lru;
-    if (gr->exec) cudaGraphExecDestroy(gr->exec);
-    gr->exec = exec;
-    std::copy(key, key + 4, gr->key_ptr);
-    gr->key_d = d;
-    gr->key_damp = damp;
-    gr->kernels = (unsigned)(gptq_kernel_launches() - n0);  // counted while capturing
-  } else {
-    count_launch(gr->kernels);
-  }
-  gr->used = ++ss->tick;
-  GPTQ_CUDA_CHECK(cudaGraphLaunch(gr->exec, o));
-  GPTQ_CUDA_CHECK(cudaEventRecord(ss->e_out, o));
+  uint32_t damp_bits = 0;
+  memcpy(&damp_bits, &damp, 4);
+  const std::vector<uint64_t> key = {(uint64_t)H, (uint64_t)U, (uint64_t)dead_mask,
+                                     (uint64_t)ws, (uint64_t)d, (uint64_t)damp_bits};
+  gptq_status st = GPTQ_OK;
+  if (!ss->graphs.run(key, ss->crit, [&](cudaStream_t o) {
+        return enqueue_prepare(H, d, damp, U, dead_mask, ws, o, ss);
+      }, &st))
+    return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, ss);  // after the join above
+  GPTQ_CUDA_CHECK(cudaEventRecord(ss->e_out, ss->crit));
   GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e_out, 0));
   return GPTQ_OK;
 }

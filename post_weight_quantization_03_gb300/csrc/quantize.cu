@@ -14,6 +14,7 @@
 #include <cfloat>
 #include <mutex>
 
+#include "graph_cache.cuh"
 #include "tc.cuh"
 
 namespace gptq {
@@ -561,6 +562,8 @@ struct QuantStreams {
   cudaEvent_t start = nullptr, crit_done = nullptr, side_done = nullptr;
   cudaEvent_t e_ready[2] = {nullptr, nullptr};   // E of a block written (by parity)
   cudaEvent_t far_done[2] = {nullptr, nullptr};  // that block's far update finished
+  cudaEvent_t g_in = nullptr, g_out = nullptr;   // joins of a graph replay
+  GraphCache graphs;                             // the sweep captured per argument set
 };
 constexpr int kMaxDevices = 128;
 std::mutex g_qs_mu;
@@ -578,7 +581,7 @@ gptq_status quant_streams(QuantStreams **out) {
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.crit, cudaStreamNonBlocking, hi));
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.side, cudaStreamNonBlocking, lo));
     cudaEvent_t *evs[] = {&q.start, &q.crit_done, &q.side_done, &q.e_ready[0], &q.e_ready[1],
-                          &q.far_done[0], &q.far_done[1]};
+                          &q.far_done[0], &q.far_done[1], &q.g_in, &q.g_out};
     for (cudaEvent_t *e : evs) GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
   *out = &q;
@@ -624,17 +627,17 @@ size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, in
 // "GPTQ Hessian"): one grid pass per layer into the shared fp32 working copy, one sweep and
 // one trailing update per block over all rows, then each layer's rows packed into its own
 // outputs.  With one layer the per-row scale and zero are written in place.
-gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
-                                   const uint8_t *dead_mask, int bits, int block, void *ws,
-                                   cudaStream_t s, bool allow_overlap) {
-  static bool attr_done = false;
-  const size_t sweep_smem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sweep_smem));
-    attr_done = true;
-  }
+namespace {
+
+constexpr size_t kSweepSmem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
+
+// The sweep's launches (no set-up, no locking): on `s`, and with `qs` the blocked sweep's
+// far updates on qs->side and the rest on qs->crit (which is `s` itself when the whole
+// routine is captured on it).
+gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
+                                    const uint8_t *dead_mask, int bits, int block, void *ws,
+                                    cudaStream_t s, QuantStreams *qs) {
+  const size_t sweep_smem = kSweepSmem;
   int64_t m = 0;
   for (int i = 0; i < n; ++i) m += L[i].m;
   QuantWs q = carve_quantize(ws, m, d, block);
@@ -681,9 +684,7 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
       return launch_gemm_nt(g, q.st, st);
     };
-    QuantStreams *qs = nullptr;
-    const bool overlap = allow_overlap && d > 2 * (int64_t)block;
-    if (overlap) GPTQ_TRY(quant_streams(&qs));
+    const bool overlap = qs != nullptr;
     if (!overlap) {
       for (int64_t b0 = 0; b0 < d; b0 += block) {
         const int nb = (int)((d - b0) < block ? (d - b0) : block);
@@ -700,7 +701,6 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
       // the next sweep.  The next-block update of block b + 1 waits for block b's far
       // update, so every column receives its blocks' contributions in block order, exactly
       // as in the single-stream order above (the results are bit for bit the same).
-      std::lock_guard<std::mutex> lock(qs->enqueue);
       cudaStream_t c = qs->crit, sd = qs->side;
       int nsm = 0, dev = 0;
       GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
@@ -756,6 +756,46 @@ gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const floa
                                       cudaMemcpyDeviceToDevice, s));
     }
   }
+  return GPTQ_OK;
+}
+
+}  // namespace
+
+gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
+                                   const uint8_t *dead_mask, int bits, int block, void *ws,
+                                   cudaStream_t s, bool allow_overlap) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSweepSmem));
+    attr_done = true;
+  }
+  if (!allow_overlap || block == 1 || d <= 2 * (int64_t)block)
+    return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, s, nullptr);
+  QuantStreams *qs = nullptr;
+  GPTQ_TRY(quant_streams(&qs));
+  std::lock_guard<std::mutex> lock(qs->enqueue);
+  if (caller_capturing(s))
+    return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, s, qs);
+  // Graph replay (graph_cache.cuh), captured on the critical stream
+  GPTQ_CUDA_CHECK(cudaEventRecord(qs->g_in, s));
+  GPTQ_CUDA_CHECK(cudaStreamWaitEvent(qs->crit, qs->g_in, 0));
+  std::vector<uint64_t> key = {(uint64_t)n, (uint64_t)d, (uint64_t)U, (uint64_t)dead_mask,
+                               (uint64_t)bits, (uint64_t)block, (uint64_t)ws};
+  for (int i = 0; i < n; ++i) {
+    const uint64_t f[] = {(uint64_t)L[i].W, (uint64_t)L[i].wdtype, (uint64_t)L[i].m,
+                          (uint64_t)L[i].ldw, (uint64_t)L[i].qpacked, (uint64_t)L[i].scale,
+                          (uint64_t)L[i].zero, (uint64_t)L[i].W_hat};
+    key.insert(key.end(), f, f + 8);
+  }
+  gptq_status st = GPTQ_OK;
+  if (!qs->graphs.run(key, qs->crit, [&](cudaStream_t o) {
+        return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, o, qs);
+      }, &st))
+    return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, s, qs);
+  GPTQ_CUDA_CHECK(cudaEventRecord(qs->g_out, qs->crit));
+  GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, qs->g_out, 0));
   return GPTQ_OK;
 }
 
