@@ -562,7 +562,9 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   PrepWs w = carve_prepare(ws, d);
   const bool overlap = ss != nullptr;
   cudaStream_t b = overlap ? ss->s : s;
-  const int side_ctas = 0;  // persistent: one CTA per SM
+  // the side stream's persistent GEMMs leave 16 SMs to the critical chain (measured: better
+  // than all SMs, than one CTA per tile, and the same as 32)
+  const int side_ctas = overlap ? std::max(1, ss->num_sms - 16) : 0;
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
   dead_damp_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead_mask, w.st);
   GPTQ_LAUNCH_CHECK();
