@@ -370,42 +370,53 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
   const int tid = threadIdx.x;
   const int64_t rb = r0 + (int64_t)blockIdx.x * RM_ROWS;
   const int q0 = blockIdx.y * NCQ;
-#pragma unroll 4
-  for (int it = 0; it < 32 * NCQ * NB / 4 / RM_THREADS; ++it) {
+  // every global load of the CTA is issued before the first shared store (one round trip)
+  constexpr int NBI = 32 * NCQ * NB / 4 / RM_THREADS, NII = RM_ROWS * NB / 4 / RM_THREADS;
+  float4 bv[NBI], iv[NII];
+#pragma unroll
+  for (int it = 0; it < NBI; ++it) {
     const int e = it * RM_THREADS + tid;  // float4 index within the CTA's Bm rows
     const int j = e / (NB / 4), t4 = 4 * (e % (NB / 4));
     const int64_t bo = (int64_t)(32 * q0 + j) * ldb + t4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    bv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (32 * q0 + j < nj) {
-      v = *reinterpret_cast<const float4 *>(Bm + bo);
+      bv[it] = *reinterpret_cast<const float4 *>(Bm + bo);
       if (Bm_lo) {
         const float4 u = *reinterpret_cast<const float4 *>(Bm_lo + bo);
-        v = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+        bv[it] = make_float4(bv[it].x + u.x, bv[it].y + u.y, bv[it].z + u.z, bv[it].w + u.w);
       }
     }
-    *reinterpret_cast<float4 *>(Bs + j * RML + t4) = v;
   }
   const bool vec = (ldi % 4) == 0 && (((uintptr_t)In) % 16) == 0;
-#pragma unroll 4
-  for (int it = 0; it < RM_ROWS * NB / 4 / RM_THREADS; ++it) {
+#pragma unroll
+  for (int it = 0; it < NII; ++it) {
     const int e = it * RM_THREADS + tid;
     const int r = e / (NB / 4), t4 = 4 * (e % (NB / 4));
     const int64_t gr = rb + r;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    iv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (gr < r1) {
       if (vec && t4 + 4 <= n) {
-        v = *reinterpret_cast<const float4 *>(In + gr * ldi + t4);
+        iv[it] = *reinterpret_cast<const float4 *>(In + gr * ldi + t4);
         if (In_lo) {
           const float4 u = *reinterpret_cast<const float4 *>(In_lo + gr * ldi + t4);
-          v = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+          iv[it] = make_float4(iv[it].x + u.x, iv[it].y + u.y, iv[it].z + u.z, iv[it].w + u.w);
         }
       } else {
 #define RM_IN(q) ((t4 + q < n) ? In[gr * ldi + t4 + q] + (In_lo ? In_lo[gr * ldi + t4 + q] : 0.f) : 0.f)
-        v = make_float4(RM_IN(0), RM_IN(1), RM_IN(2), RM_IN(3));
+        iv[it] = make_float4(RM_IN(0), RM_IN(1), RM_IN(2), RM_IN(3));
 #undef RM_IN
       }
     }
-    *reinterpret_cast<float4 *>(Is + r * RML + t4) = v;
+  }
+#pragma unroll
+  for (int it = 0; it < NBI; ++it) {
+    const int e = it * RM_THREADS + tid;
+    *reinterpret_cast<float4 *>(Bs + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = bv[it];
+  }
+#pragma unroll
+  for (int it = 0; it < NII; ++it) {
+    const int e = it * RM_THREADS + tid;
+    *reinterpret_cast<float4 *>(Is + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = iv[it];
   }
   __syncthreads();
   const int rg = tid / 32, cg = tid % 32;
