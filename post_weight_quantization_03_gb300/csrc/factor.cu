@@ -258,9 +258,8 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
   if (tid == 0) { s_skip = st->status != 0; s_bad = -1; }
   __syncthreads();
   if (s_skip) return;
-#pragma unroll
-  for (int it = 0; it < NB * NB / 4 / PF_THREADS; ++it) {
-    const int e = it * PF_THREADS + tid;
+  // the block, padded with the identity beyond n; float4 index e = (row i, columns l4..l4+3)
+  auto load4 = [&](int e) {
     const int i = e / (NB / 4), l4 = 4 * (e % (NB / 4));
     float v[4];
     if (i < n && (d % 4) == 0 && l4 + 4 <= n) {
@@ -277,8 +276,17 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
       sv[q] = (i < n && l < n) ? v[q] : (i == l ? 1.0f : 0.0f);
     }
     *reinterpret_cast<float4 *>(S + i * PL + l4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+  };
+  // warp 0 loads the first leaf's PW x PW tile and starts on it at once; the other warps
+  // load the rest of the block meanwhile (the barrier after the first leaf orders both)
+  if (warp == 0) {
+    for (int t = lane; t < PW * PW / 4; t += 32) load4((t / (PW / 4)) * (NB / 4) + t % (PW / 4));
+    __syncwarp();
+  } else {
+#pragma unroll 4
+    for (int e = tid - 32; e < NB * NB / 4; e += PF_THREADS - 32)
+      if (e / (NB / 4) >= PW || e % (NB / 4) >= PW / 4) load4(e);
   }
-  __syncthreads();
 #pragma unroll 1
   for (int p = 0; p < NB / PW; ++p) {
     const int P0 = p * PW, R0 = P0 + PW;
