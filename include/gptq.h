@@ -152,7 +152,8 @@ size_t gptq_prepare_workspace_bytes(int64_t d_in);
  * U is computed as the inverse of the reversed-order ("UL") Cholesky factor R of H
  * (H = R R^T, R upper), which is the same matrix.
  *
- *   H          [d_in, d_in] fp32 symmetric, CONSUMED: overwritten as scratch.
+ *   H          [d_in, d_in] fp32 symmetric, CONSUMED: overwritten as scratch.  Only the
+ *              upper triangle and the diagonal are read (the lower triangle may hold anything).
  *   d_in       >= 1.
  *   damp       >= 0 relative damping (0.01 for the pages' 1 %).
  *   U          [d_in, d_in] fp32 out, upper triangular (lower triangle written as 0).
@@ -160,7 +161,7 @@ size_t gptq_prepare_workspace_bytes(int64_t d_in);
  *   n_dead     HOST int32 out, may be NULL.
  *   ws         workspace of ws_bytes >= gptq_prepare_workspace_bytes(d_in).
  * SYNCHRONIZES `stream` before returning.  Errors: INVALID_ARG, WORKSPACE, NOT_PD (a
- * pivot <= 0: U is then undefined), NONFINITE (NaN/Inf in H), CUDA.
+ * pivot <= 0: U is then undefined), NONFINITE (NaN/Inf in the part of H read), CUDA.
  */
 gptq_status gptq_prepare(float *H, int64_t d_in, float damp, float *U, uint8_t *dead_mask,
                          int32_t *n_dead, void *ws, size_t ws_bytes, gptq_stream_t stream);

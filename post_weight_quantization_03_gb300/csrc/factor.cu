@@ -29,7 +29,9 @@ constexpr int NB = 128;            // panel width
 
 // ---------------------------------------------------------------------------------------
 // Dead columns and damping (one CTA): dead = {i : H_ii == 0}; H_ii <- 1 for dead i;
-// lambda = damp * mean(diag); H_ii += lambda.
+// lambda = damp * mean(diag); H_ii += lambda.  The damped diagonal is written reversed
+// (A_ii = damped H_{d-1-i, d-1-i}): thread t swaps the pair (t, d-1-t), so no entry is
+// read after another thread wrote it.
 // ---------------------------------------------------------------------------------------
 __global__ void dead_damp_kernel(float *H, int64_t d, float damp, uint8_t *dead_mask,
                                  DevStatus *st) {
@@ -67,32 +69,77 @@ __global__ void dead_damp_kernel(float *H, int64_t d, float damp, uint8_t *dead_
     st->diag_sum = diag_sum;
     if (s_bad) set_status(st, GPTQ_ERR_NONFINITE);
   }
-  for (int64_t i = threadIdx.x; i < d; i += blockDim.x) {
-    const float h = H[i * d + i];
-    const bool dead = (h == 0.0f);
-    if (dead_mask) dead_mask[i] = dead ? 1 : 0;
-    H[i * d + i] = (dead ? 1.0f : h) + lam;
+  for (int64_t i = threadIdx.x; i < (d + 1) / 2; i += blockDim.x) {
+    const int64_t j = d - 1 - i;
+    const float hi = H[i * d + i], hj = H[j * d + j];
+    const bool di = hi == 0.0f, dj = hj == 0.0f;
+    if (dead_mask) {
+      dead_mask[i] = di ? 1 : 0;
+      dead_mask[j] = dj ? 1 : 0;
+    }
+    H[i * d + i] = (dj ? 1.0f : hj) + lam;
+    H[j * d + j] = (di ? 1.0f : hi) + lam;
   }
 }
 
-// In-place reversal of the d*d array (A = P H P) with a finiteness check.
-__global__ void reverse_kernel(float *H, int64_t n, DevStatus *st) {
+// ---------------------------------------------------------------------------------------
+// A = P H P below the diagonal (P the order reversal): A_ij = H_{d-1-i, d-1-j} for i > j,
+// read from H's strict upper triangle, which no thread writes (only the upper triangle of
+// the symmetric H is read, with a finiteness check).  The same pass sets Yt to the
+// identity on every block row's diagonal block and the blocks right of it: the only part of
+// Yt that the panel loop reads.  One CTA per row i; VEC moves float4s (d % 4 == 0, H and
+// Yt 16-byte aligned), each thread issuing its loads before its stores.
+// ---------------------------------------------------------------------------------------
+constexpr int RV_THREADS = 256, RV_UNROLL = 4;
+
+template <bool VEC>
+__global__ void __launch_bounds__(RV_THREADS)
+reverse_lower_kernel(float *H, int64_t d, float *Yt, DevStatus *st) {
+  const int64_t i = blockIdx.x, r = d - 1 - i;
+  const float *src = H + r * d;   // source row: A_ij = src[d - 1 - j]
+  float *dst = H + i * d;
+  const int tid = threadIdx.x;
   int bad = 0;
-  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n / 2;
-       k += (int64_t)gridDim.x * blockDim.x) {
-    const float a = H[k], b = H[n - 1 - k];
-    bad |= !isfinite(a) | !isfinite(b);
-    H[k] = b;
-    H[n - 1 - k] = a;
+  if (VEC) {
+    // float4 q covers j = 4q .. 4q+3 < i, i.e. q < i / 4: source columns d-4-4q .. d-1-4q
+    const int64_t nq = i / 4;
+    for (int64_t q0 = tid; q0 < nq; q0 += (int64_t)RV_THREADS * RV_UNROLL) {
+      float4 v[RV_UNROLL];
+#pragma unroll
+      for (int u = 0; u < RV_UNROLL; ++u) {
+        const int64_t q = q0 + (int64_t)u * RV_THREADS;
+        if (q < nq) v[u] = *reinterpret_cast<const float4 *>(src + d - 4 - 4 * q);
+      }
+#pragma unroll
+      for (int u = 0; u < RV_UNROLL; ++u) {
+        const int64_t q = q0 + (int64_t)u * RV_THREADS;
+        if (q < nq) {
+          bad |= !isfinite(v[u].x) | !isfinite(v[u].y) | !isfinite(v[u].z) | !isfinite(v[u].w);
+          *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(v[u].w, v[u].z, v[u].y, v[u].x);
+        }
+      }
+    }
+    const int64_t j = 4 * nq + tid;   // the last i % 4 entries left of the diagonal
+    if (j < i) {
+      const float v = src[d - 1 - j];
+      bad |= !isfinite(v);
+      dst[j] = v;
+    }
+    // Yt row i from column (i / NB) * NB: identity
+    const int64_t c0 = (i / NB) * NB;
+    for (int64_t c = c0 + 4 * tid; c < d; c += 4 * RV_THREADS)
+      *reinterpret_cast<float4 *>(Yt + i * d + c) =
+          make_float4(c == i ? 1.f : 0.f, c + 1 == i ? 1.f : 0.f, c + 2 == i ? 1.f : 0.f,
+                      c + 3 == i ? 1.f : 0.f);
+  } else {
+    for (int64_t j = tid; j < i; j += RV_THREADS) {
+      const float v = src[d - 1 - j];
+      bad |= !isfinite(v);
+      dst[j] = v;
+    }
+    for (int64_t c = (i / NB) * NB + tid; c < d; c += RV_THREADS) Yt[i * d + c] = c == i ? 1.f : 0.f;
   }
-  if (bad) set_status(st, GPTQ_ERR_NONFINITE);
-}
-
-// Yt = identity.
-__global__ void identity_kernel(float *Y, int64_t d) {
-  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < d * d;
-       k += (int64_t)gridDim.x * blockDim.x)
-    Y[k] = (k / d == k % d) ? 1.0f : 0.0f;
+  if (__syncthreads_or(bad) && tid == 0) set_status(st, GPTQ_ERR_NONFINITE);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -114,9 +161,11 @@ __global__ void identity_kernel(float *Y, int64_t d) {
 //            Bt_cr -= Yt_cp L_rp^T                c < R0 <= r       (inverse, step b)
 // Phase 2 is a product over PW k in tiles of 8 rows x 64 columns per warp (A read by
 // broadcast, B as float4 along k at row stride 132: eight consecutive rows fall in distinct
-// bank groups).  Rows P0..R0-1 of Bt (identity rows, untouched until then) are written
-// while the leaf runs, and the rows of Linv that phase 1 finishes are stored during
-// phase 2.  A non-positive pivot records NOT_PD with its global index.
+// bank groups).  The leaf runs one sub-panel ahead: after phase 1 of sub-panel p, warp 0
+// applies phase 2 to the next leaf's tile alone and factors it, while the other fifteen
+// warps run the rest of phase 2 and write the next identity rows of Bt (untouched until
+// then), so one barrier per sub-panel orders both.  The rows of Linv that phase 1 finishes
+// are stored before the split.  A non-positive pivot records NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
 constexpr int PF_THREADS = 512;
 constexpr int PF_WARPS = PF_THREADS / 32;
@@ -192,6 +241,42 @@ __device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float 
   // a failed pivot left rl = 0 in its lane
   const unsigned badm = __ballot_sync(0xffffffffu, own && !(rdl > 0.0f));
   return badm ? t0 + __ffs((int)badm) - 1 : -1;
+}
+
+// The next leaf's tile (rows and columns t0..t0+PW-1 of S) minus its product over the
+// sub-panel just solved (columns c0..c0+PW-1): the part of phase 2 that the next leaf
+// waits for.  Lane (i, h) = (lane % PW, lane / PW) owns row t0 + i, columns t0 + 8h .. +7;
+// the whole tile is written (the leaf reads its lower part only and clears the rest).
+__device__ __forceinline__ void leaf_tile_update(float *S, int t0, int c0, int lane) {
+  const int i = lane % PW, h = lane / PW;
+  float x[PW];
+#pragma unroll
+  for (int q = 0; q < PW / 4; ++q) {
+    const float4 v = *reinterpret_cast<const float4 *>(S + (t0 + i) * PL + c0 + 4 * q);
+    x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+  }
+  float2 acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    acc[j] = make_float2(0.f, 0.f);
+    const float *yj = S + (t0 + 8 * h + j) * PL + c0;
+#pragma unroll
+    for (int q = 0; q < PW / 4; ++q) {
+      const float4 v = *reinterpret_cast<const float4 *>(yj + 4 * q);
+      acc[j] = __ffma2_rn(make_float2(x[4 * q], x[4 * q + 1]), make_float2(v.x, v.y), acc[j]);
+      acc[j] = __ffma2_rn(make_float2(x[4 * q + 2], x[4 * q + 3]), make_float2(v.z, v.w), acc[j]);
+    }
+  }
+  float *ci = S + (t0 + i) * PL + t0 + 8 * h;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    float4 c = *reinterpret_cast<float4 *>(ci + 4 * q);
+    c.x -= acc[4 * q].x + acc[4 * q].y;
+    c.y -= acc[4 * q + 1].x + acc[4 * q + 1].y;
+    c.z -= acc[4 * q + 2].x + acc[4 * q + 2].y;
+    c.w -= acc[4 * q + 3].x + acc[4 * q + 3].y;
+    *reinterpret_cast<float4 *>(ci + 4 * q) = c;
+  }
 }
 
 // x L_pp^T = c for one row, in place: z_l -= z_j M[j][l] (l > j), then x_j = z_j / L_jj.
@@ -277,32 +362,32 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
     }
     *reinterpret_cast<float4 *>(S + i * PL + l4) = make_float4(sv[0], sv[1], sv[2], sv[3]);
   };
-  // warp 0 loads the first leaf's PW x PW tile and starts on it at once; the other warps
-  // load the rest of the block meanwhile (the barrier after the first leaf orders both)
+  // identity rows R0..R0+PW-1 of Bt, first read by the phase 1 of sub-panel R0 / PW
+  auto identity_rows = [&](int R0) {
+    for (int e = tid - 32; e < PW * NB / 4; e += PF_THREADS - 32) {
+      const int r = R0 + e / (NB / 4), c4 = 4 * (e % (NB / 4));
+      *reinterpret_cast<float4 *>(Bt + r * PL + c4) =
+          make_float4(r == c4 ? 1.f : 0.f, r == c4 + 1 ? 1.f : 0.f, r == c4 + 2 ? 1.f : 0.f,
+                      r == c4 + 3 ? 1.f : 0.f);
+    }
+  };
+  // warp 0 loads the first leaf's PW x PW tile and factors it at once; the other warps load
+  // the rest of the block and the first identity rows meanwhile
   if (warp == 0) {
     for (int t = lane; t < PW * PW / 4; t += 32) load4((t / (PW / 4)) * (NB / 4) + t % (PW / 4));
     __syncwarp();
+    const int bad = leaf_factor(S, M, rd, cb, 0, lane);
+    if (lane == 0 && bad >= 0) s_bad = bad;
   } else {
 #pragma unroll 4
     for (int e = tid - 32; e < NB * NB / 4; e += PF_THREADS - 32)
       if (e / (NB / 4) >= PW || e % (NB / 4) >= PW / 4) load4(e);
+    identity_rows(0);
   }
+  __syncthreads();
 #pragma unroll 1
   for (int p = 0; p < NB / PW; ++p) {
     const int P0 = p * PW, R0 = P0 + PW;
-    if (warp == 0) {
-      const int bad = leaf_factor(S, M, rd, cb, P0, lane);
-      if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
-    } else {
-      // identity rows P0..R0-1 of Bt, first read by this sub-panel's phase 1
-      for (int e = tid - 32; e < PW * NB / 4; e += PF_THREADS - 32) {
-        const int r = P0 + e / (NB / 4), c4 = 4 * (e % (NB / 4));
-        *reinterpret_cast<float4 *>(Bt + r * PL + c4) =
-            make_float4(r == c4 ? 1.f : 0.f, r == c4 + 1 ? 1.f : 0.f, r == c4 + 2 ? 1.f : 0.f,
-                        r == c4 + 3 ? 1.f : 0.f);
-      }
-    }
-    __syncthreads();
     // phase 1: row r < R0 of Bt or row r >= R0 of S, columns P0..R0-1, one thread each
     if (tid < NB) {
       float *xr = (tid < R0 ? Bt : S) + tid * PL + P0;
@@ -332,16 +417,27 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
       Linv[(i4 + 2) * NB + c] = (cc && i4 + 2 < n) ? v.z : 0.0f;
       Linv[(i4 + 3) * NB + c] = (cc && i4 + 3 < n) ? v.w : 0.0f;
     }
-    // phase 2 over 8-row tiles of [Bt rows < R0 ; S rows >= R0] x 64-column tiles from R0
-    const int nct = (NB - R0 + 63) / 64;
+    if (R0 == NB) break;
+    if (warp == 0) {
+      // the next leaf: its tile's share of phase 2, then its factorization
+      leaf_tile_update(S, R0, P0, lane);
+      __syncwarp();
+      const int bad = leaf_factor(S, M, rd, cb, R0, lane);
+      if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
+    } else {
+      // phase 2 over 8-row tiles of [Bt rows < R0 ; S rows >= R0] x 64-column tiles from R0,
+      // without S rows R0..R0+PW-1 (their lower part is the next leaf's tile)
+      const int nct = (NB - R0 + 63) / 64;
 #pragma unroll 1
-    for (int t = warp; t < (NB / 8) * nct; t += PF_WARPS) {
-      const int m0 = 8 * (t / nct), n0 = R0 + 64 * (t % nct);
-      if (m0 < R0) {
-        update_tile(Bt, Bt + P0, S + P0, m0, n0, lane, false);
-      } else if (n0 <= m0 + 7) {
-        update_tile(S, S + P0, S + P0, m0, n0, lane, true);
+      for (int t = warp - 1; t < (NB / 8) * nct; t += PF_WARPS - 1) {
+        const int m0 = 8 * (t / nct), n0 = R0 + 64 * (t % nct);
+        if (m0 < R0) {
+          update_tile(Bt, Bt + P0, S + P0, m0, n0, lane, false);
+        } else if (m0 >= R0 + PW && n0 <= m0 + 7) {
+          update_tile(S, S + P0, S + P0, m0, n0, lane, true);
+        }
       }
+      identity_rows(R0);
     }
     __syncthreads();
   }
@@ -469,22 +565,60 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
   }
 }
 
-// U[i][j] = Yt[d-1-j][d-1-i] for i <= j, 0 below the diagonal (32 x 32 smem tiles).
-__global__ void assemble_u_kernel(const float *Yt, float *U, int64_t d) {
-  __shared__ float tile[32][33];
-  const int64_t i0 = (int64_t)blockIdx.y * 32, j0 = (int64_t)blockIdx.x * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  // Tile of U rows [i0, i0+32), cols [j0, j0+32) reads Yt rows d-1-j, cols d-1-i.
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int64_t j = j0 + yy, i = i0 + tx;
-    float v = 0.f;
-    if (i < d && j < d && i <= j) v = Yt[(d - 1 - j) * d + (d - 1 - i)];
-    tile[yy][tx] = v;
+// U[i][j] = Yt[d-1-j][d-1-i] for i <= j, 0 below the diagonal: 64 x 64 tiles through shared
+// memory (Yt rows read forwards and stored reversed, U rows written), float4 with VEC
+// (d % 4 == 0, both 16-byte aligned).  Tiles wholly below the diagonal only write zeros.
+constexpr int AU_T = 64;
+
+template <bool VEC>
+__global__ void __launch_bounds__(256) assemble_u_kernel(const float *Yt, float *U, int64_t d) {
+  __shared__ float tile[AU_T][AU_T + 1];   // tile[jj][ii] = Yt[d-1-j][d-1-i]
+  const int64_t i0 = (int64_t)blockIdx.y * AU_T, j0 = (int64_t)blockIdx.x * AU_T;
+  const int tid = threadIdx.x, c4 = 4 * (tid % 16), rr = tid / 16;
+  const bool any = i0 <= j0 + AU_T - 1;
+  if (any) {
+    // Yt row y = d-1-(j0+jj), columns x = xs + c4 + e hold ii = AU_T-1-c4-e (xs = d-AU_T-i0)
+    const int64_t xs = d - AU_T - i0;
+#pragma unroll
+    for (int p = 0; p < AU_T / 16; ++p) {
+      const int jj = rr + 16 * p;
+      const int64_t y = d - 1 - (j0 + jj);
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (y >= 0) {
+        const int64_t x = xs + c4;
+        if (VEC && x >= 0) {
+          const float4 u = *reinterpret_cast<const float4 *>(Yt + y * d + x);
+          v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (x + e >= 0) v[e] = Yt[y * d + x + e];
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) tile[jj][AU_T - 1 - c4 - e] = v[e];
+    }
   }
   __syncthreads();
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int64_t i = i0 + yy, j = j0 + tx;
-    if (i < d && j < d) U[i * d + j] = tile[tx][yy];
+#pragma unroll
+  for (int p = 0; p < AU_T / 16; ++p) {
+    const int ii = rr + 16 * p;
+    const int64_t i = i0 + ii;
+    if (i >= d) continue;
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t j = j0 + c4 + e;
+      v[e] = (any && i <= j) ? tile[c4 + e][ii] : 0.f;
+    }
+    const int64_t j = j0 + c4;
+    if (VEC && j + 4 <= d) {
+      *reinterpret_cast<float4 *>(U + i * d + j) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j + e < d) U[i * d + j + e] = v[e];
+    }
   }
 }
 
@@ -585,11 +719,12 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   // than all SMs, than one CTA per tile, and the same as 32)
   const int side_ctas = overlap ? std::max(1, ss->num_sms - 16) : 0;
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
+  // vector path: rows of H, Yt and U start 16-byte aligned (the workspace is)
+  const bool vec = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0 && (((uintptr_t)U) % 16) == 0;
   dead_damp_kernel<<<1, 1024, 0, s>>>(H, d, damp, dead_mask, w.st);
   GPTQ_LAUNCH_CHECK();
-  reverse_kernel<<<1024, 256, 0, s>>>(H, d * d, w.st);
-  GPTQ_LAUNCH_CHECK();
-  identity_kernel<<<1024, 256, 0, s>>>(w.Yt, d);
+  if (vec) reverse_lower_kernel<true><<<(unsigned)d, RV_THREADS, 0, s>>>(H, d, w.Yt, w.st);
+  else reverse_lower_kernel<false><<<(unsigned)d, RV_THREADS, 0, s>>>(H, d, w.Yt, w.st);
   GPTQ_LAUNCH_CHECK();
   cudaStream_t c = overlap ? ss->crit : s;  // the critical chain
   if (overlap) {
@@ -664,8 +799,9 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e1, 0));
     for (int p = 0; p < std::min(k, 2); ++p) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[p], 0));
   }
-  dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
-  assemble_u_kernel<<<tg, dim3(32, 8), 0, s>>>(w.Yt, U, d);
+  dim3 tg((unsigned)ceil_div(d, AU_T), (unsigned)ceil_div(d, AU_T));
+  if (vec) assemble_u_kernel<true><<<tg, 256, 0, s>>>(w.Yt, U, d);
+  else assemble_u_kernel<false><<<tg, 256, 0, s>>>(w.Yt, U, d);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }

@@ -196,6 +196,35 @@ def test_prepare_nonfinite():
     assert ei.value.status == 3
 
 
+def test_prepare_nonfinite_diagonal():
+    H = torch.eye(65, device=DEV)
+    H[64, 64] = float("inf")
+    with pytest.raises(gptq.GptqError) as ei:
+        gptq.prepare(H, 0.01)
+    assert ei.value.status == 3
+
+
+@pytest.mark.parametrize("d", [301, 512])     # odd (scalar path), and the float4 path
+def test_prepare_reads_only_the_upper_triangle(d):
+    # NaN below the diagonal changes nothing; the dead column sits at the middle of the
+    # order reversal (for odd d the entry that maps to itself)
+    H64 = _oracle_h(d, 2 * d, 2, 1, seed=40 + d)
+    mid = d // 2
+    H64[mid, :] = 0.0
+    H64[:, mid] = 0.0
+    H32 = H64.astype(np.float32)
+    Hd, dmask, _ = O.damp_hessian(H32.astype(np.float64))
+    Ur = O.inverse_cholesky_upper(Hd)
+    Hn = H32.copy()
+    Hn[np.tril_indices(d, -1)] = np.nan
+    U, mask, n_dead = gptq.prepare(torch.from_numpy(Hn).to(DEV), 0.01)
+    mask = mask.cpu().numpy().astype(bool)
+    assert mask[mid] and np.array_equal(mask, dmask) and n_dead == int(dmask.sum())
+    U = U.cpu().numpy()
+    assert np.all(np.tril(U, -1) == 0)
+    assert PT.u_rowwise_err(U, Ur) <= PT.TOL_U
+
+
 # ---------------------------------------------------------------------------------------
 # Steps 4-5 (+ packing): the sweep, on the oracle's U
 # ---------------------------------------------------------------------------------------
