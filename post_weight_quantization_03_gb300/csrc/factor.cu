@@ -649,9 +649,10 @@ PrepWs carve_prepare(void *ws, int64_t d) {
 // blocks are dispatched first whenever an SM has room) and the rest beside it on `s`.
 struct SideStream {
   std::mutex enqueue;  // one panel loop at a time enqueues on these events
-  cudaStream_t s = nullptr, crit = nullptr;
-  cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, e0 = nullptr,
-              e1 = nullptr, e_in = nullptr, e_out = nullptr;
+  cudaStream_t s = nullptr, crit = nullptr, crit2 = nullptr;
+  cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, en[2] = {nullptr, nullptr},
+              ep[2] = {nullptr, nullptr}, ed[2] = {nullptr, nullptr}, e0 = nullptr, e1 = nullptr,
+              e_in = nullptr, e_out = nullptr;
   int num_sms = 0;
   GraphCache graphs;   // the panel loop captured per buffer set
 };
@@ -670,10 +671,16 @@ gptq_status side_stream(SideStream **out) {
     GPTQ_CUDA_CHECK(cudaDeviceGetStreamPriorityRange(&lo, &hi));
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo));
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit, cudaStreamNonBlocking, hi));
+    // one level below the critical chain (priorities run from lo down to hi)
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit2, cudaStreamNonBlocking,
+                                                 hi < lo ? hi + 1 : hi));
     GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&ss.num_sms, cudaDevAttrMultiProcessorCount, dev));
     for (int b = 0; b < 2; ++b) {
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ea[b], cudaEventDisableTiming));
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.eb[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.en[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ep[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ed[b], cudaEventDisableTiming));
     }
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e0, cudaEventDisableTiming));
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e1, cudaEventDisableTiming));
@@ -693,16 +700,19 @@ size_t prepare_ws_bytes(int64_t d) {
 
 // Panel loop.  On the critical stream (highest priority; the caller's stream when the
 // side stream cannot be used):
-//   potrf(k) -> trsm(k) for all rows below -> the next panel column's update
-//   (rows >= k1, columns [k1, k1 + NB)) -> potrf(k + 1) ...
-// On the side stream, once panel k's factor and L panel exist:
+//   potrf(k) -> trsm(k) for the next NB rows -> the next panel column's update on its
+//   diagonal block (rows [k1, k1 + NB)) -> potrf(k + 1) ...
+// On a second critical stream, once potrf(k) is done: trsm(k) for the rows below, then (once
+// the critical stream's NB rows of L exist) the next column's update for those rows, beside
+// potrf(k + 1), which leaves all but one SM idle; trsm(k + 1) waits for it.  On the side
+// stream, once panel k's factor and L panel exist:
 //   inverse step a(k) -> the rest of the trailing update (the lower square from
 //   k1 + NB) -> inverse step b(k).
 // potrf(k) waits for the side stream's panel k - 2, which last wrote its diagonal block
 // and read the panel buffers it is about to overwrite.  Updates of one column block by
-// both streams are atomic adds (L2 reduce-adds in the tensor-core epilogue, red.add in the
+// two streams are atomic adds (L2 reduce-adds in the tensor-core epilogue, red.add in the
 // next-column update); where C is not 16-byte aligned everything runs on the caller's
-// stream.  The caller's stream waits for both at the end.
+// stream.  The caller's stream waits for all of them at the end.
 namespace {
 
 // The panel loop's launches (no set-up, no locking): on `s`, and with `ss` on its two
@@ -734,6 +744,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   }
   float *A = H;  // reversed, damped Hessian; lower triangle is the Cholesky workspace
   int k = 0;
+  bool next_rest = false;   // the last panel's column update left rows to the second stream
   for (int64_t k0 = 0; k0 < d; k0 += NB, ++k) {
     const int par = k & 1;
     const int n = (int)std::min<int64_t>(NB, d - k0);
@@ -741,23 +752,57 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->eb[par], 0));
     potrf_kernel<<<1, PF_THREADS, potrf_smem, c>>>(A, d, k0, n, w.Linv[par], w.st);
     GPTQ_LAUNCH_CHECK();
+    if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->ep[par], c));
+    // the previous column update's rows below the diagonal block (second critical stream)
+    if (overlap && next_rest) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->en[par ^ 1], 0));
+    next_rest = false;
     if (k1 < d) {
-      // trsm: rows [k1, d) of panel k -> L panel (hi/lo)
-      dim3 g((unsigned)ceil_div(d - k1, RM_ROWS), 4);
-      rowmul_kernel<1><<<g, RM_THREADS, rmq_smem, c>>>(A + k0, nullptr, d, nullptr, 0, k1, d,
-                                                      w.Linv[par], nullptr, NB, n, n, 0,
-                                                      w.Lhi[par], w.Llo[par], w.st);
-      GPTQ_LAUNCH_CHECK();
-      // next panel column: A[k1:, k1:k1+NB] -= L[k1:] L[k1:k1+NB]^T (fp32 from the head +
-      // tail panels; atomic adds: the side stream's previous trailing update adds here too)
       const int nn = (int)std::min<int64_t>(NB, d - k1);
-      dim3 g2((unsigned)ceil_div(d - k1, RM_ROWS), (unsigned)ceil_div(nn, 32));
-      rowmul_kernel<1><<<g2, RM_THREADS, rmq_smem, c>>>(
-          w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, 0, d - k1,
-          w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
-      GPTQ_LAUNCH_CHECK();
-    }
-    if (overlap) {
+      // trsm: rows [r0, r1) of panel k -> L panel (hi/lo)
+      auto trsm = [&](int64_t r0, int64_t r1, cudaStream_t st) {
+        dim3 g((unsigned)ceil_div(r1 - r0, RM_ROWS), 4);
+        rowmul_kernel<1><<<g, RM_THREADS, rmq_smem, st>>>(A + k0, nullptr, d, nullptr, 0, r0, r1,
+                                                         w.Linv[par], nullptr, NB, n, n, 0,
+                                                         w.Lhi[par], w.Llo[par], w.st);
+      };
+      // next panel column, rows k1 + [r0, r1): A[., k1:k1+NB] -= L[.] L[k1:k1+NB]^T (fp32
+      // from the head + tail panels; atomic adds: the side stream's previous trailing update
+      // adds here too)
+      auto next_col = [&](int64_t r0, int64_t r1, cudaStream_t st) {
+        dim3 g2((unsigned)ceil_div(r1 - r0, RM_ROWS), (unsigned)ceil_div(nn, 32));
+        rowmul_kernel<1><<<g2, RM_THREADS, rmq_smem, st>>>(
+            w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, r0, r1,
+            w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
+      };
+      if (overlap && d - k1 > nn) {
+        cudaStream_t c2 = ss->crit2;
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c2, ss->ep[par], 0));
+        trsm(k1 + nn, d, c2);                     // the rows below, beside the chain
+        GPTQ_LAUNCH_CHECK();
+        GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c2));
+        trsm(k1, k1 + nn, c);                     // the next potrf's rows
+        GPTQ_LAUNCH_CHECK();
+        GPTQ_CUDA_CHECK(cudaEventRecord(ss->ed[par], c));
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c2, ss->ed[par], 0));
+        next_col(nn, d - k1, c2);                 // beside the next potrf
+        GPTQ_LAUNCH_CHECK();
+        GPTQ_CUDA_CHECK(cudaEventRecord(ss->en[par], c2));
+        next_rest = true;
+        next_col(0, nn, c);                       // the next potrf's block
+        GPTQ_LAUNCH_CHECK();
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ed[par], 0));
+      } else {
+        trsm(k1, d, c);
+        GPTQ_LAUNCH_CHECK();
+        next_col(0, d - k1, c);
+        GPTQ_LAUNCH_CHECK();
+        if (overlap) {
+          GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c));
+          GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
+        }
+      }
+    } else if (overlap) {
       GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
     }

@@ -48,7 +48,11 @@ struct GraphCache {
         st = enqueue(origin);
         if (cudaStreamEndCapture(origin, &g) != cudaSuccess) st = GPTQ_ERR_CUDA;
       }
-      if (st != GPTQ_OK || !g || cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+      // kernel nodes keep the priority of the stream they were captured on (critical chain
+      // over side work); without this flag the whole graph runs at the launch stream's
+      if (st != GPTQ_OK || !g ||
+          cudaGraphInstantiateWithFlags(&exec, g, cudaGraphInstantiateFlagUseNodePriority) !=
+              cudaSuccess) {
         (void)cudaGetLastError();
         if (g) cudaGraphDestroy(g);
         if (status) *status = st;
