@@ -32,20 +32,35 @@ constexpr int UD_FLOATS = SB * LDU + SB;
 
 // ---------------------------------------------------------------------------------------
 // Grid: per-row asymmetric min-max with 0 in the range; fp32 working copy of W with dead
-// columns zeroed.  One warp per row.
+// columns zeroed.  One warp per row; with `vec` (rows 16-byte aligned) W is read 16 bytes
+// and the copy written 4 floats at a time.
 // ---------------------------------------------------------------------------------------
 template <typename T>
 __global__ void grid_kernel(const T *__restrict__ W, int64_t m, int64_t d, int64_t ldw,
                             const uint8_t *__restrict__ dead, float maxq,
                             float *__restrict__ scale, int32_t *__restrict__ zero,
-                            float *__restrict__ Wf, int64_t ldwf, DevStatus *st) {
+                            float *__restrict__ Wf, int64_t ldwf, int vec, DevStatus *st) {
+  constexpr int VE = 16 / sizeof(T);   // elements per 16-byte load
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= m) return;
   const T *w = W + row * ldw;
+  const int64_t dv = vec ? (d / VE) * VE : 0;   // the 16-byte part of the row
   float lo = 0.f, hi = 0.f;
   int bad = 0;
-  for (int64_t j = lane; j < d; j += 32) {
+#pragma unroll 4
+  for (int64_t j = (int64_t)lane * VE; j < dv; j += 32 * VE) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(w + j);
+    const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+    for (int k = 0; k < VE; ++k) {
+      const float v = to_f32(e[k]);
+      bad |= !isfinite(v);
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  }
+  for (int64_t j = dv + lane; j < d; j += 32) {
     const float v = to_f32(w[j]);
     bad |= !isfinite(v);
     lo = fminf(lo, v);
@@ -65,60 +80,107 @@ __global__ void grid_kernel(const T *__restrict__ W, int64_t m, int64_t d, int64
     if (bad) set_status(st, GPTQ_ERR_NONFINITE);
   }
   float *wf = Wf + row * ldwf;
-  for (int64_t j = lane; j < d; j += 32) wf[j] = (dead && dead[j]) ? 0.0f : to_f32(w[j]);
+#pragma unroll 2
+  for (int64_t j = (int64_t)lane * VE; j < dv; j += 32 * VE) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(w + j);
+    const T *e = reinterpret_cast<const T *>(&u);
+    float v[VE];
+#pragma unroll
+    for (int k = 0; k < VE; ++k) v[k] = (dead && dead[j + k]) ? 0.0f : to_f32(e[k]);
+#pragma unroll
+    for (int k = 0; k < VE; k += 4)
+      *reinterpret_cast<float4 *>(wf + j + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+  }
+  for (int64_t j = dv + lane; j < d; j += 32) wf[j] = (dead && dead[j]) ? 0.0f : to_f32(w[j]);
 }
 
 // ---------------------------------------------------------------------------------------
-// Lt = U^T (lower part only: Lt[i][j] = U[j][i], j <= i) as a TF32 head/tail pair.
+// Lt = U^T (lower part only: Lt[i][j] = U[j][i], j <= i) as a TF32 head/tail pair, in 64 x 64
+// tiles through shared memory (U rows read, Lt rows written; float4 with VEC: d % 4 == 0
+// and U 16-byte aligned).  Tiles wholly above the diagonal are never read and not written.
 // ---------------------------------------------------------------------------------------
-__global__ void lt_split_kernel(const float *__restrict__ U, int64_t d, float *__restrict__ hi,
-                                float *__restrict__ lo, int64_t ld) {
-  __shared__ float tile[32][33];
-  const int64_t bi = blockIdx.y, bj = blockIdx.x;  // Lt tile (rows bi, cols bj)
-  if (bi < bj) return;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
-  // Lt[bi*32 + r][bj*32 + c] = U[bj*32 + c][bi*32 + r]: read U rows bj*32+yy, cols bi*32+tx
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int64_t ur = bj * 32 + yy, uc = bi * 32 + tx;
-    tile[yy][tx] = (ur < d && uc < d && ur <= uc) ? U[ur * d + uc] : 0.0f;
+constexpr int LT_T = 64;
+
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+lt_split_kernel(const float *__restrict__ U, int64_t d, float *__restrict__ hi,
+                float *__restrict__ lo, int64_t ld) {
+  __shared__ float tile[LT_T][LT_T + 1];   // tile[cc][rr] = U[c0 + cc][r0 + rr]
+  const int64_t r0 = (int64_t)blockIdx.y * LT_T, c0 = (int64_t)blockIdx.x * LT_T;
+  if (r0 + LT_T - 1 < c0) return;
+  const int tid = threadIdx.x, c4 = 4 * (tid % 16), t16 = tid / 16;
+#pragma unroll
+  for (int p = 0; p < LT_T / 16; ++p) {
+    const int cc = t16 + 16 * p;
+    const int64_t c = c0 + cc, r = r0 + c4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (c < d) {
+      if (VEC && r + 4 <= d) {
+        const float4 u = *reinterpret_cast<const float4 *>(U + c * d + r);
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (r + e < d) v[e] = U[c * d + r + e];
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tile[cc][c4 + e] = (c <= r + e) ? v[e] : 0.f;
   }
   __syncthreads();
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int64_t r = bi * 32 + yy, c = bj * 32 + tx;
-    if (r < d && c < d) {
-      const float v = tile[tx][yy];
-      const float h = tf32_head(v);
-      hi[r * ld + c] = h;
-      lo[r * ld + c] = v - h;
+#pragma unroll
+  for (int p = 0; p < LT_T / 16; ++p) {
+    const int rr = t16 + 16 * p;
+    const int64_t r = r0 + rr, c = c0 + c4;
+    if (r >= d) continue;
+    float h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float v = tile[c4 + e][rr];
+      h[e] = tf32_head(v);
+      l[e] = v - h[e];
+    }
+    if (VEC && c + 4 <= d) {
+      *reinterpret_cast<float4 *>(hi + r * ld + c) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4 *>(lo + r * ld + c) = make_float4(l[0], l[1], l[2], l[3]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c + e < d) {
+          hi[r * ld + c + e] = h[e];
+          lo[r * ld + c + e] = l[e];
+        }
     }
   }
 }
 
 // ---------------------------------------------------------------------------------------
-// Packs the diagonal blocks of U (one CTA per block) for the sweep: upper triangle of
-// U[b0:b0+nb, b0:b0+nb], identity padding to SB x SB, then 1 / U_jj.
+// Packs the diagonal blocks of U for the sweep: upper triangle of U[b0:b0+nb, b0:b0+nb],
+// identity padding to SB x SB (zero columns up to LDU), then 1 / U_jj.  CTA (x, y) writes
+// rows [DB_ROWS y, DB_ROWS (y + 1)) of block x, 4 floats per store; y = 0 also the pivots.
 // ---------------------------------------------------------------------------------------
-__global__ void diag_blocks_kernel(const float *__restrict__ U, int64_t d, int block,
-                                   float *__restrict__ Ud) {
+constexpr int DB_ROWS = 16;
+
+__global__ void __launch_bounds__(256)
+diag_blocks_kernel(const float *__restrict__ U, int64_t d, int block, float *__restrict__ Ud) {
   const int64_t b0 = (int64_t)blockIdx.x * block;
   const int nb = (int)((d - b0) < block ? (d - b0) : block);
   float *out = Ud + (int64_t)blockIdx.x * UD_FLOATS;
-#pragma unroll 8
-  for (int it = 0; it < SB * SB / 256; ++it) {
-    const int e = it * 256 + threadIdx.x;
-    const int i = e / SB, j = e % SB;
-    float v = 0.f;
-    if (i < nb && j < nb) {
-      if (i <= j) v = U[(b0 + i) * d + (b0 + j)];
-    } else if (i == j) {
-      v = 1.f;
+  constexpr int Q = LDU / 4;   // float4 per packed row
+  for (int t = threadIdx.x; t < DB_ROWS * Q; t += 256) {
+    const int i = DB_ROWS * blockIdx.y + t / Q, j4 = 4 * (t % Q);
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j4 + e;
+      if (i < nb && j < nb) v[e] = i <= j ? U[(b0 + i) * d + (b0 + j)] : 0.f;
+      else v[e] = (i == j && j < SB) ? 1.f : 0.f;
     }
-    out[i * LDU + j] = v;
+    *reinterpret_cast<float4 *>(out + i * LDU + j4) = make_float4(v[0], v[1], v[2], v[3]);
   }
-  for (int i = threadIdx.x; i < SB * (LDU - SB); i += 256)
-    out[(i / (LDU - SB)) * LDU + SB + i % (LDU - SB)] = 0.f;
-  for (int j = threadIdx.x; j < SB; j += 256)
-    out[SB * LDU + j] = (j < nb) ? 1.0f / U[(b0 + j) * d + (b0 + j)] : 1.0f;
+  if (blockIdx.y == 0)
+    for (int j = threadIdx.x; j < SB; j += 256)
+      out[SB * LDU + j] = (j < nb) ? 1.0f / U[(b0 + j) * d + (b0 + j)] : 1.0f;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -472,39 +534,112 @@ obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__res
 }
 
 // ---------------------------------------------------------------------------------------
-// Pack codes into the row bitstream; write W_hat = scale * (code - zero).
-// One thread per output word.
+// Pack codes into the row bitstream: the 32 codes of group g fill exactly words
+// [BITS g, BITS (g + 1)) of the row, so one thread packs one group (two 16-byte loads for a
+// whole group: the code rows are 16-byte aligned).  Rows are strided over CTAs.
 // ---------------------------------------------------------------------------------------
-__global__ void pack_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m,
-                            int64_t d, int bits, int64_t words, uint32_t *__restrict__ qp) {
-  const int64_t total = m * words;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = idx / words, wi = idx % words;
-    const int64_t bit0 = wi * 32;
-    const int64_t c0 = bit0 / bits, c1 = (bit0 + 31) / bits;
-    uint32_t v = 0;
-    for (int64_t c = c0; c <= c1 && c < d; ++c) {
-      const uint32_t code = codes[row * ldc + c];
-      const int64_t sh = c * bits - bit0;
-      if (sh >= 0)
-        v |= (sh < 32) ? (code << sh) : 0u;
-      else
-        v |= code >> (-sh);
+template <int BITS>
+__global__ void __launch_bounds__(128)
+pack_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m, int64_t d,
+            int64_t words, uint32_t *__restrict__ qp) {
+  const int64_t ng = (d + 31) / 32;
+  for (int64_t row = blockIdx.x; row < m; row += gridDim.x) {
+    const uint8_t *cr = codes + row * ldc;
+    uint32_t *out = qp + row * words;
+    for (int64_t g = threadIdx.x; g < ng; g += blockDim.x) {
+      uint8_t c[32];
+      if (32 * g + 32 <= d) {
+        const uint4 u0 = *reinterpret_cast<const uint4 *>(cr + 32 * g);
+        const uint4 u1 = *reinterpret_cast<const uint4 *>(cr + 32 * g + 16);
+        memcpy(c, &u0, 16);
+        memcpy(c + 16, &u1, 16);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) c[k] = 32 * g + k < d ? cr[32 * g + k] : 0;
+      }
+      uint64_t acc = 0;
+      int nacc = 0, wo = 0;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        acc |= (uint64_t)c[k] << nacc;
+        nacc += BITS;
+        if (nacc >= 32) {
+          out[BITS * g + wo++] = (uint32_t)acc;
+          acc >>= 32;
+          nacc -= 32;
+        }
+      }
     }
-    qp[idx] = v;
   }
 }
 
-__global__ void dequant_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m,
-                               int64_t d, const float *__restrict__ scale,
-                               const int32_t *__restrict__ zero, float *__restrict__ Wh) {
-  const int64_t total = m * d;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = idx / d, c = idx % d;
-    Wh[idx] = scale[row] * ((float)codes[row * ldc + c] - (float)zero[row]);
+// W_hat = scale * (code - zero), rows strided over CTAs, 4 columns per thread (float4 stores
+// with VEC: d % 4 == 0 and W_hat 16-byte aligned).
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+dequant_kernel(const uint8_t *__restrict__ codes, int64_t ldc, int64_t m, int64_t d,
+               const float *__restrict__ scale, const int32_t *__restrict__ zero,
+               float *__restrict__ Wh) {
+  for (int64_t row = blockIdx.x; row < m; row += gridDim.x) {
+    const float s = scale[row], z = (float)zero[row];
+    const uint8_t *cr = codes + row * ldc;
+    float *wr = Wh + row * d;
+    for (int64_t c = 4 * (int64_t)threadIdx.x; c < d; c += 4 * blockDim.x) {
+      const uchar4 u = *reinterpret_cast<const uchar4 *>(cr + c);   // ldc % 16 == 0
+      const float v[4] = {s * ((float)u.x - z), s * ((float)u.y - z), s * ((float)u.z - z),
+                          s * ((float)u.w - z)};
+      if (VEC) {
+        *reinterpret_cast<float4 *>(wr + c) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c + e < d) wr[c + e] = v[e];
+      }
+    }
   }
+}
+
+// The sweep's views of U: Lt = U^T as head/tail (the trailing updates) and the packed
+// diagonal blocks (the sweep).
+gptq_status launch_lt_split(const float *U, int64_t d, float *hi, float *lo, int64_t ld,
+                            cudaStream_t s) {
+  dim3 tg((unsigned)ceil_div(d, LT_T), (unsigned)ceil_div(d, LT_T));
+  if ((d % 4) == 0) lt_split_kernel<true><<<tg, 256, 0, s>>>(U, d, hi, lo, ld);   // U: 16 B
+  else lt_split_kernel<false><<<tg, 256, 0, s>>>(U, d, hi, lo, ld);
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+gptq_status launch_diag_blocks(const float *U, int64_t d, int block, float *Ud, cudaStream_t s) {
+  diag_blocks_kernel<<<dim3((unsigned)ceil_div(d, block), SB / DB_ROWS), 256, 0, s>>>(U, d, block,
+                                                                                     Ud);
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+gptq_status launch_pack(const uint8_t *codes, int64_t ldc, int64_t m, int64_t d, int bits,
+                        int64_t words, uint32_t *qp, cudaStream_t s) {
+  const unsigned g = (unsigned)std::min<int64_t>(std::max<int64_t>(m, 1), 8192);
+  switch (bits) {
+    case 2: pack_kernel<2><<<g, 128, 0, s>>>(codes, ldc, m, d, words, qp); break;
+    case 3: pack_kernel<3><<<g, 128, 0, s>>>(codes, ldc, m, d, words, qp); break;
+    case 4: pack_kernel<4><<<g, 128, 0, s>>>(codes, ldc, m, d, words, qp); break;
+    case 8: pack_kernel<8><<<g, 128, 0, s>>>(codes, ldc, m, d, words, qp); break;
+    default: return GPTQ_ERR_INVALID_ARG;
+  }
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+gptq_status launch_dequant(const uint8_t *codes, int64_t ldc, int64_t m, int64_t d,
+                           const float *scale, const int32_t *zero, float *Wh, cudaStream_t s) {
+  const unsigned g = (unsigned)std::min<int64_t>(std::max<int64_t>(m, 1), 8192);
+  if ((d % 4) == 0 && ((uintptr_t)Wh % 16) == 0)
+    dequant_kernel<true><<<g, 256, 0, s>>>(codes, ldc, m, d, scale, zero, Wh);
+  else
+    dequant_kernel<false><<<g, 256, 0, s>>>(codes, ldc, m, d, scale, zero, Wh);
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
 }
 
 struct QuantWs {
@@ -563,6 +698,7 @@ struct QuantStreams {
   cudaEvent_t e_ready[2] = {nullptr, nullptr};   // E of a block written (by parity)
   cudaEvent_t far_done[2] = {nullptr, nullptr};  // that block's far update finished
   cudaEvent_t g_in = nullptr, g_out = nullptr;   // joins of a graph replay
+  cudaEvent_t fork = nullptr, ud_done = nullptr, lt_done = nullptr;  // U views beside the grid
   GraphCache graphs;                             // the sweep captured per argument set
 };
 constexpr int kMaxDevices = 128;
@@ -581,7 +717,8 @@ gptq_status quant_streams(QuantStreams **out) {
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.crit, cudaStreamNonBlocking, hi));
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&q.side, cudaStreamNonBlocking, lo));
     cudaEvent_t *evs[] = {&q.start, &q.crit_done, &q.side_done, &q.e_ready[0], &q.e_ready[1],
-                          &q.far_done[0], &q.far_done[1], &q.g_in, &q.g_out};
+                          &q.far_done[0], &q.far_done[1], &q.g_in, &q.g_out, &q.fork,
+                          &q.ud_done, &q.lt_done};
     for (cudaEvent_t *e : evs) GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
   }
   *out = &q;
@@ -593,19 +730,21 @@ gptq_status launch_grid(const void *W, int wdtype, int64_t m, int64_t d, int64_t
                         float *Wf, int64_t ldwf, DevStatus *st, cudaStream_t s) {
   const int warps = 8;
   const unsigned g = (unsigned)ceil_div(m, warps);
+  const int es = wdtype == GPTQ_F32 ? 4 : 2;
+  const int vec = ((uintptr_t)W % 16) == 0 && (ldw * es) % 16 == 0;
   switch (wdtype) {
     case GPTQ_F32:
       grid_kernel<float><<<g, warps * 32, 0, s>>>((const float *)W, m, d, ldw, dead_mask, maxq,
-                                                  scale, zero, Wf, ldwf, st);
+                                                  scale, zero, Wf, ldwf, vec, st);
       break;
     case GPTQ_F16:
       grid_kernel<__half><<<g, warps * 32, 0, s>>>((const __half *)W, m, d, ldw, dead_mask,
-                                                   maxq, scale, zero, Wf, ldwf, st);
+                                                   maxq, scale, zero, Wf, ldwf, vec, st);
       break;
     case GPTQ_BF16:
       grid_kernel<__nv_bfloat16><<<g, warps * 32, 0, s>>>((const __nv_bfloat16 *)W, m, d, ldw,
                                                           dead_mask, maxq, scale, zero, Wf, ldwf,
-                                                          st);
+                                                          vec, st);
       break;
     default:
       return GPTQ_ERR_INVALID_ARG;
@@ -650,6 +789,16 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
   }
   const float maxq = (float)((1 << bits) - 1);
   GPTQ_CUDA_CHECK(cudaMemsetAsync(q.st, 0, sizeof(DevStatus), s));
+  // blocked with the side stream: the U views (which need only U) beside the grid pass
+  const bool overlap = qs != nullptr && block > 1;
+  if (overlap) {
+    GPTQ_CUDA_CHECK(cudaEventRecord(qs->fork, s));
+    GPTQ_CUDA_CHECK(cudaStreamWaitEvent(qs->side, qs->fork, 0));
+    GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, qs->side));
+    GPTQ_CUDA_CHECK(cudaEventRecord(qs->ud_done, qs->side));
+    GPTQ_TRY(launch_lt_split(U, d, q.Lhi, q.Llo, q.ldl, qs->side));
+    GPTQ_CUDA_CHECK(cudaEventRecord(qs->lt_done, qs->side));
+  }
   for (int64_t i = 0, off = 0; i < n; off += L[i].m, ++i)
     GPTQ_TRY(launch_grid(L[i].W, L[i].wdtype, L[i].m, d, L[i].ldw, dead_mask, maxq,
                          scale + off, zero + off, q.Wf + off * q.ldwf, q.ldwf, q.st, s));
@@ -665,12 +814,9 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
     }
   } else {
     // blocked: in-block sweep, then one rank-B trailing update per block
-    {
-      dim3 tg((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32));
-      lt_split_kernel<<<tg, dim3(32, 8), 0, s>>>(U, d, q.Lhi, q.Llo, q.ldl);
-      GPTQ_LAUNCH_CHECK();
-      diag_blocks_kernel<<<(unsigned)ceil_div(d, block), 256, 0, s>>>(U, d, block, q.Ud);
-      GPTQ_LAUNCH_CHECK();
+    if (!overlap) {
+      GPTQ_TRY(launch_lt_split(U, d, q.Lhi, q.Llo, q.ldl, s));
+      GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, s));
     }
     const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
     // W[:, c0:c1] -= E U[b0:b1, c0:c1] with E from buffer pair e
@@ -684,7 +830,6 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
       return launch_gemm_nt(g, q.st, st);
     };
-    const bool overlap = qs != nullptr;
     if (!overlap) {
       for (int64_t b0 = 0; b0 < d; b0 += block) {
         const int nb = (int)((d - b0) < block ? (d - b0) : block);
@@ -711,6 +856,8 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->start, s));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->start, 0));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->start, 0));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->ud_done, 0));   // the first sweep
+      bool lt_waited = false;                                     // the first near update
       int k = 0;
       for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
         const int e = k & 1;
@@ -730,6 +877,8 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
         // near part: the next block's columns, after the previous block's far update
         if (b1 < d) {
           if (k > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
+          if (!lt_waited) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->lt_done, 0));
+          lt_waited = true;
           GPTQ_TRY(update(e, b0, nb, b1, f0, 0, c));
         }
       }
@@ -742,13 +891,9 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
   const int64_t words = ceil_div(d, 32) * bits;
   for (int64_t i = 0, off = 0; i < n; off += L[i].m, ++i) {
     const uint8_t *codes = q.codes + off * q.ldc;
-    pack_kernel<<<2048, 256, 0, s>>>(codes, q.ldc, L[i].m, d, bits, words, L[i].qpacked);
-    GPTQ_LAUNCH_CHECK();
-    if (L[i].W_hat) {
-      dequant_kernel<<<2048, 256, 0, s>>>(codes, q.ldc, L[i].m, d, scale + off, zero + off,
-                                          L[i].W_hat);
-      GPTQ_LAUNCH_CHECK();
-    }
+    GPTQ_TRY(launch_pack(codes, q.ldc, L[i].m, d, bits, words, L[i].qpacked, s));
+    if (L[i].W_hat)
+      GPTQ_TRY(launch_dequant(codes, q.ldc, L[i].m, d, scale + off, zero + off, L[i].W_hat, s));
     if (n > 1) {
       GPTQ_CUDA_CHECK(cudaMemcpyAsync(L[i].scale, scale + off, L[i].m * 4,
                                       cudaMemcpyDeviceToDevice, s));
@@ -829,12 +974,8 @@ gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d,
       Wf, ldwf, (int)d, Hinv, scale, zero, maxq, codes, ldc, order);
   GPTQ_LAUNCH_CHECK();
   const int64_t words = ceil_div(d, 32) * bits;
-  pack_kernel<<<2048, 256, 0, s>>>(codes, ldc, m, d, bits, words, qpacked);
-  GPTQ_LAUNCH_CHECK();
-  if (W_hat) {
-    dequant_kernel<<<2048, 256, 0, s>>>(codes, ldc, m, d, scale, zero, W_hat);
-    GPTQ_LAUNCH_CHECK();
-  }
+  GPTQ_TRY(launch_pack(codes, ldc, m, d, bits, words, qpacked, s));
+  if (W_hat) GPTQ_TRY(launch_dequant(codes, ldc, m, d, scale, zero, W_hat, s));
   return GPTQ_OK;
 }
 
