@@ -164,13 +164,21 @@ reverse_lower_kernel(float *H, int64_t d, float *Yt, DevStatus *st) {
 // bank groups).  The leaf runs one sub-panel ahead: after phase 1 of sub-panel p, warp 0
 // applies phase 2 to the next leaf's tile alone and factors it, while the other fifteen
 // warps run the rest of phase 2 and write the next identity rows of Bt (untouched until
-// then), so one barrier per sub-panel orders both.  The rows of Linv that phase 1 finishes
-// are stored before the split.  A non-positive pivot records NOT_PD with its global index.
+// then), so one barrier per sub-panel orders both; the warps that share warp 0's scheduler
+// (4, 8, 12) stay out of phase 2 so that the leaf's serial chain is not slowed.  The rows
+// of Linv that phase 1 finishes are stored before the split.  A non-positive pivot records
+// NOT_PD with its global index.
 // ---------------------------------------------------------------------------------------
 constexpr int PF_THREADS = 512;
 constexpr int PF_WARPS = PF_THREADS / 32;
 constexpr int PW = 16;             // sub-panel width
 constexpr int PL = NB + 4;         // smem leading dimension (16-byte rows)
+// Shared memory the kernel uses, and what it requests: enough that no other kernel's CTA
+// (the row-panel products of the concurrent streams need 34 KB or more) fits on its SM, so
+// that no foreign warps compete with the leaf's serial chain for issue slots.
+constexpr size_t kPotrfSmemUsed = (2 * NB * PL + PW * PL + PW) * sizeof(float);
+constexpr size_t kPotrfSmem = 200 * 1024;
+static_assert(kPotrfSmemUsed <= kPotrfSmem, "potrf shared memory");
 
 // Column J of the leaf, rl = 1/sqrt(pivot J) already known.  Lane i holds row i of the
 // tile in a[] and its running diagonal in dg.  The updates run on every lane and every
@@ -371,6 +379,15 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
                       r == c4 + 3 ? 1.f : 0.f);
     }
   };
+  // the same rows written by warps 4, 8 and 12 alone (96 threads)
+  auto identity_rows4 = [&](int R0) {
+    for (int e = 32 * (warp / 4 - 1) + lane; e < PW * NB / 4; e += 96) {
+      const int r = R0 + e / (NB / 4), c4 = 4 * (e % (NB / 4));
+      *reinterpret_cast<float4 *>(Bt + r * PL + c4) =
+          make_float4(r == c4 ? 1.f : 0.f, r == c4 + 1 ? 1.f : 0.f, r == c4 + 2 ? 1.f : 0.f,
+                      r == c4 + 3 ? 1.f : 0.f);
+    }
+  };
   // warp 0 loads the first leaf's PW x PW tile and factors it at once; the other warps load
   // the rest of the block and the first identity rows meanwhile
   if (warp == 0) {
@@ -424,12 +441,17 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
       __syncwarp();
       const int bad = leaf_factor(S, M, rd, cb, R0, lane);
       if (lane == 0 && bad >= 0 && s_bad < 0) s_bad = bad;
+    } else if (warp % 4 == 0) {
+      // warps 4, 8, 12 share warp 0's scheduler: they take only the next identity rows
+      identity_rows4(R0);
     } else {
       // phase 2 over 8-row tiles of [Bt rows < R0 ; S rows >= R0] x 64-column tiles from R0,
-      // without S rows R0..R0+PW-1 (their lower part is the next leaf's tile)
+      // without S rows R0..R0+PW-1 (their lower part is the next leaf's tile), on the twelve
+      // warps of the other three schedulers
       const int nct = (NB - R0 + 63) / 64;
+      const int wi = 3 * (warp / 4) + warp % 4 - 1;
 #pragma unroll 1
-      for (int t = warp - 1; t < (NB / 8) * nct; t += PF_WARPS - 1) {
+      for (int t = wi; t < (NB / 8) * nct; t += PF_WARPS - PF_WARPS / 4) {
         const int m0 = 8 * (t / nct), n0 = R0 + 64 * (t % nct);
         if (m0 < R0) {
           update_tile(Bt, Bt + P0, S + P0, m0, n0, lane, false);
@@ -437,7 +459,6 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
           update_tile(S, S + P0, S + P0, m0, n0, lane, true);
         }
       }
-      identity_rows(R0);
     }
     __syncthreads();
   }
@@ -721,7 +742,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
                             void *ws, cudaStream_t s, SideStream *ss) {
   const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);       // whole rows
   const size_t rmq_smem = (32 + RM_ROWS) * RML * sizeof(float);       // one column quarter
-  const size_t potrf_smem = (2 * NB * PL + PW * PL + PW) * sizeof(float);
+  const size_t potrf_smem = kPotrfSmem;
   PrepWs w = carve_prepare(ws, d);
   const bool overlap = ss != nullptr;
   cudaStream_t b = overlap ? ss->s : s;
@@ -859,7 +880,7 @@ gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *d
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((2 * NB * PL + PW * PL + PW) * sizeof(float))));
+                                         (int)kPotrfSmem));
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel<4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)((NB + RM_ROWS) * RML * sizeof(float))));
