@@ -41,6 +41,8 @@ __global__ void dead_damp_kernel(float *H, int64_t d, float damp, uint8_t *dead_
   __syncthreads();
   double sum = 0.0;
   int ndead = 0, bad = 0;
+  // the diagonal entries lie in distinct lines: four loads in flight per thread and round trip
+#pragma unroll 4
   for (int64_t i = threadIdx.x; i < d; i += blockDim.x) {
     const float h = H[i * d + i];
     if (!isfinite(h)) bad = 1;
@@ -69,16 +71,28 @@ __global__ void dead_damp_kernel(float *H, int64_t d, float damp, uint8_t *dead_
     st->diag_sum = diag_sum;
     if (s_bad) set_status(st, GPTQ_ERR_NONFINITE);
   }
-  for (int64_t i = threadIdx.x; i < (d + 1) / 2; i += blockDim.x) {
-    const int64_t j = d - 1 - i;
-    const float hi = H[i * d + i], hj = H[j * d + j];
-    const bool di = hi == 0.0f, dj = hj == 0.0f;
+  // pairs (i, d-1-i), two per thread and round trip (all four loads before the stores)
+  const int64_t half = (d + 1) / 2;
+  for (int64_t i0 = threadIdx.x; i0 < half; i0 += 2 * (int64_t)blockDim.x) {
+    const int64_t i1 = i0 + blockDim.x;
+    const bool two = i1 < half;
+    const int64_t j0 = d - 1 - i0, j1 = d - 1 - i1;
+    const float h0 = H[i0 * d + i0], g0 = H[j0 * d + j0];
+    const float h1 = two ? H[i1 * d + i1] : 0.0f, g1 = two ? H[j1 * d + j1] : 0.0f;
     if (dead_mask) {
-      dead_mask[i] = di ? 1 : 0;
-      dead_mask[j] = dj ? 1 : 0;
+      dead_mask[i0] = h0 == 0.0f;
+      dead_mask[j0] = g0 == 0.0f;
+      if (two) {
+        dead_mask[i1] = h1 == 0.0f;
+        dead_mask[j1] = g1 == 0.0f;
+      }
     }
-    H[i * d + i] = (dj ? 1.0f : hj) + lam;
-    H[j * d + j] = (di ? 1.0f : hi) + lam;
+    H[i0 * d + i0] = (g0 == 0.0f ? 1.0f : g0) + lam;
+    H[j0 * d + j0] = (h0 == 0.0f ? 1.0f : h0) + lam;
+    if (two) {
+      H[i1 * d + i1] = (g1 == 0.0f ? 1.0f : g1) + lam;
+      H[j1 * d + j1] = (h1 == 0.0f ? 1.0f : h1) + lam;
+    }
   }
 }
 
