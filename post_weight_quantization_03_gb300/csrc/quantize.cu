@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(SW_THREADS)
 sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, int nb,
              const float *__restrict__ Ud, const float *__restrict__ scale,
              const int32_t *__restrict__ zero, float maxq, float *__restrict__ Ehi,
-             float *__restrict__ Elo, uint8_t *__restrict__ codes, int64_t ldc,
+             float *__restrict__ Elo, int64_t lde, uint8_t *__restrict__ codes, int64_t ldc,
              DevStatus *st) {
   extern __shared__ __align__(16) float sm[];
   float *Us = sm;                        // SB x LDU, then SB reciprocals
@@ -354,21 +354,33 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
     }
   }
   __syncthreads();
-  // E (now in the stage rows) -> global as a TF32 head/tail pair, coalesced
+  // E (now in the stage rows) -> global as a TF32 head/tail pair, coalesced: its nb columns
+  // (float4 stores when E's rows start on 16-byte boundaries, single floats otherwise)
+  if (((uintptr_t)Ehi % 16) != 0 || ((uintptr_t)Elo % 16) != 0 || (lde % 4) != 0) {
+    for (int e = tid; e < SW_ROWS * SB; e += SW_THREADS) {
+      const int r = e / SB, j = e % SB;
+      const int64_t gr = r0 + r;
+      if (gr < m && j < nb) {
+        const float v = stage[r * LDW + j], h = tf32_head(v);
+        Ehi[gr * lde + j] = h;
+        Elo[gr * lde + j] = v - h;
+      }
+    }
+  } else
 #pragma unroll 4
   for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
     const int e = it * SW_THREADS + tid;
     const int r = e / (SB / 4), q = e % (SB / 4);
     const int64_t gr = r0 + r;
-    if (gr < m) {
+    if (gr < m && 4 * q < nb) {
       float4 v = *reinterpret_cast<const float4 *>(stage + r * LDW + 4 * q);
       if (4 * q + 0 >= nb) v.x = 0.f;
       if (4 * q + 1 >= nb) v.y = 0.f;
       if (4 * q + 2 >= nb) v.z = 0.f;
       if (4 * q + 3 >= nb) v.w = 0.f;
       const float4 h = make_float4(tf32_head(v.x), tf32_head(v.y), tf32_head(v.z), tf32_head(v.w));
-      *reinterpret_cast<float4 *>(Ehi + gr * SB + 4 * q) = h;
-      *reinterpret_cast<float4 *>(Elo + gr * SB + 4 * q) =
+      *reinterpret_cast<float4 *>(Ehi + gr * lde + 4 * q) = h;
+      *reinterpret_cast<float4 *>(Elo + gr * lde + 4 * q) =
           make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
     }
   }
@@ -649,7 +661,8 @@ struct QuantWs {
   float *Lhi, *Llo; int64_t ldl;
   uint8_t *codes; int64_t ldc;
   float *Ud;
-  float *Ehi2, *Elo2;   // second E pair (blocks of odd index when the far update overlaps)
+  float *Ehi2, *Elo2;   // second E pair buffer
+  int64_t lde;          // E row stride: two blocks side by side (a pair of blocks)
 };
 
 QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
@@ -658,8 +671,9 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   q.st = (DevStatus *)p; p += 256;
   q.ldwf = (int64_t)round_up((size_t)d, 4);
   q.Wf = (float *)p; p += round_up((size_t)m * q.ldwf * 4, 256);
-  q.Ehi = (float *)p; p += round_up((size_t)m * SB * 4, 256);
-  q.Elo = (float *)p; p += round_up((size_t)m * SB * 4, 256);
+  q.lde = block > 1 ? 2 * SB : SB;
+  q.Ehi = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
+  q.Elo = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
   q.ldl = (int64_t)round_up((size_t)d, 4);
   q.Lhi = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
   q.Llo = (float *)p; p += round_up((size_t)d * q.ldl * 4, 256);
@@ -668,7 +682,7 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   q.Ud = (float *)p;
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
   p += block > 1 ? nblk * UD_FLOATS * 4 : 0;
-  q.Ehi2 = (float *)p; p += round_up((size_t)m * SB * 4, 256);
+  q.Ehi2 = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
   q.Elo2 = (float *)p;
   return q;
 }
@@ -680,9 +694,10 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
   const size_t ldwf = round_up((size_t)d, 4), ldl = round_up((size_t)d, 4);
   const size_t ldc = round_up((size_t)d, 16);
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
-  return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * SB * 4, 256) +
+  const size_t lde = block > 1 ? 2 * SB : SB;
+  return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * lde * 4, 256) +
          2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
-         (block > 1 ? nblk * UD_FLOATS * 4 + 2 * round_up((size_t)m * SB * 4, 256)
+         (block > 1 ? nblk * UD_FLOATS * 4 + 2 * round_up((size_t)m * lde * 4, 256)
                     : 0);   // B = 1 needs neither packed diagonal blocks nor a second E pair
 }
 
@@ -819,33 +834,49 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, s));
     }
     const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
-    // W[:, c0:c1] -= E U[b0:b1, c0:c1] with E from buffer pair e
-    auto update = [&](int e, int64_t b0, int nb, int64_t c0, int64_t c1, int max_ctas,
+    // Blocks are taken in pairs (2p, 2p + 1) for the trailing update: the E of both blocks
+    // of pair p sit side by side in buffer p % 2 (block 2p + h at column h * block), so one
+    // product of depth up to 2B applies the pair to every column past it.  Block 2p's own
+    // update reaches only the next block (2p + 1), which is swept before the pair's product.
+    // Every column thus receives the contributions of earlier blocks in the same order and
+    // grouping in both schedules below (the results are bit for bit the same).
+    // W[:, c0:c1] -= E U[kb0:kb0+K, c0:c1] with E the first K columns of pair buffer e
+    auto update = [&](int e, int64_t kb0, int K, int64_t c0, int64_t c1, int max_ctas,
                       cudaStream_t st) -> gptq_status {
       GemmArgs g{};
-      g.a_hi = e ? q.Ehi2 : q.Ehi; g.a_lo = e ? q.Elo2 : q.Elo; g.lda = SB;
-      g.b_hi = q.Lhi + c0 * q.ldl + b0; g.b_lo = q.Llo + c0 * q.ldl + b0; g.ldb = q.ldl;
+      g.a_hi = e ? q.Ehi2 : q.Ehi; g.a_lo = e ? q.Elo2 : q.Elo; g.lda = q.lde;
+      g.b_hi = q.Lhi + c0 * q.ldl + kb0; g.b_lo = q.Llo + c0 * q.ldl + kb0; g.ldb = q.ldl;
       g.c = q.Wf + c0; g.ldc = q.ldwf;
-      g.M = m; g.N = c1 - c0; g.K = nb;
+      g.M = m; g.N = c1 - c0; g.K = K;
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
       return launch_gemm_nt(g, q.st, st);
     };
+    auto sweep = [&](int64_t b0, int nb, int e, int h, cudaStream_t st) -> gptq_status {
+      sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, st>>>(
+          q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq,
+          (e ? q.Ehi2 : q.Ehi) + h * block, (e ? q.Elo2 : q.Elo) + h * block, q.lde, q.codes,
+          q.ldc, q.st);
+      GPTQ_LAUNCH_CHECK();
+      return GPTQ_OK;
+    };
     if (!overlap) {
-      for (int64_t b0 = 0; b0 < d; b0 += block) {
+      int k = 0;
+      for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
+        const int e = (k >> 1) & 1, h = k & 1;
         const int nb = (int)((d - b0) < block ? (d - b0) : block);
         const int64_t b1 = b0 + nb;
-        sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, s>>>(
-            q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq, q.Ehi,
-            q.Elo, q.codes, q.ldc, q.st);
-        GPTQ_LAUNCH_CHECK();
-        if (b1 < d) GPTQ_TRY(update(0, b0, nb, b1, d, 0, s));
+        GPTQ_TRY(sweep(b0, nb, e, h, s));
+        if (b1 < d) {
+          if (h == 0) GPTQ_TRY(update(e, b0, nb, b1, std::min<int64_t>(b1 + block, d), 0, s));
+          else GPTQ_TRY(update(e, b0 - block, block + nb, b1, d, 0, s));
+        }
       }
     } else {
-      // Block b's trailing update is split at b1 + B: the next block's columns on the
-      // critical stream right after the sweep, the far columns on the side stream beside
-      // the next sweep.  The next-block update of block b + 1 waits for block b's far
-      // update, so every column receives its blocks' contributions in block order, exactly
-      // as in the single-stream order above (the results are bit for bit the same).
+      // After pair p its product splits two blocks on: those two blocks' columns on the
+      // critical stream right after the sweep, the far columns on the side stream, where they
+      // have two sweeps and two near updates' time before the sweep that needs them.  Pair
+      // p's near update waits for pair p - 1's far update, which keeps each column's
+      // contributions in the single-stream order and frees the pair buffer pair p + 1 reuses.
       cudaStream_t c = qs->crit, sd = qs->side;
       int nsm = 0, dev = 0;
       GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
@@ -857,29 +888,27 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->start, 0));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->start, 0));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->ud_done, 0));   // the first sweep
-      bool lt_waited = false;                                     // the first near update
+      bool lt_waited = false;                                     // the first update on c
       int k = 0;
       for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
-        const int e = k & 1;
+        const int p = k >> 1, e = p & 1, h = k & 1;
         const int nb = (int)((d - b0) < block ? (d - b0) : block);
         const int64_t b1 = b0 + nb;
-        const int64_t f0 = b1 + block < d ? b1 + block : d;   // far columns [f0, d)
-        sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, c>>>(
-            q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq,
-            e ? q.Ehi2 : q.Ehi, e ? q.Elo2 : q.Elo, q.codes, q.ldc, q.st);
-        GPTQ_LAUNCH_CHECK();
-        GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
-        // far part of this block (E stays untouched until the sweep two blocks on, which
-        // follows the next block's near update, which waits for this far update)
-        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
-        if (f0 < d) GPTQ_TRY(update(e, b0, nb, f0, d, far_ctas, sd));
-        GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
-        // near part: the next block's columns, after the previous block's far update
-        if (b1 < d) {
-          if (k > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
-          if (!lt_waited) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->lt_done, 0));
-          lt_waited = true;
-          GPTQ_TRY(update(e, b0, nb, b1, f0, 0, c));
+        GPTQ_TRY(sweep(b0, nb, e, h, c));
+        if (b1 >= d) break;
+        if (!lt_waited) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->lt_done, 0));
+        lt_waited = true;
+        if (h == 0) {
+          // block 2p -> block 2p + 1
+          GPTQ_TRY(update(e, b0, nb, b1, std::min<int64_t>(b1 + block, d), 0, c));
+        } else {
+          const int64_t f0 = std::min<int64_t>(b1 + 2 * block, d);   // far columns [f0, d)
+          GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
+          if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
+          GPTQ_TRY(update(e, b0 - block, block + nb, b1, f0, 0, c));   // the next two blocks
+          GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
+          if (f0 < d) GPTQ_TRY(update(e, b0 - block, block + nb, f0, d, far_ctas, sd));
+          GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
         }
       }
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->crit_done, c));
