@@ -496,26 +496,31 @@ constexpr int RML = NB + 4;  // smem leading dimension: float4 rows of 8 consecu
                              // threads fall in distinct bank groups
 
 // Thread (rg, cg) computes rows 4rg..4rg+3 x columns 32(q0 + q) + cg (q < NCQ): per 4-wide
-// K step, 4 broadcast + NCQ float4 shared loads feed 8 NCQ paired FMAs.
-template <int NCQ>
+// K step, 4 broadcast + NCQ float4 shared loads feed 8 NCQ paired FMAs.  With KS > 1 the CTA
+// takes only K chunk blockIdx.z of NB / KS (a quarter of the loads and of the dependent
+// product); its partial sums are subtracted by atomic adds, so KS > 1 needs sub and no
+// head/tail output.
+template <int NCQ, int KS = 1>
 __global__ void __launch_bounds__(RM_THREADS)
 rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int64_t ldo,
               int64_t r0, int64_t r1, const float *Bm, const float *Bm_lo, int64_t ldb, int n,
               int nj, int sub, float *hi, float *lo, const DevStatus *st) {
+  constexpr int KC = NB / KS, LD = KC + 4;   // K chunk and its shared row stride
   extern __shared__ __align__(16) float sm[];
-  float *Bs = sm;                    // 32 NCQ x RML: the CTA's Bm rows (output columns, K)
-  float *Is = sm + 32 * NCQ * RML;   // RM_ROWS x RML: the CTA's input rows
+  float *Bs = sm;                    // 32 NCQ x LD: the CTA's Bm rows (output columns, K)
+  float *Is = sm + 32 * NCQ * LD;    // RM_ROWS x LD: the CTA's input rows
   if (st->status != 0) return;
+  const int kz = KS > 1 ? KC * (int)blockIdx.z : 0;   // first K of the chunk
   const int tid = threadIdx.x;
   const int64_t rb = r0 + (int64_t)blockIdx.x * RM_ROWS;
   const int q0 = blockIdx.y * NCQ;
   // every global load of the CTA is issued before the first shared store (one round trip)
-  constexpr int NBI = 32 * NCQ * NB / 4 / RM_THREADS, NII = RM_ROWS * NB / 4 / RM_THREADS;
+  constexpr int NBI = 32 * NCQ * KC / 4 / RM_THREADS, NII = RM_ROWS * KC / 4 / RM_THREADS;
   float4 bv[NBI], iv[NII];
 #pragma unroll
   for (int it = 0; it < NBI; ++it) {
     const int e = it * RM_THREADS + tid;  // float4 index within the CTA's Bm rows
-    const int j = e / (NB / 4), t4 = 4 * (e % (NB / 4));
+    const int j = e / (KC / 4), t4 = kz + 4 * (e % (KC / 4));
     const int64_t bo = (int64_t)(32 * q0 + j) * ldb + t4;
     bv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (32 * q0 + j < nj) {
@@ -530,7 +535,7 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
 #pragma unroll
   for (int it = 0; it < NII; ++it) {
     const int e = it * RM_THREADS + tid;
-    const int r = e / (NB / 4), t4 = 4 * (e % (NB / 4));
+    const int r = e / (KC / 4), t4 = kz + 4 * (e % (KC / 4));
     const int64_t gr = rb + r;
     iv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (gr < r1) {
@@ -550,12 +555,12 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
 #pragma unroll
   for (int it = 0; it < NBI; ++it) {
     const int e = it * RM_THREADS + tid;
-    *reinterpret_cast<float4 *>(Bs + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = bv[it];
+    *reinterpret_cast<float4 *>(Bs + (e / (KC / 4)) * LD + 4 * (e % (KC / 4))) = bv[it];
   }
 #pragma unroll
   for (int it = 0; it < NII; ++it) {
     const int e = it * RM_THREADS + tid;
-    *reinterpret_cast<float4 *>(Is + (e / (NB / 4)) * RML + 4 * (e % (NB / 4))) = iv[it];
+    *reinterpret_cast<float4 *>(Is + (e / (KC / 4)) * LD + 4 * (e % (KC / 4))) = iv[it];
   }
   __syncthreads();
   const int rg = tid / 32, cg = tid % 32;
@@ -565,12 +570,12 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
 #pragma unroll
     for (int q = 0; q < NCQ; ++q) acc[i][q] = make_float2(0.f, 0.f);
 #pragma unroll 2
-  for (int t = 0; t < NB; t += 4) {
+  for (int t = 0; t < KC; t += 4) {
     float4 a[4], b[NCQ];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Is + (4 * rg + i) * RML + t);
+    for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4 *>(Is + (4 * rg + i) * LD + t);
 #pragma unroll
-    for (int q = 0; q < NCQ; ++q) b[q] = *reinterpret_cast<const float4 *>(Bs + (32 * q + cg) * RML + t);
+    for (int q = 0; q < NCQ; ++q) b[q] = *reinterpret_cast<const float4 *>(Bs + (32 * q + cg) * LD + t);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -756,6 +761,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
                             void *ws, cudaStream_t s, SideStream *ss) {
   const size_t rm_smem = (NB + RM_ROWS) * RML * sizeof(float);       // whole rows
   const size_t rmq_smem = (32 + RM_ROWS) * RML * sizeof(float);       // one column quarter
+  const size_t rmk_smem = (32 + RM_ROWS) * (NB / 4 + 4) * sizeof(float);   // and a K quarter
   const size_t potrf_smem = kPotrfSmem;
   PrepWs w = carve_prepare(ws, d);
   const bool overlap = ss != nullptr;
@@ -823,8 +829,14 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
         GPTQ_LAUNCH_CHECK();
         GPTQ_CUDA_CHECK(cudaEventRecord(ss->en[par], c2));
         next_rest = true;
-        next_col(0, nn, c);                       // the next potrf's block
-        GPTQ_LAUNCH_CHECK();
+        {
+          // the next potrf's block, in four K chunks (64 CTAs; atomic adds)
+          dim3 g2((unsigned)ceil_div(nn, RM_ROWS), (unsigned)ceil_div(nn, 32), 4);
+          rowmul_kernel<1, 4><<<g2, RM_THREADS, rmk_smem, c>>>(
+              w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, 0, nn,
+              w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
+          GPTQ_LAUNCH_CHECK();
+        }
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ed[par], 0));
       } else {
