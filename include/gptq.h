@@ -52,7 +52,7 @@ typedef enum gptq_status {
   GPTQ_ERR_NONFINITE = 3,    /* NaN/Inf found in an input                                 */
   GPTQ_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up                        */
   GPTQ_ERR_CUDA = 5,         /* a CUDA runtime call or kernel launch failed               */
-  GPTQ_ERR_UNSUPPORTED = 6,  /* valid request this build does not implement               */
+  GPTQ_ERR_UNSUPPORTED = 6,  /* valid request this library does not implement             */
   GPTQ_ERR_WORKSPACE = 7     /* workspace missing, too small or not 256-byte aligned      */
 } gptq_status;
 
