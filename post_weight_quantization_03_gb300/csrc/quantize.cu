@@ -538,8 +538,24 @@ obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__res
     if (free) {
       w = fmaf(-s_e, Hs[j * L + q], w);
       const float f = __fdiv_rn(Hs[q * L + j], Hs[q * L + q]);
-      for (int i = 0; i < d; ++i)
-        if (s_free[i]) Hs[i * L + j] = fmaf(-Hs[i * L + q], f, Hs[i * L + j]);
+      // column q is not written in this step (its thread has left the free set), so each
+      // batch of eight rows is read before any of it is written: one shared-memory round
+      // trip per batch instead of one per row
+#pragma unroll 1
+      for (int i0 = 0; i0 < d; i0 += 8) {
+        float hq[8], hj[8];
+        bool fr[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u;
+          fr[u] = i < d && s_free[i];
+          hq[u] = i < d ? Hs[i * L + q] : 0.f;
+          hj[u] = i < d ? Hs[i * L + j] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (fr[u]) Hs[(i0 + u) * L + j] = fmaf(-hq[u], f, hj[u]);
+      }
     }
     __syncthreads();
   }
