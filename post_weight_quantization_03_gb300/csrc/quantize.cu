@@ -485,18 +485,29 @@ __global__ void __launch_bounds__(OBQ_MAX_D)
 obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__restrict__ Hinv,
            const float *__restrict__ scale, const int32_t *__restrict__ zero, float maxq,
            uint8_t *__restrict__ codes, int64_t ldc, int32_t *__restrict__ order) {
-  extern __shared__ float Hs[];  // d x (d + 1)
+  // R = the transpose of H_F^-1 as downdated column by column: thread j owns row j of R, so
+  // its update is a float4 sweep along its own row against row q (a broadcast).  R starts
+  // as H^-1 itself (bitwise symmetric), and each step computes exactly the transpose of the
+  // column-wise downdate H_ij -= H_iq (H_qj / H_qq):  R_ji -= R_qi (R_jq / R_qq).
+  extern __shared__ __align__(16) float Rs[];  // d x LH
   __shared__ float s_val[OBQ_MAX_D / 32];
   __shared__ int s_idx[OBQ_MAX_D / 32];
   __shared__ float s_e;
-  __shared__ uint8_t s_free[OBQ_MAX_D];
   const int j = threadIdx.x, lane = j % 32, wid = j / 32;
   const int64_t row = blockIdx.x;
-  const int L = d + 1;
-  for (int e = j; e < d * d; e += OBQ_MAX_D) Hs[(e / d) * L + e % d] = Hinv[e];
+  const int LH = ((d + 3) / 4) * 4 + 4;
+  for (int e = j; e < d * LH; e += OBQ_MAX_D) {
+    const int i = e / LH, c = e % LH;
+    Rs[e] = c < d ? Hinv[i * d + c] : 0.f;
+  }
   bool free = j < d;
+  uint32_t fm[OBQ_MAX_D / 32];   // free columns, the same in every thread
+#pragma unroll
+  for (int k = 0; k < OBQ_MAX_D / 32; ++k) {
+    const int lo = 32 * k;
+    fm[k] = d >= lo + 32 ? 0xffffffffu : (d > lo ? (1u << (d - lo)) - 1u : 0u);
+  }
   float w = free ? Wf[row * ldwf + j] : 0.f;
-  if (free) s_free[j] = 1;
   const float sc_row = scale[row], z = (float)zero[row];
   __syncthreads();
 #pragma unroll 1
@@ -506,7 +517,7 @@ obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__res
       cd = fminf(fmaxf(rintf(__fdiv_rn(w, sc_row)) + z, 0.f), maxq);
       qv = sc_row * (cd - z);
       const float er = w - qv;
-      const float cost = __fdiv_rn(er * er, Hs[j * L + j]);
+      const float cost = __fdiv_rn(er * er, Rs[j * LH + j]);
       key = (cost >= 0.f && cost <= FLT_MAX) ? cost : FLT_MAX;  // NaN/inf: last among free
     }
     int idx = free ? j : OBQ_MAX_D;
@@ -526,35 +537,45 @@ obq_kernel(const float *__restrict__ Wf, int64_t ldwf, int d, const float *__res
     // a free column always exists while step < d, so q < d; the clamp only keeps every
     // index inside the tile should that ever fail
     q = q < d ? q : d - 1;
+    fm[q / 32] &= ~(1u << (q % 32));
     if (j == q) {
       codes[row * ldc + q] = (uint8_t)cd;
       if (order) order[row * d + step] = q;
-      s_e = __fdiv_rn(w - qv, Hs[q * L + q]);
-      s_free[q] = 0;
+      s_e = __fdiv_rn(w - qv, Rs[q * LH + q]);
       w = qv;
       free = false;
     }
     __syncthreads();
     if (free) {
-      w = fmaf(-s_e, Hs[j * L + q], w);
-      const float f = __fdiv_rn(Hs[q * L + j], Hs[q * L + q]);
-      // column q is not written in this step (its thread has left the free set), so each
-      // batch of eight rows is read before any of it is written: one shared-memory round
-      // trip per batch instead of one per row
+      w = fmaf(-s_e, Rs[q * LH + j], w);                 // H_jq = R_qj
+      const float f = __fdiv_rn(Rs[j * LH + q], Rs[q * LH + q]);   // H_qj / H_qq
+      // row q is not written in this step (its thread has left the free set): each batch of
+      // sixteen columns is read before any of it is written
+      float *rj = Rs + j * LH;
+      const float *rq = Rs + q * LH;
 #pragma unroll 1
-      for (int i0 = 0; i0 < d; i0 += 8) {
-        float hq[8], hj[8];
-        bool fr[8];
+      for (int i0 = 0; i0 < d; i0 += 16) {
+        float4 hq[4], hj[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u;
-          fr[u] = i < d && s_free[i];
-          hq[u] = i < d ? Hs[i * L + q] : 0.f;
-          hj[u] = i < d ? Hs[i * L + j] : 0.f;
+        for (int u = 0; u < 4; ++u) {
+          if (i0 + 4 * u < d) {
+            hq[u] = *reinterpret_cast<const float4 *>(rq + i0 + 4 * u);
+            hj[u] = *reinterpret_cast<const float4 *>(rj + i0 + 4 * u);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (fr[u]) Hs[(i0 + u) * L + j] = fmaf(-hq[u], f, hj[u]);
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + 4 * u;
+          if (i < d) {
+            const uint32_t bits = (fm[i / 32] >> (i % 32)) & 0xfu;   // i % 4 == 0: one word
+            float4 v = hj[u];
+            if (bits & 1u) v.x = fmaf(-hq[u].x, f, v.x);
+            if (bits & 2u) v.y = fmaf(-hq[u].y, f, v.y);
+            if (bits & 4u) v.z = fmaf(-hq[u].z, f, v.z);
+            if (bits & 8u) v.w = fmaf(-hq[u].w, f, v.w);
+            *reinterpret_cast<float4 *>(rj + i) = v;
+          }
+        }
       }
     }
     __syncthreads();
@@ -1001,7 +1022,7 @@ gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d,
   static bool attr_done = false;
   if (!attr_done) {
     GPTQ_CUDA_CHECK(cudaFuncSetAttribute(obq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(OBQ_MAX_D * (OBQ_MAX_D + 1) * sizeof(float))));
+                                         (int)(OBQ_MAX_D * (OBQ_MAX_D + 4) * sizeof(float))));
     attr_done = true;
   }
   char *p = (char *)ws;
@@ -1015,7 +1036,7 @@ gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d,
   GPTQ_TRY(launch_grid(W, wdtype, m, d, ldw, dead_mask, maxq, scale, zero, Wf, ldwf, st, s));
   hinv_kernel<<<(unsigned)ceil_div(d * d, 256), 256, 0, s>>>(U, d, Hinv);
   GPTQ_LAUNCH_CHECK();
-  obq_kernel<<<(unsigned)m, OBQ_MAX_D, (size_t)d * (d + 1) * sizeof(float), s>>>(
+  obq_kernel<<<(unsigned)m, OBQ_MAX_D, (size_t)d * (((d + 3) / 4) * 4 + 4) * sizeof(float), s>>>(
       Wf, ldwf, (int)d, Hinv, scale, zero, maxq, codes, ldc, order);
   GPTQ_LAUNCH_CHECK();
   const int64_t words = ceil_div(d, 32) * bits;
