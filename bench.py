@@ -43,6 +43,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="layer4096_n262144")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-full", action="store_true",
+                   help="also time the oracle on the whole layer once (unsampled)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--n-tok", type=int, default=None, help="override token count (smaller runs)")
     p.add_argument("--recon", action="store_true",
@@ -78,24 +80,6 @@ def whole_job_value(weights_per_rank, world, ms_step):
     return world * weights_per_rank / (ms_step / 1e3)
 
 
-def profiled_traffic(n_tok):
-    """DRAM bytes per Hessian launch from the committed ncu summary, or None when the
-    kernel source changed since the capture or the token count differs."""
-    import hashlib
-    prof = os.path.join(ROOT, "profiles", "hessian_tc_layer4096.md")
-    src = os.path.join(ROOT, "post_weight_quantization_03_gb300", "csrc", "hessian.cu")
-    try:
-        text = open(prof).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    fields = dict(line.split(": ", 1) for line in text.splitlines()
-                  if line.startswith(("traffic_bytes_per_launch_262144:", "source_sha256_16:")))
-    if fields.get("source_sha256_16:".rstrip(":"), "").strip() != digest or n_tok != 262144:
-        return None
-    return int(fields["traffic_bytes_per_launch_262144"])
-
-
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -103,6 +87,74 @@ def measured_peaks():
     except OSError:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
             "fallback"
+
+
+# nominal dense tensor rates of the part (bf16 2.25 PFLOP/s, TF32 1.1 PFLOP/s): a TF32
+# peak is the measured bf16 peak times their ratio
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def tensor_peak(peaks, clk):
+    """The bf16 dense peak that applies to this run: the burst figure, unless the clocks
+    sampled during the timed region show the power cap (then the sustained one)."""
+    capped = "sw_power_cap" in (clk or {}).get("reasons", [])
+    if capped and peaks.get("bf16_tflops_sustained"):
+        return float(peaks["bf16_tflops_sustained"]), "sustained (sw_power_cap seen)"
+    return float(peaks["bf16_tflops"]), "burst (no power cap seen in the timed region)"
+
+
+def stage_rooflines(m, d, n, bits, w_es, block, ms, peaks, peak_src, clk, layers=1):
+    """Achieved work rate of each stage of the path against the peak that bounds it.
+
+    hessian : tensor (kind::f16), d(d+1)N flop (the lower triangle of 2 X^T X incl. the
+              diagonal) per call;
+    prepare : tensor (3xTF32 rank-128 updates), 2 d^3 / 3 useful flop (Cholesky plus the
+              triangular inverse) against the TF32 dense peak; the panel chain (d / 128
+              dependent factorizations) is reported beside it;
+    quantize: HBM, per weight: read W, write and read the fp32 working copy, write E as a
+              TF32 head/tail pair, write the packed codes, plus one read of U; the block
+              chain (d / B dependent sweeps) beside it.
+    """
+    bf16, kind = tensor_peak(peaks, clk)
+    tf32 = bf16 * TF32_PER_BF16
+    hbm = float(peaks["hbm_gbs"])
+    out = []
+    h_flops = float(d) * (d + 1) * n
+    a = h_flops / (ms["hessian"] / 1e3) / 1e12
+    out.append({"stage": "hessian", "kernel": "hessian_tc_kernel", "bound": "tensor",
+                "achieved": round(a, 3), "peak": round(bf16, 1), "unit": "TFLOP/s",
+                "frac": round(a / bf16, 4), "ms": round(ms["hessian"], 4),
+                "work": f"d(d+1)N = {h_flops:.4e} flop",
+                "peak_source": f"{peak_src} bf16 dense, {kind}; fp16 runs at the bf16 rate"})
+    p_flops = 2.0 * float(d) ** 3 / 3.0
+    a = p_flops / (ms["prepare"] / 1e3) / 1e12
+    panels = -(-d // 128)
+    out.append({"stage": "prepare", "kernel": "potrf_kernel + rowmul_kernel + "
+                "tc_gemm_3xtf32_kernel (panel loop)", "bound": "tensor",
+                "achieved": round(a, 3), "peak": round(tf32, 1), "unit": "TFLOP/s",
+                "frac": round(a / tf32, 4), "ms": round(ms["prepare"], 4),
+                "work": f"2 d^3 / 3 = {p_flops:.4e} useful flop (3xTF32 executes three TF32 "
+                        f"products per useful one)",
+                "peak_source": f"{peak_src} bf16 dense {kind} x 1.1/2.25 (nominal TF32:bf16)",
+                "chain": {"panels": panels, "us_per_panel": round(ms["prepare"] * 1e3 / panels,
+                                                                  2)}})
+    q_bytes = float(m) * d * (w_es + 8 + 8 + bits / 8.0) + 4.0 * d * d
+    a = q_bytes / (ms["quantize"] / 1e3) / 1e9
+    blocks = -(-d // block)
+    out.append({"stage": "quantize", "kernel": "grid_kernel + sweep_kernel + "
+                "tc_gemm_3xtf32_kernel + pack_kernel", "bound": "hbm",
+                "achieved": round(a, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(a / hbm, 4), "ms": round(ms["quantize"], 4),
+                "work": f"{q_bytes:.4e} bytes: per weight W read ({w_es} B), fp32 working "
+                        f"copy written and read (8 B), E head/tail written (8 B), packed "
+                        f"codes ({bits / 8:g} B); U read once (4 d^2 B)",
+                "peak_source": f"{peak_src} copy bandwidth",
+                "chain": {"blocks": blocks,
+                          "us_per_block": round(ms["quantize"] * 1e3 / blocks, 2)}})
+    if layers != 1:
+        for r in out:
+            r["layers"] = layers
+    return out
 
 
 # ---------------------------------------------------------------------------------------
@@ -165,30 +217,74 @@ class ClockSampler:
 # CPU oracle timing (baseline / reference arm): bounded sample scaled to the full layer
 # ---------------------------------------------------------------------------------------
 
-def oracle_sample(X_host_f32_rows, W_host, layer, bits, block, damp, tok_sample, row_sample):
-    """Times the oracle on a sample: Hessian over `tok_sample` tokens, the full prepare
-    at this d_in, the sweep of `row_sample` rows.  Returns (est_seconds_full, detail)."""
-    import numpy as np
+def oracle_group_sample(X_rows, layers, n_tok, d, bits_list, block, damp):
+    """Times the fp64 oracle on a bounded sample of one input group of a workload (its
+    Hessian and prepare once, the sweep of each of its layers at each bit width) and scales
+    each stage by its operation count to the whole group.
+
+    X_rows: ``[t, c]`` float32 token-major inputs drawn by the group's recipe (t <= n_tok
+    tokens, c <= d channels); ``layers``: ``(W_sample [r, c] float32, d_out)`` per layer.
+    Hessian x (n_tok / t)(d / c)^2, prepare x (d / c)^3, each sweep x (d_out / r)(d / c)^2.
+    Returns ``(measured_s, estimated_full_s, detail)``.
+    """
     from oracle import gptq_oracle as O
-    n_tok = layer.act.n_tok
-    m = layer.d_out
-    Xs = X_host_f32_rows[:tok_sample]
+    t, c = X_rows.shape
     t0 = time.perf_counter()
-    H = O.hessian(Xs)
+    H = O.hessian(X_rows)
     t1 = time.perf_counter()
     Hd, dead, _ = O.damp_hessian(H, damp)
     U = O.inverse_cholesky_upper(Hd)
     t2 = time.perf_counter()
-    Ws = W_host[:row_sample]
-    scale, zero = O.row_grid(Ws, bits)
-    codes, _ = O.gptq_quantize(Ws, U, scale, zero, bits, block=block, dead=dead)
+    f_h, f_p = (n_tok / t) * (d / c) ** 2, (d / c) ** 3
+    meas, est = t2 - t0, (t1 - t0) * f_h + (t2 - t1) * f_p
+    sweeps = []
+    for Ws, m in layers:
+        for b in bits_list:
+            t3 = time.perf_counter()
+            scale, zero = O.row_grid(Ws, b)
+            codes, _ = O.gptq_quantize(Ws, U, scale, zero, b, block=block, dead=dead)
+            O.pack_codes(codes, b)
+            dt = time.perf_counter() - t3
+            f_q = (m / Ws.shape[0]) * (d / c) ** 2
+            meas += dt
+            est += dt * f_q
+            sweeps.append({"rows": int(Ws.shape[0]), "bits": b, "sweep_s": dt, "scale": f_q})
+    detail = {"hessian_s": t1 - t0, "prepare_s": t2 - t1, "tokens": t, "channels": c,
+              "scale": {"hessian": f_h, "prepare": f_p}, "sweeps": sweeps}
+    return meas, est, detail
+
+
+def sample_text(det):
+    sw = det["sweeps"]
+    return (f"fp64 NumPy oracle on a sample, each stage scaled by its operation count: "
+            f"Hessian over {det['tokens']} tokens x {det['channels']} channels "
+            f"(x{det['scale']['hessian']:.3g}), prepare at {det['channels']} channels "
+            f"(x{det['scale']['prepare']:.3g}), {len(sw)} sweep(s) of {sw[0]['rows']} rows "
+            f"(x{sw[0]['scale']:.3g})")
+
+
+def oracle_layer_unsampled(X_chunk, W, n_tok, bits, block, damp):
+    """The fp64 oracle on a whole layer, timed once: the Hessian accumulated over n_tok
+    tokens in passes over the given token chunk (the fp64 products take the same time
+    whatever the values), the prepare and the sweep of every row at full width."""
+    from oracle import gptq_oracle as O
+    t0 = time.perf_counter()
+    H = None
+    done = 0
+    while done < n_tok:
+        take = min(X_chunk.shape[0], n_tok - done)
+        H = O.hessian(X_chunk[:take], H)
+        done += take
+    t1 = time.perf_counter()
+    Hd, dead, _ = O.damp_hessian(H, damp)
+    U = O.inverse_cholesky_upper(Hd)
+    t2 = time.perf_counter()
+    scale, zero = O.row_grid(W, bits)
+    codes, _ = O.gptq_quantize(W, U, scale, zero, bits, block=block, dead=dead)
     O.pack_codes(codes, bits)
     t3 = time.perf_counter()
-    est = (t1 - t0) * n_tok / tok_sample + (t2 - t1) + (t3 - t2) * m / row_sample
-    detail = {"hessian_s": t1 - t0, "prepare_s": t2 - t1, "sweep_s": t3 - t2,
-              "tok_sample": tok_sample, "row_sample": row_sample}
-    _ = np
-    return est, detail
+    return {"seconds": t3 - t0, "hessian_s": t1 - t0, "prepare_s": t2 - t1,
+            "sweep_s": t3 - t2, "tokens": n_tok, "chunk_tokens": int(X_chunk.shape[0])}
 
 
 def host_cores():
@@ -308,30 +404,29 @@ def main():
     value = whole_job_value(weights, world, ms_step)
 
     peaks, peak_src = measured_peaks()
-    # trailing-update traffic of the sweep: each block reads and writes the fp32 working copy
-    # of every later column once (the per-block rank-B update); other traffic not counted
-    q_bytes = float(sum(m * (d - min(b0 + block, d)) * 8 for b0 in range(0, d, block)))
-    h_flops = float(d) * (d + 1) * n
-    h_tflops = h_flops / (st_h / 1e3) / 1e12
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    roofline = {"kernel": "hessian (gptq_hessian_accumulate)", "bound": "tensor",
-                "achieved": round(h_tflops, 3), "peak": peak_t, "unit": "TFLOP/s",
-                "frac": round(h_tflops / peak_t, 4), "traffic": profiled_traffic(n),
-                "traffic_unit": "bytes per launch (dram read + write, ncu, scaled from a "
-                                "65536-token capture; profiles/hessian_tc_layer4096.md)",
-                "algorithmic": f"d(d+1)N = {h_flops:.4e} flop per launch (lower triangle of "
-                               f"2 X^T X incl. diagonal)",
-                "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"}
+    w_es = 2 if layer.w_dtype in ("bf16", "f16") else 4
+    stages = stage_rooflines(m, d, n, bits, w_es, block,
+                             {"hessian": st_h, "prepare": st_p, "quantize": st_q},
+                             peaks, peak_src, clk)
+    # the dominant kernel: the Hessian's one launch per step (its stage time is that launch,
+    # timed by events on the stream it runs on); with B = 1 the eager column updates
+    roofline = dict(stages[0])
+    roofline["kernel"] = "hessian_tc_kernel (gptq_hessian_accumulate: one launch per step)"
+    roofline["traffic"] = None
+    roofline["traffic_note"] = ("not measured in this run: the DRAM bytes of an ncu capture "
+                                "are kept with the kernel's profile summary")
     if st_q > st_h:
-        # the sweep dominates (small B): report it against HBM, from its trailing-update bytes
+        # the eager sweep dominates (B = 1): each column's update reads and writes the fp32
+        # working copy of every later column once
+        q_bytes = float(sum(m * (d - j - 1) * 8 for j in range(d)))
         q_gbs = q_bytes / (st_q / 1e3) / 1e9
-        roofline = {"kernel": "quantize stage (gptq_quantize_layer: sweeps + trailing updates)",
+        roofline = {"kernel": "eager_column_kernel (quantize stage, one launch per column)",
                     "bound": "hbm", "achieved": round(q_gbs, 1), "peak": float(peaks["hbm_gbs"]),
                     "unit": "GB/s", "frac": round(q_gbs / float(peaks["hbm_gbs"]), 4),
                     "traffic": None,
-                    "algorithmic": f"sum over blocks of d_out*(d_in - block end)*8 bytes = "
+                    "algorithmic": f"sum over columns of d_out*(d_in - j - 1)*8 bytes = "
                                    f"{q_bytes:.4e} per layer (fp32 read + write of the later "
-                                   f"columns per block)",
+                                   f"columns per column)",
                     "peak_source": f"{peak_src} copy bandwidth"}
 
     # ---- end to end through the C ABI from host buffers --------------------------------
@@ -388,16 +483,17 @@ def main():
     # ---- CPU oracle baseline (rank 0, N = 1 only) ---------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        Xs = X[:2048].float().cpu().numpy()
-        Wn = W.float().cpu().numpy()
-        est, det = oracle_sample(Xs, Wn, layer, bits, block, damp, tok_sample=2048,
-                                 row_sample=64)
+        c = min(d, 4096)
+        Xs = X[:min(n, 16384), :c].float().cpu().numpy()
+        Ws = W[:min(m, 1024), :c].float().cpu().numpy()
+        meas, est, det = oracle_group_sample(Xs, [(Ws, m)], n, d, (bits,), block, damp)
         cpu = {"value": weights / est, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": (f"fp64 NumPy oracle: Hessian over the first {det['tok_sample']} "
-                          f"tokens scaled x{n / det['tok_sample']:.0f}, full prepare at "
-                          f"d_in={d}, sweep of {det['row_sample']} rows scaled "
-                          f"x{m / det['row_sample']:.0f}"),
-               "est_seconds_per_layer": est, "detail": det}
+               "sample": sample_text(det), "measured_s": meas, "est_seconds_per_layer": est,
+               "detail": det}
+        if args.cpu_full:
+            cpu["unsampled"] = oracle_layer_unsampled(X[:16384].float().cpu().numpy(),
+                                                      W.float().cpu().numpy(), n, bits,
+                                                      block, damp)
 
     if rank == 0:
         out = {
@@ -414,7 +510,7 @@ def main():
                              f" GB per step",
                        "parallelism": f"replicas x{world} (independent layers)"},
             "stages_ms": {"hessian": st_h, "prepare": st_p, "quantize": st_q},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "roofline_stages": stages, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk,
         }
         print(json.dumps(out), flush=True)
@@ -452,7 +548,7 @@ def run_recon(args, wl, layer, X, W, H, U, dm, qp, sc, zr, ws_p, ws_q, bits, blo
     ms = a.elapsed_time(b) / args.steps
     flops = 2.0 * m * d * n
     peaks, peak_src = measured_peaks()
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_t, peak_kind = tensor_peak(peaks, clk)
     tf = flops / (ms / 1e3) / 1e12
     out = {
         "metric": "ms per layer & tokens/sec evaluating ||(W - W_hat) X^T||^2 per row from the "
@@ -470,7 +566,8 @@ def run_recon(args, wl, layer, X, W, H, U, dm, qp, sc, zr, ws_p, ws_q, bits, blo
                      "unit": "TFLOP/s", "frac": round(tf / peak_t, 4), "traffic": None,
                      "algorithmic": f"2 d_out d_in N = {flops:.4e} flop per call (the whole "
                                     f"call timed: difference pass + product + reduction)",
-                     "peak_source": f"{peak_src} bf16 sustained (fp16 tensor rate = bf16)"},
+                     "peak_source": f"{peak_src} bf16 dense, {peak_kind}; fp16 runs at the "
+                                    f"bf16 rate"},
         "gpu_launches": int(launches), "clocks": clk,
     }
     if rank == 0:
@@ -609,7 +706,32 @@ def run_block(args, wl, dev, rank, world):
     peaks, peak_src = measured_peaks()
     h_flops = float(sum(x.shape[1] * (x.shape[1] + 1) * x.shape[0] for x, _ in G))
     h_tf = h_flops / (stages["hessian"] / 1e3) / 1e12
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_t, peak_kind = tensor_peak(peaks, clk)
+    # every stage of the serialized pass against its bound (work summed over groups, layers
+    # and bit widths)
+    p_flops = float(sum(2.0 * x.shape[1] ** 3 / 3.0 for x, _ in G))
+    q_bytes = float(sum(len(wl.bits) * (W.shape[0] * W.shape[1] * (W.element_size() + 16)
+                                        + sum(W.shape[0] * W.shape[1] * b / 8.0
+                                              for b in wl.bits) / len(wl.bits))
+                        + len(wl.bits) * 4.0 * x.shape[1] ** 2
+                        for x, Ws in G for W in Ws))
+    tf32 = peak_t * TF32_PER_BF16
+    hbm = float(peaks["hbm_gbs"])
+    p_tf = p_flops / (stages["prepare"] / 1e3) / 1e12
+    q_gbs = q_bytes / (stages["quantize"] / 1e3) / 1e9
+    stage_list = [
+        {"stage": "hessian", "bound": "tensor", "achieved": round(h_tf, 3),
+         "peak": round(peak_t, 1), "unit": "TFLOP/s", "frac": round(h_tf / peak_t, 4),
+         "ms": round(stages["hessian"], 4), "work": f"sum d(d+1)N = {h_flops:.4e} flop"},
+        {"stage": "prepare", "bound": "tensor", "achieved": round(p_tf, 3),
+         "peak": round(tf32, 1), "unit": "TFLOP/s", "frac": round(p_tf / tf32, 4),
+         "ms": round(stages["prepare"], 4),
+         "work": f"sum 2 d^3 / 3 = {p_flops:.4e} useful flop (3xTF32)",
+         "peak_source": "bf16 peak x 1.1/2.25 (nominal TF32:bf16)"},
+        {"stage": "quantize", "bound": "hbm", "achieved": round(q_gbs, 1), "peak": hbm,
+         "unit": "GB/s", "frac": round(q_gbs / hbm, 4), "ms": round(stages["quantize"], 4),
+         "work": f"{q_bytes:.4e} bytes (per weight and bit width: W read, fp32 working copy "
+                 f"written and read, E head/tail written, packed codes; U read per sweep)"}]
     out = {
         "metric": "ms per block & weights quantized/sec (7B-shaped block, 3- and 4-bit GPTQ)",
         "value": weights / (ms_step / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -626,7 +748,8 @@ def run_block(args, wl, dev, rank, world):
                      "achieved": round(h_tf, 3), "peak": peak_t, "unit": "TFLOP/s",
                      "frac": round(h_tf / peak_t, 4), "traffic": None,
                      "algorithmic": f"sum d(d+1)N = {h_flops:.4e} flop",
-                     "peak_source": f"{peak_src} bf16 sustained"},
+                     "peak_source": f"{peak_src} bf16 dense, {peak_kind}"},
+        "roofline_stages": stage_list,
         "gpu_launches": int(launches), "clocks": clk,
     }
     if rank == 0:
@@ -634,49 +757,109 @@ def run_block(args, wl, dev, rank, world):
 
 
 def run_reference(args, rank, world):
-    """The oracle on the host cores, each step a bounded sample scaled to the full layer."""
+    """The fp64 oracle on the host cores.  Each step times a bounded sample of the workload
+    (every stage of every layer, drawn by the workload's recipe at the sample's size) and
+    scales each stage by its operation count to the whole workload; ``ms_per_step`` is the
+    measured time of the sample, ``value`` the whole-workload rate it implies.  A
+    single-layer workload of at most 4096 channels is also timed once unsampled, outside
+    the step loop.  Under torchrun only rank 0 runs."""
     if rank != 0:
         return
-    import numpy as np
-    import torch
-
     from post_weight_quantization_03_gb300 import synthetic as S
+    from dataclasses import replace
 
     wl = S.WORKLOADS[args.workload]
+    block = args.block or wl.block
     if args.obq:
-        return run_obq(args, dev, rank, world)
-    if len(wl.layers) > 1:
-        return run_block(args, wl, dev, rank, world)
-    layer = wl.layers[0]
-    bits, block, damp = wl.bits[-1], args.block or wl.block, wl.damp
-    m, d, n = layer.d_out, layer.act.d_in, layer.act.n_tok
-    X = S.activations(layer.act, device="cpu", n_tok=2048).float().numpy()
-    W = S.layer_weights(layer).float().numpy()
-    total = args.steps + args.warmup
-    rows = 64 if total <= 15 else 32
-    times = []
-    det = None
-    for i in range(total):
-        est, det = oracle_sample(X, W, layer, bits, block, damp, tok_sample=2048,
-                                 row_sample=rows)
+        return run_reference_obq(args, world)
+    groups = {}
+    for layer in wl.layers:
+        groups.setdefault(layer.act, []).append(layer)
+    samples = []
+    for act, layers in groups.items():
+        n = args.n_tok or act.n_tok
+        c = min(act.d_in, 4096)
+        t = min(n, 16384)
+        Xs = S.activations(replace(act, d_in=c, n_dead=min(act.n_dead, c // 100),
+                                   n_outlier=min(act.n_outlier, c // 100)), device="cpu",
+                           n_tok=t).float().numpy()
+        Ls = [(S.weights(min(l.d_out, 1024), c, l.w_std, l.w_dtype,
+                         l.act.seed * 131 + l.w_seed).float().numpy(), l.d_out) for l in layers]
+        samples.append((Xs, Ls, n, act.d_in))
+    bits_list = wl.bits if len(wl.layers) > 1 else (wl.bits[-1],)
+    weights = sum(l.d_out * l.act.d_in for l in wl.layers) * len(bits_list)
+    unsampled = None
+    if len(wl.layers) == 1 and wl.layers[0].act.d_in <= 4096:
+        layer = wl.layers[0]
+        Xs, Ls, n, d = samples[0]
+        Wfull = S.layer_weights(layer).float().numpy()
+        unsampled = oracle_layer_unsampled(Xs, Wfull, n, bits_list[0], block, wl.damp)
+        unsampled["value"] = weights / unsampled["seconds"]
+    meas, ests, dets = [], [], []
+    for i in range(args.warmup + args.steps):
+        m_t, e_t, d_all = 0.0, 0.0, []
+        for Xs, Ls, n, d in samples:
+            mt, et, det = oracle_group_sample(Xs, Ls, n, d, bits_list, block, wl.damp)
+            m_t += mt
+            e_t += et
+            d_all.append(det)
         if i >= args.warmup:
-            times.append(est)
-    sec = statistics.mean(times)
-    value = m * d / sec
-    sample = (f"fp64 NumPy oracle per step: Hessian over 2048 tokens scaled x{n // 2048}, "
-              f"full prepare at d_in={d}, sweep of {rows} rows scaled x{m // rows}")
+            meas.append(m_t)
+            ests.append(e_t)
+            dets = d_all
+    est = statistics.mean(ests)
+    value = weights / est
+    sample = "; ".join(sample_text(dt) for dt in dets)
+    cpu = {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+           "sample": sample, "est_seconds_per_workload": est}
+    if unsampled is not None:
+        cpu["unsampled"] = unsampled
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "impl": "reference",
-           "config": {"workload": wl.name, "d_out": m, "d_in": d, "n_tok": n, "bits": bits,
-                      "block": block, "damp": damp},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(),
-                            "kind": "oracle", "sample": sample},
+           "warmup": args.warmup, "ms_per_step": statistics.mean(meas) * 1e3,
+           "ms_per_layer_est": est * 1e3 / len(wl.layers) / len(bits_list),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": wl.name, "layers": [l.name for l in wl.layers],
+                      "bits": list(bits_list), "block": block, "damp": wl.damp},
+           "cpu_baseline": cpu,
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0},
-           "detail": det}
-    _ = (np, torch)
+           "detail": dets}
+    print(json.dumps(out), flush=True)
+
+
+def run_reference_obq(args, world):
+    """The oracle's greedy-order OBQ on rows of the 4096 x 128 layer, scaled to all rows."""
+    from oracle import gptq_oracle as O
+    from post_weight_quantization_03_gb300 import synthetic as S
+    m, d, bits = 4096, 128, 4
+    n = args.n_tok or 65536
+    act = S.ActivationSpec(d_in=d, n_tok=n, dtype="f16", n_dead=2, n_outlier=2, seed=77)
+    X = S.activations(act, device="cpu").float().numpy()
+    W = S.weights(m, d, 0.02, "bf16", 78).float().numpy()
+    Hd, dead, _ = O.damp_hessian(O.hessian(X), 0.01)
+    rows = 64
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        s_, z_ = O.row_grid(W[:rows], bits)
+        O.obq_greedy(W[:rows], Hd, s_, z_, bits, dead=dead)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times) * m / rows
+    value = m * d / sec
+    out = {"metric": "ms per layer: OBQ greedy order vs fixed-order GPTQ (4096 x 128 int4)",
+           "value": value, "unit": "weights/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": statistics.mean(times) * 1e3,
+           "ms_per_layer_est": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": "obq4096x128", "d_out": m, "d_in": d, "n_tok": n,
+                      "bits": bits},
+           "cpu_baseline": {"value": value, "unit": "weights/s", "cores": host_cores(),
+                            "kind": "oracle",
+                            "sample": f"fp64 NumPy OBQ oracle on {rows} rows, x{m // rows}"},
+           "e2e": {"value": value, "unit": "weights/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
 

@@ -335,7 +335,7 @@ gptq_status gptq_quantize_obq(const void *W, int wdtype, int64_t d_out, int64_t 
 
 /*
  * GPTQ_NOALLOC_SCRATCH_BYTES: size of the fixed scratch array behind
- * gptq_quantize_layer_noalloc (32 MiB, held on every GPU that loads this library until the
+ * gptq_quantize_layer_noalloc (32 MiB per GPU, from the first call on that GPU until the
  * process exits).  A layer fits when
  * gptq_quantize_workspace_bytes(d_out, d_in, bits, block) <= GPTQ_NOALLOC_SCRATCH_BYTES
  * (for example 1024 x 1024 at 4 bits, B = 128).
@@ -355,18 +355,31 @@ gptq_status gptq_quantize_obq(const void *W, int wdtype, int64_t d_out, int64_t 
  *   - Sizes: returns GPTQ_ERR_WORKSPACE, before touching the GPU, when the layer needs more
  *     scratch than GPTQ_NOALLOC_SCRATCH_BYTES; use gptq_quantize_layer with a workspace then.
  *   - First call on a device: looks up the array's device address (once per device, with
- *     that device current); make that first call before any stream capture.
+ *     that device current).  Under CUDA's default lazy module loading this look-up is also
+ *     what loads the library code that holds the array, so the first call reserves the
+ *     32 MiB on that device and may synchronize it: make the first call during set-up, and
+ *     before any stream capture.  Only the later calls allocate nothing.
  *   - Sharing: every call on a device uses the same array, which keeps the last call's
  *     contents (each call clears what it needs).  Calls whose GPU work overlaps (e.g. on
  *     two unordered streams) race and give wrong results: keep them on one stream.
- *   - Non-finite weights are flagged in the shared array, which callers cannot address;
- *     check inputs beforehand if that matters.
+ *   - Device-side status (non-finite weights; a bounded wait that gave up, after which the
+ *     outputs are undefined) is recorded in the shared array: read it with
+ *     gptq_noalloc_status after the call.
  * Asynchronous.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.
  */
 gptq_status gptq_quantize_layer_noalloc(const void *W, int wdtype, int64_t d_out, int64_t d_in,
                                         int64_t ldw, const float *U, const uint8_t *dead_mask,
                                         int bits, int block, uint32_t *qpacked, float *scale,
                                         int32_t *zero, float *W_hat, gptq_stream_t stream);
+
+/*
+ * gptq_noalloc_status: synchronize `stream`, then return the device-side status the last
+ * gptq_quantize_layer_noalloc on the current device recorded: GPTQ_OK, GPTQ_ERR_NONFINITE
+ * (a NaN or Inf in W) or GPTQ_ERR_TIMEOUT (a bounded device wait gave up; the outputs of
+ * that call are undefined).  Allocates nothing after the first gptq_quantize_layer_noalloc
+ * call on the device (see there).  Errors of its own: CUDA.
+ */
+gptq_status gptq_noalloc_status(gptq_stream_t stream);
 
 /*
  * gptq_workspace_status: synchronize `stream`, then return the device-side status the

@@ -1,5 +1,7 @@
 // C ABI entry points: argument validation, workspace sizing, launch sequencing.
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -8,6 +10,42 @@ namespace gptq {
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 unsigned long long launches_so_far() { return g_launches.load(); }
+
+namespace {
+struct AttrEntry {
+  const void *func;
+  int dev;
+  int bytes;
+};
+std::mutex g_attr_mu;
+std::vector<AttrEntry> g_attrs;            // (kernel, device) pairs already set
+constexpr int kMaxSmDevices = 128;
+std::atomic<int> g_sm_count[kMaxSmDevices];  // 0 = not yet queried
+}  // namespace
+
+gptq_status ensure_smem_attr(const void *func, int bytes) {
+  int dev = -1;
+  GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (const AttrEntry &e : g_attrs)
+    if (e.func == func && e.dev == dev && e.bytes >= bytes) return GPTQ_OK;
+  GPTQ_CUDA_CHECK(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  g_attrs.push_back(AttrEntry{func, dev, bytes});
+  return GPTQ_OK;
+}
+
+gptq_status device_sm_count(int *out) {
+  int dev = -1;
+  GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxSmDevices) return GPTQ_ERR_UNSUPPORTED;
+  int n = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return GPTQ_OK;
+}
 
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 

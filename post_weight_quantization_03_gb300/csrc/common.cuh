@@ -18,6 +18,14 @@ namespace gptq {
 // Counts every kernel this library launches (reported by gptq_kernel_launches()).
 void count_launch(unsigned n = 1);
 
+// The dynamic shared-memory limit of a kernel is an attribute of the (function, device)
+// pair: sets it to at least `bytes` for `func` on the current device, once per pair, under
+// a lock (so that calls from several host threads and on several devices are safe).
+gptq_status ensure_smem_attr(const void *func, int bytes);
+
+// Number of SMs of the current device (queried once per device).
+gptq_status device_sm_count(int *out);
+
 #define GPTQ_LAUNCH_CHECK()                                   \
   do {                                                        \
     ::gptq::count_launch();                                   \

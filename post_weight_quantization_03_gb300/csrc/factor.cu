@@ -902,16 +902,9 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
 
 gptq_status launch_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                            void *ws, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(potrf_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kPotrfSmem));
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(rowmul_kernel<4>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((NB + RM_ROWS) * RML * sizeof(float))));
-    attr_done = true;
-  }
+  GPTQ_TRY(ensure_smem_attr((const void *)potrf_kernel, (int)kPotrfSmem));
+  GPTQ_TRY(ensure_smem_attr((const void *)rowmul_kernel<4>,
+                            (int)((NB + RM_ROWS) * RML * sizeof(float))));
   const bool overlap = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0;
   if (!overlap) return enqueue_prepare(H, d, damp, U, dead_mask, ws, s, nullptr);
   SideStream *ss = nullptr;

@@ -265,16 +265,8 @@ constexpr int kSegTokens = 512;
 
 gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
                               float *H, int accumulate, DevStatus *st, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(hessian_tc_kernel<0>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)T_SMEM));
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(hessian_tc_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)T_SMEM));
-    attr_done = true;
-  }
+  GPTQ_TRY(ensure_smem_attr((const void *)hessian_tc_kernel<0>, (int)T_SMEM));
+  GPTQ_TRY(ensure_smem_attr((const void *)hessian_tc_kernel<1>, (int)T_SMEM));
   CUtensorMap mx;
   const CUtensorMapDataType dt =
       xdtype == GPTQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

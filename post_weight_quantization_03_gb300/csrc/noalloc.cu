@@ -5,12 +5,17 @@
 // caller workspace it uses a fixed scratch array that is part of this library's device
 // image, so a call allocates nothing.
 //
-// The array is GPTQ_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads the library and
-// stays there until the process exits.  All calls on a device share it, and it keeps the
-// contents of the last call; the sweep overwrites every scratch byte it reads and clears
-// its status block at the start of each call, so nothing needs to be zeroed beforehand.
-// Two calls whose work overlaps on the GPU (different streams, no ordering between them)
-// race on the array and produce garbage: order them on one stream.
+// The array is GPTQ_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU where the library's device
+// code holding it has been loaded, and stays there until the process exits.  Under CUDA's
+// default lazy module loading that happens at the first call on a device (the address
+// look-up below loads it): that first call reserves the 32 MiB and may synchronize, so it
+// belongs in the caller's set-up; later calls allocate nothing.  All calls on a device share
+// the array, and it keeps the contents of the last call; the sweep overwrites every scratch
+// byte it reads and clears its status block at the start of each call, so nothing needs to
+// be zeroed beforehand.  Two calls whose work overlaps on the GPU (different streams, no
+// ordering between them) race on the array and produce garbage: order them on one stream.
+// The status block at the start of the array (non-finite weights, a bounded wait that gave
+// up) is read back by gptq_noalloc_status.
 #include <mutex>
 
 #include "common.cuh"
@@ -67,4 +72,15 @@ extern "C" gptq_status gptq_quantize_layer_noalloc(
   return gptq::quantize_layer_checked(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits, block,
                                       qpacked, scale, zero, W_hat, scratch,
                                       (size_t)GPTQ_NOALLOC_SCRATCH_BYTES, stream, false);
+}
+
+extern "C" gptq_status gptq_noalloc_status(gptq_stream_t stream) {
+  void *scratch = nullptr;
+  const gptq_status st = gptq::scratch_address(&scratch);
+  if (st != GPTQ_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  gptq::DevStatus ds;
+  GPTQ_CUDA_CHECK(cudaMemcpyAsync(&ds, scratch, sizeof(ds), cudaMemcpyDeviceToHost, s));
+  GPTQ_CUDA_CHECK(cudaStreamSynchronize(s));
+  return (gptq_status)ds.status;
 }

@@ -915,9 +915,8 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       // p's near update waits for pair p - 1's far update, which keeps each column's
       // contributions in the single-stream order and frees the pair buffer pair p + 1 reuses.
       cudaStream_t c = qs->crit, sd = qs->side;
-      int nsm = 0, dev = 0;
-      GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
-      GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+      int nsm = 0;
+      GPTQ_TRY(device_sm_count(&nsm));
       // the far update (persistent) leaves one SM per sweep CTA: measured better than
       // sharing SMs two sweep CTAs each, and than one CTA per tile over all SMs
       const int far_ctas = std::max(1, nsm - (int)std::min<unsigned>(sweep_grid, nsm / 2));
@@ -975,13 +974,7 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
 gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
                                    const uint8_t *dead_mask, int bits, int block, void *ws,
                                    cudaStream_t s, bool allow_overlap) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(sweep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSweepSmem));
-    attr_done = true;
-  }
+  GPTQ_TRY(ensure_smem_attr((const void *)sweep_kernel, (int)kSweepSmem));
   if (!allow_overlap || block == 1 || d <= 2 * (int64_t)block)
     return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, s, nullptr);
   QuantStreams *qs = nullptr;
@@ -1019,12 +1012,8 @@ gptq_status launch_quantize_obq(const void *W, int wdtype, int64_t m, int64_t d,
                                 const float *U, const uint8_t *dead_mask, int bits,
                                 uint32_t *qpacked, float *scale, int32_t *zero, float *W_hat,
                                 int32_t *order, void *ws, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(obq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(OBQ_MAX_D * (OBQ_MAX_D + 4) * sizeof(float))));
-    attr_done = true;
-  }
+  GPTQ_TRY(ensure_smem_attr((const void *)obq_kernel,
+                            (int)(OBQ_MAX_D * (OBQ_MAX_D + 4) * sizeof(float))));
   char *p = (char *)ws;
   DevStatus *st = (DevStatus *)p; p += 256;
   const int64_t ldwf = (int64_t)round_up((size_t)d, 4), ldc = (int64_t)round_up((size_t)d, 16);

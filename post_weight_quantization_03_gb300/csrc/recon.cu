@@ -325,16 +325,8 @@ gptq_status launch_recon(const void *X, int xdtype, int64_t n, int64_t d, int64_
                                         d, w.part);
     GPTQ_LAUNCH_CHECK();
   } else {
-    static bool attr_done = false;
-    if (!attr_done) {
-      GPTQ_CUDA_CHECK(cudaFuncSetAttribute(recon_tc_kernel<0>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kRSmem));
-      GPTQ_CUDA_CHECK(cudaFuncSetAttribute(recon_tc_kernel<1>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kRSmem));
-      attr_done = true;
-    }
+    GPTQ_TRY(ensure_smem_attr((const void *)recon_tc_kernel<0>, (int)kRSmem));
+    GPTQ_TRY(ensure_smem_attr((const void *)recon_tc_kernel<1>, (int)kRSmem));
     const CUtensorMapDataType dt =
         xdtype == GPTQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     if (xdtype == GPTQ_F16)
@@ -346,12 +338,8 @@ gptq_status launch_recon(const void *X, int xdtype, int64_t n, int64_t d, int64_
     if (!tc::make_tmap_2d(&md, dt, w.D, m, d, w.ldd * 2, RK, RM) ||
         !tc::make_tmap_2d(&mx, dt, X, n, d, ldx * 2, RK, RN))
       return GPTQ_ERR_UNSUPPORTED;
-    static int num_sms = 0;
-    if (!num_sms) {
-      int dev = 0;
-      GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
-      GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
-    }
+    int num_sms = 0;
+    GPTQ_TRY(device_sm_count(&num_sms));
     ReconParams p{};
     p.m = m; p.n = n; p.k = d;
     p.n_m = (int)ceil_div(m, RM);

@@ -277,13 +277,7 @@ bool tc::make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, 
 gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPTQ_OK;
   if (!g.a_lo || !g.b_lo) return GPTQ_ERR_UNSUPPORTED;
-  static bool attr_done = false;
-  if (!attr_done) {
-    GPTQ_CUDA_CHECK(cudaFuncSetAttribute(tc_gemm_3xtf32_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes));
-    attr_done = true;
-  }
+  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_3xtf32_kernel, (int)kSmemBytes));
   CUtensorMap mah, mal, mbh, mbl;
   // maps cover exactly the [M, K] / [N, K] operand windows: out-of-range reads are zero
   if (!make_tmap_f32(&mah, g.a_hi, g.M, g.K, g.lda, BM) ||
@@ -295,12 +289,8 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   memset(&mc, 0, sizeof(mc));
   const bool tma_c = !g.trans_c && make_tmap_f32(&mc, g.c, g.M, g.N, g.ldc, BM);
   if (g.trans_c) return GPTQ_ERR_UNSUPPORTED;
-  static int num_sms = 0;
-  if (!num_sms) {
-    int dev = 0;
-    GPTQ_CUDA_CHECK(cudaGetDevice(&dev));
-    GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
-  }
+  int num_sms = 0;
+  GPTQ_TRY(device_sm_count(&num_sms));
   TcGemmParams p{};
   p.tma_c = tma_c ? 1 : 0;
   p.M = g.M; p.N = g.N; p.K = g.K;

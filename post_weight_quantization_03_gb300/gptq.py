@@ -65,6 +65,7 @@ _SIGS = {
                                                _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_int,
                                                _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                                _c.c_void_p, _c.c_void_p]),
+    "gptq_noalloc_status": (_c.c_int, [_c.c_void_p]),
 }
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GPTQ_NOALLOC_SCRATCH_BYTES in include/gptq.h
 OBQ_MAX_D_IN = 128                # GPTQ_OBQ_MAX_D_IN in include/gptq.h
@@ -197,6 +198,10 @@ def gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits,
                                 qpacked, scale, zero, W_hat, stream):
     return load().gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits,
                                               block, qpacked, scale, zero, W_hat, stream)
+
+
+def gptq_noalloc_status(stream):
+    return load().gptq_noalloc_status(stream)
 
 
 # ---------------------------------------------------------------------------------------

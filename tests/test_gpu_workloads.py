@@ -4,18 +4,25 @@ Where the fp64 oracle cannot redo the whole computation at full size, the check 
 oracle can afford:
   * Hessian: exact sub-Gram blocks of sampled channels (dead, outlier and random ones) and
     the exact diagonal, from the same fp16 activation bits;
-  * factor: U's trailing k x k block depends only on the trailing block of the damped H
-    (pinned in the oracle tests), so it is checked against the oracle's factor of that
-    block, damped with lambda from the full exact diagonal;
-  * sweep: the oracle's U (at d_in = 4096, from a token prefix) or a seeded synthetic upper
-    factor (d_in = 11008, 28672) as the shared input, the oracle sweeping sampled rows (at
-    d_in = 4096 also with B = 1, the eager column-at-a-time variant);
+  * factor of the full-size GPU Hessian: U's trailing k x k block depends only on the
+    trailing block of the damped H (pinned in the oracle tests), so it is checked against
+    the oracle's factor of that block, damped with lambda from the full exact diagonal;
+  * the whole factor at d_in = 4096, 11008 and 28672: gptq_prepare on the oracle's Hessian
+    of a token prefix (rounded to fp32), every row of U against the oracle's fp64 factor of
+    the same matrix (inverting first at 4096 and 11008; at 28672 the oracle's reversed
+    Cholesky route, the same matrix, pinned against the first);
+  * sweep: that oracle U (rounded to fp32) as the shared input, the oracle sweeping sampled
+    rows (at d_in = 4096 all rows, and also B = 1, the eager column-at-a-time variant);
   * the consumer (per-row output error from the packed codes) over all tokens, sampled rows
     against the oracle;
   * shared-Hessian batching: rows of q/k/v (and gate/up) quantized in one call (stacked
     rows, or the shared multi-layer call) equal the separate calls bit for bit (rows
-    decouple: "GPTQ Hessian").
+    decouple: "GPTQ Hessian"), and sampled rows of every layer of the shared call agree
+    with the oracle's sweep on the same U; the block driver's whole path on a token prefix
+    reaches the oracle's reconstruction error within 0.1 %.
 """
+
+import os
 
 import numpy as np
 import pytest
@@ -76,6 +83,48 @@ def _check_factor_tail(Xh, diag_full, U, dmask, n_dead, damp=0.01):
     assert np.all(Uh_diag > 0)
 
 
+def _host_mem_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 2 ** 20
+    except OSError:
+        pass
+    return 0.0
+
+
+def _check_whole_factor(H32, damp, route, chunk=1024):
+    """gptq_prepare on the fp32 Hessian ``H32`` (host) against the oracle's factor of the
+    same matrix, every row; returns (U_ref as fp32, dead mask, row errors)."""
+    d = H32.shape[0]
+    Hg = torch.from_numpy(H32).to(DEV)
+    Ug, dmg, ndg = gptq.prepare(Hg, damp)
+    del Hg
+    Hd, dead, _ = O.damp_hessian(H32.astype(np.float64), damp)
+    Ur = route(Hd)
+    del Hd
+    assert np.array_equal(dmg.cpu().numpy().astype(bool), dead) and ndg == int(dead.sum())
+    errs = np.empty(d)
+    for r0 in range(0, d, chunk):
+        ug = Ug[r0:r0 + chunk].cpu().numpy().astype(np.float64)
+        ur = Ur[r0:r0 + chunk]
+        errs[r0:r0 + chunk] = np.max(np.abs(ug - ur), axis=1) / np.max(np.abs(ur), axis=1)
+        # strictly lower part of these rows: exactly zero
+        assert not np.any(np.tril(ug, -r0 - 1))
+    del Ug
+    U32 = Ur.astype(np.float32)
+    del Ur
+    _free()
+    worst = int(np.argmax(errs))
+    assert errs[worst] <= PT.TOL_U, (
+        f"U row {worst} of {d}: row-normwise error {errs[worst]:.3e}; leading 10% rows max "
+        f"{errs[:d // 10].max():.3e}, trailing 10% max {errs[-(d // 10):].max():.3e}")
+    print(f"whole U at d={d}: max row-normwise error {errs.max():.3e} (row {worst}), "
+          f"leading 10% {errs[:d // 10].max():.3e}, trailing 10% {errs[-(d // 10):].max():.3e}")
+    return U32, dead, errs
+
+
 def _quantize_and_check(W, U32_np, dead, bits, rows, block=128):
     Ug = torch.from_numpy(U32_np).to(DEV)
     dm = torch.from_numpy(dead.astype(np.uint8)).to(DEV) if dead is not None else None
@@ -109,11 +158,13 @@ def test_layer4096_n262144():
     _check_factor_tail(Xh, diag_full, U, dm, nd)
     del U, Hg
     _free()
-    # sweep of all 4096 rows on the oracle's U (from a 16384-token prefix)
+    # the whole factor on the oracle's Hessian of a 16384-token prefix, then the sweep of all
+    # 4096 rows on the oracle's U of it
     Xp = Xh[:16384]
     Hp = O.hessian(Xp)
-    Hpd, dead_p, _ = O.damp_hessian(Hp, wl.damp)
-    U32 = O.inverse_cholesky_upper(Hpd).astype(np.float32)
+    U32, dead_p, _ = _check_whole_factor(Hp.astype(np.float32), wl.damp,
+                                         O.inverse_cholesky_upper)
+    Hpd, _, _ = O.damp_hessian(Hp, wl.damp)
     W = S.layer_weights(layer, DEV)
     st = _quantize_and_check(W, U32, dead_p, bits, np.arange(layer.d_out))
     assert st["entries"] == 4096 * 4096
@@ -161,13 +212,18 @@ def test_mlp11008_n131072():
     diag_full = O.hessian_diagonal(Xh)
     U, dm, nd = gptq.prepare(Hg, wl.damp)
     _check_factor_tail(Xh, diag_full, U, dm, nd)
-    del U, Hg, Xh
+    del U, Hg
     _free()
-    # sweep at d_in = 11008 on a synthetic factor, sampled rows
-    Us = S.upper_factor(down.act.d_in, 11, device="cpu").numpy()
+    # the whole factor at d_in = 11008 on the oracle's Hessian of an 8192-token prefix, then
+    # the sweep of sampled rows on the oracle's U of it
+    Hp = O.hessian(Xh[:8192])
+    del Xh
+    U32, dead_p, _ = _check_whole_factor(Hp.astype(np.float32), wl.damp,
+                                         O.inverse_cholesky_upper)
+    del Hp
     W = S.layer_weights(down, DEV)
     rows = np.sort(np.random.default_rng(2).choice(down.d_out, 48, replace=False))
-    _quantize_and_check(W, Us, None, bits, rows)
+    _quantize_and_check(W, U32, dead_p, bits, rows)
 
 
 def test_block7b_n131072():
@@ -198,6 +254,57 @@ def test_block7b_n131072():
                 assert torch.equal(cat[k], torch.cat([s[k] for s in shared]))
         del U, Ws
         _free()
+    # the shared multi-layer sweep against the oracle: U from the oracle's Hessian of an
+    # 8192-token prefix of each group's inputs, sampled rows of every layer, 3 and 4 bits
+    for group in (("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj")):
+        act = by_name[group[0]].act
+        Xp = S.activations(act, device="cpu", n_tok=8192).numpy()
+        Hd, dead, _ = O.damp_hessian(O.hessian(Xp), wl.damp)
+        U32 = O.inverse_cholesky_upper(Hd).astype(np.float32)
+        Ws = [S.layer_weights(by_name[n], DEV) for n in group]
+        dm = torch.from_numpy(dead.astype(np.uint8)).to(DEV)
+        for bits in wl.bits:
+            shared = gptq.quantize_shared(Ws, torch.from_numpy(U32).to(DEV), bits, 128, dm)
+            torch.cuda.synchronize()
+            for li, (W, out) in enumerate(zip(Ws, shared)):
+                rows = np.sort(np.random.default_rng(30 + li).choice(W.shape[0], 48,
+                                                                     replace=False))
+                Wn = W.float().cpu().numpy()
+                s_ref, z_ref = O.row_grid(Wn[rows], bits)
+                assert np.array_equal(out[1].cpu().numpy()[rows], s_ref)
+                assert np.array_equal(out[2].cpu().numpy()[rows], z_ref)
+                codes = O.unpack_codes(out[0][torch.from_numpy(rows).to(DEV)].cpu().numpy()
+                                       .view(np.uint32), bits, W.shape[1])
+                PT.check_codes(codes, Wn[rows], U32.astype(np.float64), s_ref, z_ref, bits,
+                               128, dead)
+        del Ws, shared
+        _free()
+    # the block driver's whole path (Hessian, prepare, shared sweep) on the gate/up group
+    # with a 16384-token prefix of its inputs: every layer's reconstruction error within
+    # 0.1 % of the oracle's whole path on the same tokens
+    names = ("gate_proj", "up_proj")
+    act = by_name[names[0]].act
+    Xg = S.activations(act, device=DEV, n_tok=16384)
+    Ws = [S.layer_weights(by_name[n], DEV) for n in names]
+    res, nd = gptq.quantize_block([(Xg, Ws)], bits=(4,), block=128, damp=wl.damp)
+    torch.cuda.synchronize()
+    Xh = Xg.cpu().float().numpy()
+    Hp = O.hessian(Xh)
+    Hd, dead, _ = O.damp_hessian(Hp, wl.damp)
+    assert nd[0] == int(dead.sum())
+    Ur = O.inverse_cholesky_upper(Hd)
+    for W, (qp, sc, zr, _) in zip(Ws, res[0][4]):
+        Wn = W.float().cpu().numpy()
+        s_ref, z_ref = O.row_grid(Wn, 4)
+        assert np.array_equal(sc.cpu().numpy(), s_ref) and np.array_equal(zr.cpu().numpy(), z_ref)
+        codes = O.unpack_codes(qp.cpu().numpy().view(np.uint32), 4, W.shape[1])
+        Wh = (s_ref[:, None] * (codes - z_ref[:, None]).astype(np.float32)).astype(np.float64)
+        ref = O.gptq_quantize(Wn, Ur, s_ref, z_ref, 4, block=128, dead=dead)[1]
+        e_gpu = O.reconstruction_error(Wn, Wh, Hp)
+        e_ref = O.reconstruction_error(Wn, ref, Hp)
+        assert abs(e_gpu - e_ref) <= PT.TOL_RECON * e_ref, (e_gpu, e_ref)
+    del Xg, Ws, res
+    _free()
     # o_proj at 3 and 4 bits against the oracle (U from an 8192-token prefix), sampled rows
     o = by_name["o_proj"]
     Xo = S.activations(o.act, device="cpu", n_tok=8192).numpy()
@@ -223,9 +330,20 @@ def test_downproj28672_n65536():
     U, dm, nd = gptq.prepare(Hg, wl.damp)
     assert nd == act.n_dead
     _check_factor_tail(Xh, diag_full, U, dm, nd)
-    del U, Hg, Xh
+    del U, Hg
     _free()
-    Us = S.upper_factor(act.d_in, 28, device="cpu").numpy()
+    # the whole 28672-wide factor on the oracle's Hessian of an 8192-token prefix (the
+    # oracle's fp64 matrices take about 20 GB of host memory: skipped on a smaller host)
+    if _host_mem_available_gb() < 48:
+        pytest.skip("whole-factor check at d_in = 28672 needs ~48 GB of free host memory")
+    Xp = Xh[:8192].astype(np.float64)
+    del Xh
+    Hp = O.hessian(Xp)
+    del Xp
+    H32 = Hp.astype(np.float32)
+    del Hp
+    U32, dead_p, _ = _check_whole_factor(H32, wl.damp, O.inverse_cholesky_upper_reversed)
+    del H32
     W = S.layer_weights(layer, DEV)
     rows = np.sort(np.random.default_rng(4).choice(layer.d_out, 12, replace=False))
-    _quantize_and_check(W, Us, None, bits, rows)
+    _quantize_and_check(W, U32, dead_p, bits, rows)

@@ -88,12 +88,26 @@ def test_inverse_factor_identity_and_reversed_route(d, seed):
     assert np.allclose(np.tril(R, -1), 0)
     U2 = sla.solve_triangular(R, np.eye(d), lower=False)
     np.testing.assert_allclose(U, U2, rtol=0, atol=50 * cond * 1e-16 * np.abs(U).max())
+    # the oracle's own reversed route (used where inverting first is too slow on the host)
+    U3 = O.inverse_cholesky_upper_reversed(Hd)
+    assert np.all(np.tril(U3, -1) == 0)
+    np.testing.assert_allclose(U, U3, rtol=0, atol=50 * cond * 1e-16 * np.abs(U).max())
 
 
 def test_not_positive_definite_raises():
     H = np.array([[1.0, 2.0], [2.0, 1.0]])  # eigenvalues 3 and -1
     with pytest.raises(O.NotPositiveDefinite):
         O.inverse_cholesky_upper(H)
+    with pytest.raises(O.NotPositiveDefinite):
+        O.inverse_cholesky_upper_reversed(H)
+
+
+def test_reversed_route_worked_example_factor():
+    # the 2 x 2 factor of the worked example by hand: U = [[sqrt(3/8), -1/sqrt(6)],
+    # [0, 1/sqrt(3)]] ("tm_gptq_math", "A worked two-weight example")
+    U = O.inverse_cholesky_upper_reversed(np.array([[4.0, 2.0], [2.0, 3.0]]))
+    np.testing.assert_allclose(U, [[np.sqrt(3 / 8), -1 / np.sqrt(6)], [0.0, 1 / np.sqrt(3)]],
+                               rtol=0, atol=1e-15)
 
 
 # ---------------------------------------------------------------------------------------

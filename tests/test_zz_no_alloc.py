@@ -5,7 +5,9 @@ or code that must not trigger the synchronization an allocation or free can brin
 them the library offers a variant of gptq_quantize_layer that takes no workspace and
 runs on a fixed scratch array built into the library.  These tests call it through the C
 ABI, twice in a row on different layers, and check its outputs against the regular
-entry point's on the same inputs.  The file is named so pytest collects it last.
+entry point's on the same inputs; they also check that calls after the first leave the
+device's memory untouched, and that the status the call records on the device can be read
+back.  The file is named so pytest collects it last.
 """
 
 import ctypes
@@ -53,14 +55,18 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
-def _noalloc(W, U, dm, bits, block):
+def _noalloc(W, U, dm, bits, block, out=None):
     m, d = W.shape
-    qp, sc, zr, wh = _outputs(m, d, bits)
+    qp, sc, zr, wh = out if out is not None else _outputs(m, d, bits)
     st = gptq.gptq_quantize_layer_noalloc(_p(W), DT[W.dtype], m, d, W.stride(0), _p(U), _p(dm),
                                           bits, block, _p(qp), _p(sc), _p(zr), _p(wh),
                                           gptq._stream(None))
     assert st == 0, gptq.gptq_status_str(st)
     return qp, sc, zr, wh
+
+
+def _status():
+    return gptq.gptq_noalloc_status(gptq._stream(None))
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
@@ -79,6 +85,41 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     torch.cuda.synchronize()
     for a, b in zip(again, got[0]):
         assert torch.equal(a, b)
+
+
+def test_noalloc_allocates_nothing_after_the_first_call():
+    # eager (B = 1) and blocked sweeps, outputs allocated beforehand: after a warm-up call
+    # (which loads the scratch array) neither the device's free memory nor torch's
+    # allocator may move across further calls
+    W, U, dm = _layer(160, 200, "bf16", 21)
+    outs = {blk: _outputs(160, 200, 4) for blk in (1, 128)}
+    for blk in (1, 128):
+        _noalloc(W, U, dm, 4, blk, outs[blk])
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(2):
+        for blk in (1, 128):
+            _noalloc(W, U, dm, 4, blk, outs[blk])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert _status() == 0
+    for blk in (1, 128):
+        ref = gptq.quantize(W, U, 4, blk, dm)
+        torch.cuda.synchronize()
+        for a, b in zip(outs[blk], ref):
+            assert torch.equal(a, b)
+
+
+def test_noalloc_status_reports_nonfinite_weights():
+    W, U, dm = _layer(64, 128, "f32", 31)
+    W[5, 17] = float("nan")
+    _noalloc(W, U, dm, 4, 128)
+    assert _status() == 3          # GPTQ_ERR_NONFINITE
+    W[5, 17] = 0.0
+    _noalloc(W, U, dm, 4, 128)     # each call clears the status it records
+    assert _status() == 0
 
 
 def test_noalloc_rejects_layers_larger_than_its_scratch():
