@@ -415,7 +415,7 @@ def main():
     roofline["traffic"] = None
     roofline["traffic_note"] = ("not measured in this run: the DRAM bytes of an ncu capture "
                                 "are kept with the kernel's profile summary")
-    if st_q > st_h:
+    if block == 1:
         # the eager sweep dominates (B = 1): each column's update reads and writes the fp32
         # working copy of every later column once
         q_bytes = float(sum(m * (d - j - 1) * 8 for j in range(d)))

@@ -162,6 +162,12 @@ size_t gptq_prepare_workspace_bytes(int64_t d_in);
  *   ws         workspace of ws_bytes >= gptq_prepare_workspace_bytes(d_in).
  * SYNCHRONIZES `stream` before returning.  Errors: INVALID_ARG, WORKSPACE, NOT_PD (a
  * pivot <= 0: U is then undefined), NONFINITE (NaN/Inf in the part of H read), CUDA.
+ *
+ * Repeatability: the factorization runs on several streams of this library that add into
+ * shared blocks of the workspace in an order that is not fixed, so two calls on the same
+ * H can give U's that differ in their last bits (relative row differences of order 1e-6).
+ * A sweep on either gives the same codes except where a weight sits within rounding noise
+ * of a grid boundary (the two codes are then adjacent).
  */
 gptq_status gptq_prepare(float *H, int64_t d_in, float damp, float *U, uint8_t *dead_mask,
                          int32_t *n_dead, void *ws, size_t ws_bytes, gptq_stream_t stream);
@@ -387,6 +393,33 @@ gptq_status gptq_noalloc_status(gptq_stream_t stream);
  * GPTQ_ERR_TIMEOUT).  `ws` must be a workspace that call used.
  */
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream);
+
+/*
+ * gptq_debug_hessian_lost_stage: test hook of the bounded device waits (the pages have no
+ * counterpart; it exists so that the failure path of the tensor-core kernels can be tested
+ * without hanging a GPU).
+ *
+ * Runs the fp16/bf16 tensor-core Hessian exactly as gptq_hessian_accumulate with
+ * accumulate = 0 would, except that its TMA producer issues nothing for token stage
+ * `lost_stage` (stages are 64 tokens): no copy and no arrival, so the MMA issuer's wait for
+ * that stage can never complete.  Every wait of the launch gives up after `wait_ns`
+ * nanoseconds of the GPU's global timer, records GPTQ_ERR_TIMEOUT in the status block and
+ * returns; the CTA then leaves with no copy or tensor-core operation of its own in flight
+ * and its tensor memory freed, so the context stays usable.
+ *
+ *   X, xdtype, n_tok, d_in, ldx, H
+ *              as gptq_hessian_accumulate; xdtype GPTQ_F16 or GPTQ_BF16 with d_in >= 64
+ *              and n_tok >= 64 (else UNSUPPORTED).  H is left undefined.
+ *   lost_stage 0 <= lost_stage < ceil(n_tok / 64).
+ *   wait_ns    1e3 .. 1e10: budget of every wait (the regular calls use 2 s).
+ *   status_ws  DEVICE buffer of >= 256 bytes, 256-byte aligned, for the status block.
+ * SYNCHRONIZES `stream` and returns the device status: GPTQ_ERR_TIMEOUT when the waits ran
+ * out as designed.  Errors: INVALID_ARG, WORKSPACE, UNSUPPORTED, CUDA.
+ */
+gptq_status gptq_debug_hessian_lost_stage(const void *X, int xdtype, int64_t n_tok,
+                                          int64_t d_in, int64_t ldx, float *H,
+                                          int64_t lost_stage, uint64_t wait_ns, void *status_ws,
+                                          gptq_stream_t stream);
 
 #ifdef __cplusplus
 }

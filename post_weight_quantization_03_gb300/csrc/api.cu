@@ -267,6 +267,27 @@ gptq_status gptq_quantize_layer(const void *W, int wdtype, int64_t d_out, int64_
                                       qpacked, scale, zero, W_hat, ws, ws_bytes, stream, true);
 }
 
+gptq_status gptq_debug_hessian_lost_stage(const void *X, int xdtype, int64_t n_tok,
+                                          int64_t d_in, int64_t ldx, float *H,
+                                          int64_t lost_stage, uint64_t wait_ns, void *status_ws,
+                                          gptq_stream_t stream) {
+  const size_t es = elem_size(xdtype);
+  if (es == 0 || n_tok < 1 || d_in < 1 || ldx < d_in || !X || !H || !status_ws)
+    return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || (ldx * (int64_t)es) % 16 != 0 || !aligned(H, 16))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(status_ws, 256)) return GPTQ_ERR_WORKSPACE;
+  if (wait_ns < 1000 || wait_ns > 10000000000ull) return GPTQ_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  GPTQ_CUDA_CHECK(cudaMemsetAsync(status_ws, 0, sizeof(DevStatus), s));
+  GPTQ_TRY(launch_hessian_lost_stage(X, xdtype, n_tok, d_in, ldx, H, lost_stage, wait_ns,
+                                     (DevStatus *)status_ws, s));
+  DevStatus st;
+  GPTQ_CUDA_CHECK(cudaMemcpyAsync(&st, status_ws, sizeof(DevStatus), cudaMemcpyDeviceToHost, s));
+  GPTQ_CUDA_CHECK(cudaStreamSynchronize(s));
+  return (gptq_status)st.status;
+}
+
 gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream) {
   if (!ws || !aligned(ws, 256)) return GPTQ_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

@@ -50,6 +50,40 @@ gptq_status device_sm_count(int *out);
   } while (0)
 
 static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Programmatic dependent launch.  Kernels on the critical chains (factorization panels,
+// blocked sweep) start with pdl_launch_next() -- the next kernel on the stream may then be
+// launched and scheduled while this one runs -- and pdl_wait() -- which returns once the
+// previous kernel on the stream has completed and its writes are visible -- before any
+// global memory access.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kern` on `s`, with the programmatic-stream-serialization attribute when `pdl`
+// (the kernel must then begin with pdl_wait() before touching global memory); counts the
+// launch and maps a launch error to GPTQ_ERR_CUDA.
+template <typename... KArgs, typename... Args>
+gptq_status launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  count_launch();
+  if (cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GPTQ_ERR_CUDA;
+  }
+  return GPTQ_OK;
+}
 static inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Device-side status block at the start of every workspace.
@@ -91,6 +125,12 @@ __device__ __forceinline__ float tf32_head(float x) {
 // `st` (may be null) receives TIMEOUT if a bounded wait of the tensor-core kernel gives up.
 gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
                            float *H, int accumulate, DevStatus *st, cudaStream_t s);
+
+// Test hook of the bounded waits: the fp16/bf16 tensor-core Hessian with its producer
+// skipping token stage `lost_stage` (no copy, no arrival) and every wait limited to wait_ns.
+gptq_status launch_hessian_lost_stage(const void *X, int xdtype, int64_t n_tok, int64_t d,
+                                      int64_t ldx, float *H, int64_t lost_stage,
+                                      uint64_t wait_ns, DevStatus *st, cudaStream_t s);
 
 // host_stream.cu: X streamed from host memory in chunks (see gptq_hessian_accumulate_host)
 size_t hessian_host_ws_bytes(int64_t d, size_t es, int64_t chunk_tok);

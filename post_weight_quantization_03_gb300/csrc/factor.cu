@@ -165,9 +165,9 @@ reverse_lower_kernel(float *H, int64_t d, float *Yt, DevStatus *st) {
 // with the inverse built alongside in transposed form (Bt = right-hand side of L Y = I,
 // transposed, which becomes Yt = Linv^T), exactly like the panel loop of the whole
 // factorization:
-//   leaf   : one warp factors the PW x PW tile (lane i holds row i; the next pivot is
-//            issued before the current column's updates) and writes the scaled transpose
-//            M[j][i] = L_ij / L_jj and the reciprocal pivots rd
+//   leaf   : one warp factors the PW x PW tile (lane i holds row i; four columns per
+//            step, each lane factoring the step's 4 x 4 diagonal block itself) and writes the
+//            scaled transpose M[j][i] = L_ij / L_jj and the reciprocal pivots rd
 //   phase 1: L_ip  L_pp^T = A_ip                  rows i >= R0      (trsm)
 //            Yt_cp L_pp^T = Bt_cp                  rows c <  R0      (inverse, step a)
 //            one thread per row, forward substitution against M
@@ -194,48 +194,87 @@ constexpr size_t kPotrfSmemUsed = (2 * NB * PL + PW * PL + PW) * sizeof(float);
 constexpr size_t kPotrfSmem = 200 * 1024;
 static_assert(kPotrfSmemUsed <= kPotrfSmem, "potrf shared memory");
 
-// Column J of the leaf, rl = 1/sqrt(pivot J) already known.  Lane i holds row i of the
-// tile in a[] and its running diagonal in dg.  The updates run on every lane and every
-// later column: what lands above the diagonal is never read and is cleared at the end.
-template <int J>
-struct LeafCol {
-  static __device__ __forceinline__ void run(float (&a)[PW], float &dg, float rl, float &rdl,
-                                             float *cb, float *M, int lane) {
-    if (lane == J) rdl = rl;
-    const float lij = (lane == J ? dg : a[J]) * rl;  // L[i][J]
-    a[J] = lij;
-    dg = fmaf(-lij, lij, dg);
-    float rn = 0.0f;
-    if (J + 1 < PW) {                                // next pivot, off the update path
-      const float pn = __shfl_sync(0xffffffffu, dg, J + 1);
-      rn = pn > 0.0f ? rsqrtf(pn) : 0.0f;
+// Columns JB .. JB + 3 of the leaf at once.  Lane i holds row i of the tile in a[] (its
+// diagonal entry included, updated like the others).  Every lane takes the block's 4 x 4
+// lower part from lanes JB .. JB + 3 by shuffles and factors it itself (the same values in
+// every lane), then solves its own row against it, L[i][JB + c] = x_c, and subtracts the
+// rank-4 product of the block's columns from its later entries, with the rows' x exchanged
+// through shared memory (two buffers by block parity).  Per entry the operations and their
+// order are those of eliminating the four columns one after another.  What lands above the
+// diagonal is never read and is cleared at the end.
+template <int JB>
+struct LeafBlock {
+  static __device__ __forceinline__ void run(float (&a)[PW], float &rdl, float4 *xb, float *M,
+                                             int lane) {
+    constexpr unsigned F = 0xffffffffu;
+    const float b00 = __shfl_sync(F, a[JB], JB);
+    const float b10 = __shfl_sync(F, a[JB], JB + 1), b11 = __shfl_sync(F, a[JB + 1], JB + 1);
+    const float b20 = __shfl_sync(F, a[JB], JB + 2), b21 = __shfl_sync(F, a[JB + 1], JB + 2);
+    const float b22 = __shfl_sync(F, a[JB + 2], JB + 2);
+    const float b30 = __shfl_sync(F, a[JB], JB + 3), b31 = __shfl_sync(F, a[JB + 1], JB + 3);
+    const float b32 = __shfl_sync(F, a[JB + 2], JB + 3), b33 = __shfl_sync(F, a[JB + 3], JB + 3);
+    // the block's factor; a failed pivot leaves r = 0
+    const float r0 = b00 > 0.0f ? rsqrtf(b00) : 0.0f;
+    const float l10 = b10 * r0, l20 = b20 * r0, l30 = b30 * r0;
+    const float t11 = fmaf(-l10, l10, b11);
+    const float r1 = t11 > 0.0f ? rsqrtf(t11) : 0.0f;
+    const float l21 = fmaf(-l20, l10, b21) * r1, l31 = fmaf(-l30, l10, b31) * r1;
+    const float t22 = fmaf(-l21, l21, fmaf(-l20, l20, b22));
+    const float r2 = t22 > 0.0f ? rsqrtf(t22) : 0.0f;
+    const float l32 = fmaf(-l31, l21, fmaf(-l30, l20, b32)) * r2;
+    const float t33 = fmaf(-l32, l32, fmaf(-l31, l31, fmaf(-l30, l30, b33)));
+    const float r3 = t33 > 0.0f ? rsqrtf(t33) : 0.0f;
+    // this lane's row in the block's columns
+    const int rr = lane - JB;
+    float x0 = 0.0f, x1 = 0.0f, x2 = 0.0f, x3 = 0.0f;
+    if (rr >= 4) {
+      x0 = a[JB] * r0;
+      x1 = fmaf(-x0, l10, a[JB + 1]) * r1;
+      x2 = fmaf(-x1, l21, fmaf(-x0, l20, a[JB + 2])) * r2;
+      x3 = fmaf(-x2, l32, fmaf(-x1, l31, fmaf(-x0, l30, a[JB + 3]))) * r3;
+    } else if (rr == 0) {
+      x0 = b00 * r0;
+      rdl = r0;
+    } else if (rr == 1) {
+      x0 = l10; x1 = t11 * r1;
+      rdl = r1;
+    } else if (rr == 2) {
+      x0 = l20; x1 = l21; x2 = t22 * r2;
+      rdl = r2;
+    } else if (rr == 3) {
+      x0 = l30; x1 = l31; x2 = l32; x3 = t33 * r3;
+      rdl = r3;
     }
-    M[J * PL + lane] = lij * rl;                     // L[i][J] / L[J][J]
-    if (J + 1 < PW) {
-      float *c = cb + (J & 1) * 32;
-      c[lane] = lij;
+    M[(JB + 0) * PL + lane] = x0 * r0;   // L[i][j] / L[j][j]
+    M[(JB + 1) * PL + lane] = x1 * r1;
+    M[(JB + 2) * PL + lane] = x2 * r2;
+    M[(JB + 3) * PL + lane] = x3 * r3;
+    a[JB] = x0; a[JB + 1] = x1; a[JB + 2] = x2; a[JB + 3] = x3;
+    if (JB + 4 < PW) {
+      float4 *xs = xb + ((JB / 4) & 1) * 32;
+      xs[lane] = make_float4(x0, x1, x2, x3);
       __syncwarp();
 #pragma unroll
-      for (int l4 = (J + 1) / 4; l4 < PW / 4; ++l4) {
-        const float4 v = *reinterpret_cast<const float4 *>(c + 4 * l4);
-        if (4 * l4 + 0 > J) a[4 * l4 + 0] = fmaf(-lij, v.x, a[4 * l4 + 0]);
-        if (4 * l4 + 1 > J) a[4 * l4 + 1] = fmaf(-lij, v.y, a[4 * l4 + 1]);
-        if (4 * l4 + 2 > J) a[4 * l4 + 2] = fmaf(-lij, v.z, a[4 * l4 + 2]);
-        if (4 * l4 + 3 > J) a[4 * l4 + 3] = fmaf(-lij, v.w, a[4 * l4 + 3]);
+      for (int k = JB + 4; k < PW; ++k) {
+        const float4 v = xs[k];          // L[k][JB .. JB + 3]
+        a[k] = fmaf(-x0, v.x, a[k]);
+        a[k] = fmaf(-x1, v.y, a[k]);
+        a[k] = fmaf(-x2, v.z, a[k]);
+        a[k] = fmaf(-x3, v.w, a[k]);
       }
     }
-    LeafCol<J + 1>::run(a, dg, rn, rdl, cb, M, lane);
+    LeafBlock<JB + 4>::run(a, rdl, xb, M, lane);
   }
 };
 template <>
-struct LeafCol<PW> {
-  static __device__ __forceinline__ void run(float (&)[PW], float &, float, float &, float *,
-                                             float *, int) {}
+struct LeafBlock<PW> {
+  static __device__ __forceinline__ void run(float (&)[PW], float &, float4 *, float *, int) {}
 };
+static_assert(PW % 4 == 0, "the leaf eliminates four columns at a time");
 
 // Factor the PW x PW tile at (t0, t0) of S in place (lower part; lanes >= PW carry zeros).
 // Returns the first column with a non-positive (or NaN) pivot, or -1.
-__device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float *cb, int t0,
+__device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float4 *xb, int t0,
                                            int lane) {
   const bool own = lane < PW;
   float *row = S + (t0 + (own ? lane : 0)) * PL + t0;
@@ -248,10 +287,8 @@ __device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float 
 #pragma unroll
   for (int l = 0; l < PW; ++l)
     if (l > lane || !own) a[l] = 0.0f;
-  float dg = own ? row[lane] : 1.0f;
-  const float p0 = __shfl_sync(0xffffffffu, dg, 0);
   float rdl = 0.0f;
-  LeafCol<0>::run(a, dg, p0 > 0.0f ? rsqrtf(p0) : 0.0f, rdl, cb, M, lane);
+  LeafBlock<0>::run(a, rdl, xb, M, lane);
   if (own) {
 #pragma unroll
     for (int q = 0; q < PW / 4; ++q)
@@ -260,7 +297,7 @@ __device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float 
                       4 * q + 2 <= lane ? a[4 * q + 2] : 0.0f, 4 * q + 3 <= lane ? a[4 * q + 3] : 0.0f);
     rd[lane] = rdl;
   }
-  // a failed pivot left rl = 0 in its lane
+  // a failed pivot left r = 0 in its lane
   const unsigned badm = __ballot_sync(0xffffffffu, own && !(rdl > 0.0f));
   return badm ? t0 + __ffs((int)badm) - 1 : -1;
 }
@@ -359,9 +396,11 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
   float *Bt = psm + NB * PL;     // NB x PL: transposed right-hand side -> Linv^T
   float *M = Bt + NB * PL;       // PW x PL: scaled transpose of the current leaf
   float *rd = M + PW * PL;       // PW reciprocal pivots of the current leaf
-  __shared__ __align__(16) float cb[64];
+  __shared__ __align__(16) float4 cb[64];   // the leaf's row exchange (two buffers)
   __shared__ int s_skip, s_bad;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  pdl_launch_next();
+  pdl_wait();
   if (tid == 0) { s_skip = st->status != 0; s_bad = -1; }
   __syncthreads();
   if (s_skip) return;
@@ -509,6 +548,8 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
   extern __shared__ __align__(16) float sm[];
   float *Bs = sm;                    // 32 NCQ x LD: the CTA's Bm rows (output columns, K)
   float *Is = sm + 32 * NCQ * LD;    // RM_ROWS x LD: the CTA's input rows
+  pdl_launch_next();
+  pdl_wait();
   if (st->status != 0) return;
   const int kz = KS > 1 ? KC * (int)blockIdx.z : 0;   // first K of the chunk
   const int tid = threadIdx.x;
@@ -791,8 +832,8 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
     if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->eb[par], 0));
-    potrf_kernel<<<1, PF_THREADS, potrf_smem, c>>>(A, d, k0, n, w.Linv[par], w.st);
-    GPTQ_LAUNCH_CHECK();
+    GPTQ_TRY(launch_kernel(potrf_kernel, 1, PF_THREADS, potrf_smem, c, true, A, d, k0, n,
+                           w.Linv[par], w.st));
     if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->ep[par], c));
     // the previous column update's rows below the diagonal block (second critical stream)
     if (overlap && next_rest) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->en[par ^ 1], 0));
@@ -800,50 +841,51 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     if (k1 < d) {
       const int nn = (int)std::min<int64_t>(NB, d - k1);
       // trsm: rows [r0, r1) of panel k -> L panel (hi/lo)
+      // programmatic early launch only on the critical stream (its kernels are small); on
+      // the other streams CTAs waiting for their predecessor would hold SMs
       auto trsm = [&](int64_t r0, int64_t r1, cudaStream_t st) {
         dim3 g((unsigned)ceil_div(r1 - r0, RM_ROWS), 4);
-        rowmul_kernel<1><<<g, RM_THREADS, rmq_smem, st>>>(A + k0, nullptr, d, nullptr, 0, r0, r1,
-                                                         w.Linv[par], nullptr, NB, n, n, 0,
-                                                         w.Lhi[par], w.Llo[par], w.st);
+        return launch_kernel(rowmul_kernel<1>, g, RM_THREADS, rmq_smem, st, st == c, A + k0,
+                             (const float *)nullptr, d, (float *)nullptr, (int64_t)0, r0, r1,
+                             w.Linv[par], (const float *)nullptr, (int64_t)NB, n, n, 0,
+                             w.Lhi[par], w.Llo[par], w.st);
       };
       // next panel column, rows k1 + [r0, r1): A[., k1:k1+NB] -= L[.] L[k1:k1+NB]^T (fp32
       // from the head + tail panels; atomic adds: the side stream's previous trailing update
       // adds here too)
       auto next_col = [&](int64_t r0, int64_t r1, cudaStream_t st) {
         dim3 g2((unsigned)ceil_div(r1 - r0, RM_ROWS), (unsigned)ceil_div(nn, 32));
-        rowmul_kernel<1><<<g2, RM_THREADS, rmq_smem, st>>>(
-            w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, r0, r1,
-            w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
+        return launch_kernel(rowmul_kernel<1>, g2, RM_THREADS, rmq_smem, st, st == c,
+                             w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
+                             A + k1 * d + k1, d, r0, r1, w.Lhi[par] + k1 * NB,
+                             w.Llo[par] + k1 * NB, (int64_t)NB, n, nn, 1, (float *)nullptr,
+                             (float *)nullptr, w.st);
       };
       if (overlap && d - k1 > nn) {
         cudaStream_t c2 = ss->crit2;
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c2, ss->ep[par], 0));
-        trsm(k1 + nn, d, c2);                     // the rows below, beside the chain
-        GPTQ_LAUNCH_CHECK();
+        GPTQ_TRY(trsm(k1 + nn, d, c2));           // the rows below, beside the chain
         GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c2));
-        trsm(k1, k1 + nn, c);                     // the next potrf's rows
-        GPTQ_LAUNCH_CHECK();
+        GPTQ_TRY(trsm(k1, k1 + nn, c));           // the next potrf's rows
         GPTQ_CUDA_CHECK(cudaEventRecord(ss->ed[par], c));
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c2, ss->ed[par], 0));
-        next_col(nn, d - k1, c2);                 // beside the next potrf
-        GPTQ_LAUNCH_CHECK();
+        GPTQ_TRY(next_col(nn, d - k1, c2));       // beside the next potrf
         GPTQ_CUDA_CHECK(cudaEventRecord(ss->en[par], c2));
         next_rest = true;
         {
           // the next potrf's block, in four K chunks (64 CTAs; atomic adds)
           dim3 g2((unsigned)ceil_div(nn, RM_ROWS), (unsigned)ceil_div(nn, 32), 4);
-          rowmul_kernel<1, 4><<<g2, RM_THREADS, rmk_smem, c>>>(
-              w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, A + k1 * d + k1, d, 0, nn,
-              w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, NB, n, nn, 1, nullptr, nullptr, w.st);
-          GPTQ_LAUNCH_CHECK();
+          GPTQ_TRY(launch_kernel(rowmul_kernel<1, 4>, g2, RM_THREADS, rmk_smem, c, true,
+                                 w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
+                                 A + k1 * d + k1, d, (int64_t)0, (int64_t)nn,
+                                 w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB, n, nn,
+                                 1, (float *)nullptr, (float *)nullptr, w.st));
         }
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ed[par], 0));
       } else {
-        trsm(k1, d, c);
-        GPTQ_LAUNCH_CHECK();
-        next_col(0, d - k1, c);
-        GPTQ_LAUNCH_CHECK();
+        GPTQ_TRY(trsm(k1, d, c));
+        GPTQ_TRY(next_col(0, d - k1, c));
         if (overlap) {
           GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c));
           GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
@@ -856,10 +898,10 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     // inverse step a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
     {
       const unsigned g = (unsigned)ceil_div(k1, RM_ROWS);
-      rowmul_kernel<4><<<g, RM_THREADS, rm_smem, b>>>(w.Yt + k0, nullptr, d, w.Yt + k0, d, 0,
-                                                      k1, w.Linv[par], nullptr, NB, n, n, 0,
-                                                      w.Yhi, w.Ylo, w.st);
-      GPTQ_LAUNCH_CHECK();
+      GPTQ_TRY(launch_kernel(rowmul_kernel<4>, g, RM_THREADS, rm_smem, b, false,
+                             (const float *)(w.Yt + k0), (const float *)nullptr, d, w.Yt + k0, d,
+                             (int64_t)0, k1, (const float *)w.Linv[par], (const float *)nullptr,
+                             (int64_t)NB, n, n, 0, w.Yhi, w.Ylo, w.st));
     }
     if (k1 < d) {
       if (d - k1 > NB) {

@@ -8,7 +8,9 @@
 // fp16/bf16 inputs run on the tcgen05 tensor cores (kind::f16, fp32 accumulation in
 // TMEM): the products of two 16-bit values are exact in fp32, and the accumulator is
 // drained into fp32 registers every kSegTokens tokens so that no truncating tensor-core
-// running sum spans more than one segment.  fp32 inputs (and tiny shapes) take a CUDA-core kernel.
+// running sum spans more than one segment.  fp32 inputs run on the tensor cores too, as
+// kind::tf32 products of TF32 head/tail splits (3xTF32); tiny shapes take a CUDA-core
+// kernel.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -97,6 +99,8 @@ hessian_simt_kernel(const T *__restrict__ X, int64_t n_tok, int64_t d, int64_t l
 //   warp 0      : TMA producer, 64 tokens per stage (2 + 4 boxes of 64 ch x 64 tok)
 //   warp 1      : TMEM allocator (2 x 256 columns) + MMA issuer
 //   warps 2..9  : drain TMEM segments into fp32 registers, then write H and its mirror
+// All CTAs of a wave walk the tokens in the same order, so each chunk of X is fetched from
+// HBM about once per wave and served to the other tiles from L2.
 // ---------------------------------------------------------------------------------------
 constexpr int TB_M = 128, TB_N = 256, TB_K = 64;
 constexpr int T_STAGES = 4;
@@ -114,6 +118,8 @@ struct HessTcParams {
   int seg_stages;     // stages (of 64 tokens) per accumulation segment
   float *H;
   int accumulate;
+  uint64_t wait_ns;   // budget of every mbarrier wait
+  int lost_stage;     // test hook: the producer issues nothing for this stage (-1: none)
 };
 
 template <int FMT>  // 0 = fp16, 1 = bf16
@@ -163,7 +169,10 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
     tc::tma_prefetch_desc(&mx);
     for (int g = 0; g < total; ++g) {
       const int s = g % T_STAGES;
-      if (g >= T_STAGES && !tc::mbar_wait(&empty[s], ((g / T_STAGES) - 1) & 1, st)) break;
+      if (g >= T_STAGES &&
+          !tc::mbar_wait(&empty[s], ((g / T_STAGES) - 1) & 1, st, p.wait_ns))
+        break;
+      if (g == p.lost_stage) continue;   // test hook: no copy and no arrival for this stage
       uint8_t *a = smem + s * T_STAGE;
       uint8_t *b = a + T_TILE_A;
       const int32_t t0 = g * TB_K;
@@ -181,7 +190,7 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
     for (int sg = 0; sg < nseg && ok; ++sg) {
       const int buf = sg & 1;
       if (sg >= 2) {
-        ok = tc::mbar_wait(&tempty[buf], ((sg / 2) - 1) & 1, st);
+        ok = tc::mbar_wait(&tempty[buf], ((sg / 2) - 1) & 1, st, p.wait_ns);
         if (!ok) break;
         tc::tc_fence_after();
       }
@@ -189,7 +198,7 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
       const int gend = min(total, (sg + 1) * p.seg_stages);
       for (int first = 1; g < gend; ++g, first = 0) {
         const int s = g % T_STAGES;
-        ok = tc::mbar_wait(&full[s], (g / T_STAGES) & 1, st);
+        ok = tc::mbar_wait(&full[s], (g / T_STAGES) & 1, st, p.wait_ns);
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t a = tc::smem_u32(smem + s * T_STAGE);
@@ -202,7 +211,7 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
         }
         tc::mma_commit(&empty[s]);
       }
-      tc::mma_commit(&tfull[buf]);
+      tc::mma_commit(&tfull[buf]);   // segment complete (or abandoned after a timeout)
     }
   } else if (warp >= 2) {
     const int e = warp - 2, q = warp & 3, h = e / 4;
@@ -213,7 +222,7 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
     for (int sg = 0; sg < nseg && ok; ++sg) {
       const int buf = sg & 1;
       int okl = 0;
-      if (lane == 0) okl = tc::mbar_wait(&tfull[buf], (sg / 2) & 1, st) ? 1 : 0;
+      if (lane == 0) okl = tc::mbar_wait(&tfull[buf], (sg / 2) & 1, st, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
       __syncwarp();
       if (!ok) break;
@@ -251,6 +260,225 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------------------------------
+// fp32 inputs on the tensor cores: tcgen05 kind::tf32 in the 3xTF32 scheme.  One CTA per
+// 128 x 128 tile of H on or below the diagonal.  Per stage, 32 tokens of the tile's two
+// channel ranges arrive by TMA as token-major boxes (channels contiguous, 128-byte
+// swizzle); four converter warps transpose them into the K-major layout the MMA reads
+// (rows = channels, 32 tokens = one 128-byte swizzled row) while splitting every element
+// into its TF32 head (low 13 mantissa bits cleared) and the exact remainder; the MMA warp
+// accumulates head head^T + head tail^T + tail head^T, which reproduces the fp32 products
+// to about 2^-21 relative.
+//   warp 0      : TMA producer (raw ring of F_RAW stages)
+//   warp 1      : TMEM allocator (2 x 128 columns) + MMA issuer (converted ring of F_CONV)
+//   warps 2..5  : drain the accumulator every kSegTokensTf32 tokens into fp32 registers,
+//                 then write H and its mirror
+//   warps 6..9  : transpose + head/tail split, raw stage -> converted stage
+// ---------------------------------------------------------------------------------------
+constexpr int F_M = 128, F_K = 32;               // tile edge (channels), tokens per stage
+constexpr int F_RAW = 2, F_CONV = 2;
+constexpr uint32_t F_BOX = 32 * F_K * 4;         // 32 channels x 32 tokens of fp32: 4 KB
+constexpr uint32_t F_TILE = F_M * F_K * 4;       // 128 channels x 32 tokens: 16 KB
+constexpr uint32_t F_RAW_STAGE = 2 * F_TILE;     // the two channel ranges, token-major
+constexpr uint32_t F_CONV_STAGE = 4 * F_TILE;    // A, B heads then A, B tails, K-major
+constexpr int F_CONV_WARPS = 4;
+constexpr int F_THREADS = 64 + 32 * 4 + 32 * F_CONV_WARPS;   // 320
+constexpr size_t F_SMEM = 1024 + F_RAW * F_RAW_STAGE + F_CONV * F_CONV_STAGE + 256;
+
+struct HessF32Params {
+  int64_t d, n_tok;
+  int seg_stages;     // stages (of F_K tokens) per accumulation segment
+  float *H;
+  int accumulate;
+};
+
+__global__ void __launch_bounds__(F_THREADS, 1)
+hessian_tf32_kernel(const __grid_constant__ CUtensorMap mx, HessF32Params p, DevStatus *st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *raw = smem;                                   // F_RAW x F_RAW_STAGE
+  uint8_t *cvt = smem + F_RAW * F_RAW_STAGE;             // F_CONV x F_CONV_STAGE
+  uint64_t *rfull = (uint64_t *)(cvt + F_CONV * F_CONV_STAGE);
+  uint64_t *rempty = rfull + F_RAW;     // raw stage read by all converter warps
+  uint64_t *cfull = rempty + F_RAW;     // converted stage written by all converter warps
+  uint64_t *cempty = cfull + F_CONV;    // converted stage consumed by the MMAs
+  uint64_t *tfull = cempty + F_CONV;    // [2]: accumulator buffer ready to drain
+  uint64_t *tempty = tfull + 2;         // [2]: accumulator buffer drained
+  uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  int ti, tj;
+  lower_tile(blockIdx.x, ti, tj);
+  const int64_t m0 = (int64_t)ti * F_M, n0 = (int64_t)tj * F_M;
+  const int total = (int)((p.n_tok + F_K - 1) / F_K);
+  const int nseg = (total + p.seg_stages - 1) / p.seg_stages;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < F_RAW; ++s) {
+      tc::mbar_init(&rfull[s], 1);
+      tc::mbar_init(&rempty[s], F_CONV_WARPS);
+    }
+    for (int s = 0; s < F_CONV; ++s) {
+      tc::mbar_init(&cfull[s], F_CONV_WARPS);
+      tc::mbar_init(&cempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 4);
+    }
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * F_M);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&mx);
+      for (int g = 0; g < total; ++g) {
+        const int s = g % F_RAW;
+        if (g >= F_RAW && !tc::mbar_wait(&rempty[s], ((g / F_RAW) - 1) & 1, st)) break;
+        uint8_t *a = raw + s * F_RAW_STAGE;
+        const int32_t t0 = g * F_K;
+        tc::mbar_arrive_expect_tx(&rfull[s], F_RAW_STAGE);
+#pragma unroll
+        for (int q = 0; q < F_M / 32; ++q) {
+          tc::tma_load_2d(a + q * F_BOX, &mx, (int32_t)m0 + 32 * q, t0, &rfull[s]);
+          tc::tma_load_2d(a + F_TILE + q * F_BOX, &mx, (int32_t)n0 + 32 * q, t0, &rfull[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::instr_desc(2, 2, F_M, F_M, 0, 0);
+      int g = 0;
+      bool ok = true;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+        const int buf = sg & 1;
+        if (sg >= 2) {
+          ok = tc::mbar_wait(&tempty[buf], ((sg / 2) - 1) & 1, st);
+          if (!ok) break;
+          tc::tc_fence_after();
+        }
+        const uint32_t dt = tmem + (uint32_t)(buf * F_M);
+        const int gend = min(total, (sg + 1) * p.seg_stages);
+        for (int first = 1; g < gend; ++g, first = 0) {
+          const int s = g % F_CONV;
+          ok = tc::mbar_wait(&cfull[s], (g / F_CONV) & 1, st);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t ah = tc::smem_u32(cvt + s * F_CONV_STAGE);
+          const uint32_t bh = ah + F_TILE, al = ah + 2 * F_TILE, bl = ah + 3 * F_TILE;
+#pragma unroll
+          for (int kk = 0; kk < F_K / 8; ++kk) {   // 8 tf32 = 32 bytes of each row per MMA
+            const uint32_t off = kk * 32;
+            const uint64_t dah = tc::smem_desc_sw128(ah + off, 16, 1024);
+            const uint64_t dbh = tc::smem_desc_sw128(bh + off, 16, 1024);
+            const uint64_t dal = tc::smem_desc_sw128(al + off, 16, 1024);
+            const uint64_t dbl = tc::smem_desc_sw128(bl + off, 16, 1024);
+            tc::mma_tf32(dt, dah, dbh, idesc, (first && kk == 0) ? 0u : 1u);
+            tc::mma_tf32(dt, dah, dbl, idesc, 1u);
+            tc::mma_tf32(dt, dal, dbh, idesc, 1u);
+          }
+          tc::mma_commit(&cempty[s]);
+        }
+        tc::mma_commit(&tfull[buf]);
+      }
+    }
+  } else if (warp >= 6) {
+    // Raw stage: per channel range, four boxes of 32 channels; in box q token t's 128-byte
+    // row holds its 32 channels with 16-byte chunk c stored at chunk c ^ (t % 8).  Output:
+    // per channel r a 128-byte row of 32 tokens, chunk c (tokens 4c .. 4c + 3) stored at
+    // chunk c ^ (r % 8) -- the layout a K-major 128-byte-swizzled TMA box has.
+    const int ct = threadIdx.x - 32 * 6;
+    for (int g = 0; g < total; ++g) {
+      const int rs = g % F_RAW, cs = g % F_CONV;
+      int okl = 0;
+      if (lane == 0)
+        okl = tc::mbar_wait(&rfull[rs], (g / F_RAW) & 1, st) &&
+              (g < F_CONV || tc::mbar_wait(&cempty[cs], ((g / F_CONV) - 1) & 1, st));
+      if (!__shfl_sync(0xffffffffu, okl, 0)) break;
+      const uint8_t *rb = raw + rs * F_RAW_STAGE;
+      uint8_t *cb = cvt + cs * F_CONV_STAGE;
+#pragma unroll 4
+      for (int i = 0; i < 2 * F_M * (F_K / 4) / (32 * F_CONV_WARPS); ++i) {
+        const int idx = i * 32 * F_CONV_WARPS + ct;    // (tile, chunk, row), row fastest
+        const int tile = idx / (F_M * (F_K / 4));
+        const int rem = idx % (F_M * (F_K / 4));
+        const int c = rem / F_M, r = rem % F_M;
+        const uint8_t *box = rb + tile * F_TILE + (r / 32) * F_BOX;
+        const int rc = r % 32;
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int t = 4 * c + j;
+          v[j] = *reinterpret_cast<const float *>(box + t * 128 + (((rc / 4) ^ (t & 7)) * 16) +
+                                                  (rc % 4) * 4);
+        }
+        const float4 h = make_float4(tf32_head(v[0]), tf32_head(v[1]), tf32_head(v[2]),
+                                     tf32_head(v[3]));
+        const uint32_t o = tile * F_TILE + r * 128 + ((c ^ (r & 7)) * 16);
+        *reinterpret_cast<float4 *>(cb + o) = h;
+        *reinterpret_cast<float4 *>(cb + 2 * F_TILE + o) =
+            make_float4(v[0] - h.x, v[1] - h.y, v[2] - h.z, v[3] - h.w);
+      }
+      tc::fence_proxy_async_smem();   // the tensor core reads these through the async proxy
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(&rempty[rs]);
+        tc::mbar_arrive(&cfull[cs]);
+      }
+    }
+  } else {
+    // warps 2..5: drain and write
+    const int q = warp & 3;
+    float acc[F_M];
+#pragma unroll
+    for (int i = 0; i < F_M; ++i) acc[i] = 0.f;
+    bool ok = true;
+    for (int sg = 0; sg < nseg && ok; ++sg) {
+      const int buf = sg & 1;
+      int okl = 0;
+      if (lane == 0) okl = tc::mbar_wait(&tfull[buf], (sg / 2) & 1, st) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+      __syncwarp();
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * F_M);
+#pragma unroll
+      for (int c = 0; c < F_M / 32; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(base + (uint32_t)(c * 32), r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c * 32 + i] += __uint_as_float(r[i]);
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+    }
+    const int64_t r = m0 + q * 32 + lane;
+    const int64_t d = p.d;
+    if (ok && r < d) {
+#pragma unroll
+      for (int i = 0; i < F_M; ++i) {
+        const int64_t c = n0 + i;
+        if (c < d && c <= r) {
+          float v = 2.0f * acc[i];
+          if (p.accumulate) v += p.H[r * d + c];
+          p.H[r * d + c] = v;
+          if (c != r) p.H[c * d + r] = v;
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * F_M);
+}
+
 __global__ void zero_kernel(float *p, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -262,9 +490,14 @@ __global__ void zero_kernel(float *p, int64_t n) {
 // summed in TMEM (measured: ~2e-5 after 256 MMAs of 16 tokens); 512 tokens (32 MMAs) keep
 // it near 2e-6, and the segments are summed in round-to-nearest fp32 registers.
 constexpr int kSegTokens = 512;
+// The 3xTF32 kernel issues 12 MMAs per 32 tokens (three products of four 8-wide steps), so
+// its segments are shorter: 64 tokens, 24 MMAs per TMEM running sum (512-token segments,
+// 192 MMAs, left H about 1e-5 low).
+constexpr int kSegTokensTf32 = 64;
 
 gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t d, int64_t ldx,
-                              float *H, int accumulate, DevStatus *st, cudaStream_t s) {
+                              float *H, int accumulate, DevStatus *st, cudaStream_t s,
+                              uint64_t wait_ns = tc::kWaitNs, int lost_stage = -1) {
   GPTQ_TRY(ensure_smem_attr((const void *)hessian_tc_kernel<0>, (int)T_SMEM));
   GPTQ_TRY(ensure_smem_attr((const void *)hessian_tc_kernel<1>, (int)T_SMEM));
   CUtensorMap mx;
@@ -278,6 +511,8 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
   p.seg_stages = kSegTokens / TB_K;
   p.H = H;
   p.accumulate = accumulate;
+  p.wait_ns = wait_ns;
+  p.lost_stage = lost_stage;
   const int ncb = (int)ceil_div(d, TB_N);
   int64_t tiles = 0;
   for (int j = 0; j < ncb; ++j) tiles += std::max(0, p.n_row_blocks - 2 * j);
@@ -285,6 +520,24 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
     hessian_tc_kernel<0><<<(unsigned)tiles, T_THREADS, T_SMEM, s>>>(mx, p, st);
   else
     hessian_tc_kernel<1><<<(unsigned)tiles, T_THREADS, T_SMEM, s>>>(mx, p, st);
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+gptq_status launch_hessian_tf32(const void *X, int64_t n_tok, int64_t d, int64_t ldx, float *H,
+                                int accumulate, DevStatus *st, cudaStream_t s) {
+  GPTQ_TRY(ensure_smem_attr((const void *)hessian_tf32_kernel, (int)F_SMEM));
+  CUtensorMap mx;
+  if (!tc::make_tmap_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, X, n_tok, d, ldx * 4, 32, F_K))
+    return GPTQ_ERR_UNSUPPORTED;
+  HessF32Params p{};
+  p.d = d;
+  p.n_tok = n_tok;
+  p.seg_stages = kSegTokensTf32 / F_K;
+  p.H = H;
+  p.accumulate = accumulate;
+  const int64_t nb = ceil_div(d, F_M);
+  hessian_tf32_kernel<<<(unsigned)(nb * (nb + 1) / 2), F_THREADS, F_SMEM, s>>>(mx, p, st);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
@@ -302,6 +555,10 @@ gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, 
   }
   if ((xdtype == GPTQ_F16 || xdtype == GPTQ_BF16) && d >= 64 && n_tok >= 64) {
     const gptq_status t = launch_hessian_tc(X, xdtype, n_tok, d, ldx, H, accumulate, st, s);
+    if (t != GPTQ_ERR_UNSUPPORTED) return t;
+  }
+  if (xdtype == GPTQ_F32 && d >= 32 && n_tok >= 32) {
+    const gptq_status t = launch_hessian_tf32(X, n_tok, d, ldx, H, accumulate, st, s);
     if (t != GPTQ_ERR_UNSUPPORTED) return t;
   }
   const int64_t nt = ceil_div(d, HT);
@@ -324,6 +581,15 @@ gptq_status launch_hessian(const void *X, int xdtype, int64_t n_tok, int64_t d, 
   }
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
+}
+
+gptq_status launch_hessian_lost_stage(const void *X, int xdtype, int64_t n_tok, int64_t d,
+                                      int64_t ldx, float *H, int64_t lost_stage,
+                                      uint64_t wait_ns, DevStatus *st, cudaStream_t s) {
+  if (!((xdtype == GPTQ_F16 || xdtype == GPTQ_BF16) && d >= 64 && n_tok >= 64))
+    return GPTQ_ERR_UNSUPPORTED;
+  if (lost_stage < 0 || lost_stage >= ceil_div(n_tok, TB_K)) return GPTQ_ERR_INVALID_ARG;
+  return launch_hessian_tc(X, xdtype, n_tok, d, ldx, H, 0, st, s, wait_ns, (int)lost_stage);
 }
 
 }  // namespace gptq

@@ -256,15 +256,17 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
+  pdl_launch_next();
+  // the packed U block was written before the sweeps began (it depends on U alone): its
+  // copy starts before the wait for the previous kernel on the stream
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::mbar_fence_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar, UD_FLOATS * 4);
     tc::bulk_load(Us, Ud, UD_FLOATS * 4, &bar);
   }
+  pdl_wait();
+  __syncthreads();
   // working weights, coalesced; float4 when the tile rows are 16-byte aligned
   if ((b0 % 4) == 0 && (ldwf % 4) == 0) {
 #pragma unroll 8
@@ -889,12 +891,12 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       return launch_gemm_nt(g, q.st, st);
     };
     auto sweep = [&](int64_t b0, int nb, int e, int h, cudaStream_t st) -> gptq_status {
-      sweep_kernel<<<sweep_grid, SW_THREADS, sweep_smem, st>>>(
-          q.Wf, q.ldwf, m, b0, nb, q.Ud + (b0 / block) * UD_FLOATS, scale, zero, maxq,
-          (e ? q.Ehi2 : q.Ehi) + h * block, (e ? q.Elo2 : q.Elo) + h * block, q.lde, q.codes,
-          q.ldc, q.st);
-      GPTQ_LAUNCH_CHECK();
-      return GPTQ_OK;
+      return launch_kernel(sweep_kernel, sweep_grid, SW_THREADS, sweep_smem, st, true,
+                           (const float *)q.Wf, q.ldwf, m, b0, nb,
+                           (const float *)(q.Ud + (b0 / block) * UD_FLOATS),
+                           (const float *)scale, (const int32_t *)zero, maxq,
+                           (e ? q.Ehi2 : q.Ehi) + h * block, (e ? q.Elo2 : q.Elo) + h * block,
+                           q.lde, q.codes, q.ldc, q.st);
     };
     if (!overlap) {
       int k = 0;

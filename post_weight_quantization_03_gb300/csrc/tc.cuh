@@ -2,8 +2,9 @@
 // mbarriers with bounded waits, TMA tiled loads, tcgen05 TMEM allocation, MMA issue,
 // commit and TMEM loads, and the shared-memory / instruction descriptors.
 //
-// Every wait is bounded: after `kSpinLimit` polls the waiter records GPTQ_ERR_TIMEOUT in
-// the device status block and gives up, so a lost arrival can never hang the GPU.
+// Every wait is bounded in time: after kWaitNs nanoseconds of the GPU's global timer (or a
+// shorter budget a launch passes) the waiter records GPTQ_ERR_TIMEOUT in the device status
+// block and gives up, so a lost arrival can never hang the GPU.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap
@@ -13,7 +14,14 @@
 namespace gptq {
 namespace tc {
 
-constexpr uint32_t kSpinLimit = 1u << 24;  // polls of try_wait (each may block ~µs)
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait here
+
+// The GPU's global nanosecond timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -53,10 +61,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (and records TIMEOUT) if the
-// phase did not complete within kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, DevStatus *st) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+// phase did not complete within `budget_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, DevStatus *st,
+                                          uint64_t budget_ns = kWaitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > budget_ns) break;
+  }
   if (st) atomicCAS(&st->status, 0, (int)GPTQ_ERR_TIMEOUT);
   return false;
 }
@@ -122,6 +137,20 @@ __device__ __forceinline__ void bulk_wait_all() {
 
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also returns the AND of `pred` over the `nthreads` participants.
+__device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -2,22 +2,30 @@
 //
 // A [M, K] and B [N, K] are K-contiguous fp32 operands, each stored as a TF32 head and
 // tail (x = head + tail exactly, head with its low 13 mantissa bits clear).  Per K step the
-// tensor core accumulates head_A head_B^T + head_A tail_B^T + tail_A head_B^T into an fp32
-// TMEM accumulator, which reproduces fp32 products to about 2^-21 relative.
+// tensor core accumulates head_A head_B^T + head_A tail_B^T + tail_A head_B^T, which
+// reproduces fp32 products to about 2^-21 relative.
+//
+// The tensor core's fp32 accumulation truncates (rounds toward zero), so a long running
+// sum in TMEM drifts.  The head products therefore go to an accumulator of their own that
+// the epilogue drains into round-to-nearest fp32 registers every kGroup K stages, and the
+// two cross products (about 2^-11 of the head product) to a second accumulator drained once
+// per tile.  (One accumulator per 128-deep tile left the factor U of a 28672-wide layer
+// with row errors up to 2e-4 against the fp64 oracle; short head sums bring it to the
+// fp32 storage floor, about 7e-5.)
 //
 // Persistent: each CTA walks a static list of 128 x 128 output tiles; warp roles:
 //   warp 0      : TMA producer (one lane): 4 operand tiles per 32-wide K stage, running
 //                 ahead across tile boundaries through a 3-stage ring
-//   warp 1      : TMEM allocator + MMA issuer (one lane), alternating between two
-//                 128-column TMEM accumulators so the next tile's MMAs overlap this
-//                 tile's epilogue
-//   warps 2..5  : epilogue: TMEM -> registers -> alpha * acc staged in shared memory in
-//                 the 128-byte-swizzled box layout (two 64-column halves) -> TMA
-//                 reduce-add into C (the add happens in L2, so concurrent updates of
-//                 the same C are safe); plain read-modify-write when C is not 16-byte
-//                 aligned
-// Every mbarrier wait is bounded (tc.cuh); the epilogue's wait is taken by one leader
-// thread and broadcast, so all four epilogue warps leave their loop together.
+//   warp 1      : TMEM allocator + MMA issuer (one lane): head products into two alternating
+//                 128-column accumulators (kGroup stages each), cross products into two
+//                 more, alternating by tile
+//   warps 2..5  : epilogue: TMEM -> registers (the tile's running sum, one row per thread);
+//                 per tile alpha * sum staged in shared memory in the 128-byte-swizzled box
+//                 layout (two 64-column halves) -> TMA reduce-add into C (the add happens in
+//                 L2, so concurrent updates of the same C are safe); plain
+//                 read-modify-write when C is not 16-byte aligned
+// Every mbarrier wait is bounded (tc.cuh); the epilogue warps agree on the outcome of their
+// waits once per tile (a barrier with an AND vote), so all four leave their loops together.
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -34,7 +42,8 @@ constexpr uint32_t kTileA = BM * BK * 4;  // 16 KB
 constexpr uint32_t kTileB = BN * BK * 4;  // 16 KB
 constexpr uint32_t kStageBytes = 2 * kTileA + 2 * kTileB;
 constexpr uint32_t kStagingBytes = 2 * BM * 128;  // two 32-column boxes (one 64-col half)
-constexpr uint32_t kTmemCols = 2 * BN;            // two accumulators
+constexpr int kGroup = 2;                         // K stages per head-product sum
+constexpr uint32_t kTmemCols = 4 * BN;            // 2 head + 2 cross accumulators: 512
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 
 struct TcGemmParams {
@@ -74,13 +83,16 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
   uint8_t *staging = smem + kStages * kStageBytes;
   uint64_t *full = (uint64_t *)(staging + kStagingBytes);
   uint64_t *empty = full + kStages;
-  uint64_t *tfull = empty + kStages;   // [2] accumulator ready
-  uint64_t *tempty = tfull + 2;        // [2] accumulator drained
-  uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
-  int *epi_ok = (int *)(tmem_slot + 1);
+  uint64_t *hfull = empty + kStages;    // [2] head-product accumulator ready
+  uint64_t *hempty = hfull + 2;         // [2] head-product accumulator drained
+  uint64_t *xfull = hempty + 2;         // [2] cross-product accumulator ready (per tile)
+  uint64_t *xempty = xfull + 2;         // [2] cross-product accumulator drained
+  uint32_t *tmem_slot = (uint32_t *)(xempty + 2);
 
   __shared__ int s_skip;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  pdl_launch_next();
+  pdl_wait();
   if (threadIdx.x == 0) s_skip = (st && st->status != 0);
   __syncthreads();
   if (s_skip) return;  // uniform for the whole CTA, before any barrier or TMEM use
@@ -92,8 +104,10 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
       tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+      tc::mbar_init(&hfull[b], 1);
+      tc::mbar_init(&hempty[b], 4);  // one arrival per epilogue warp
+      tc::mbar_init(&xfull[b], 1);
+      tc::mbar_init(&xempty[b], 4);
     }
     tc::mbar_fence_init();
   }
@@ -133,21 +147,30 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
-    int g = 0, it = 0;
+    int g = 0, hg = 0, it = 0, hb = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
-      const int b = it & 1;
+      const int xb = it & 1;
       if (it >= 2) {
-        ok = tc::mbar_wait(&tempty[b], ((it / 2) - 1) & 1, st);
+        ok = tc::mbar_wait(&xempty[xb], ((it / 2) - 1) & 1, st);
         if (!ok) break;
         tc::tc_fence_after();
       }
-      const uint32_t dt = tmem + (uint32_t)(b * BN);
+      const uint32_t dx = tmem + (uint32_t)((2 + xb) * BN);
       for (int kt = 0; kt < ktiles; ++kt, ++g) {
         const int s = g % kStages;
+        if (kt % kGroup == 0) {
+          hb = hg & 1;
+          if (hg >= 2) {
+            ok = tc::mbar_wait(&hempty[hb], ((hg / 2) - 1) & 1, st);
+            if (!ok) break;
+            tc::tc_fence_after();
+          }
+        }
         ok = tc::mbar_wait(&full[s], (g / kStages) & 1, st);
         if (!ok) break;
         tc::tc_fence_after();
+        const uint32_t dh = tmem + (uint32_t)(hb * BN);
         const uint32_t a_hi = tc::smem_u32(smem + s * kStageBytes);
         const uint32_t a_lo = a_hi + kTileA;
         const uint32_t b_hi = a_hi + 2 * kTileA;
@@ -159,43 +182,83 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
           const uint64_t dal = tc::smem_desc_sw128(a_lo + off, 16, 1024);
           const uint64_t dbh = tc::smem_desc_sw128(b_hi + off, 16, 1024);
           const uint64_t dbl = tc::smem_desc_sw128(b_lo + off, 16, 1024);
-          const uint32_t acc0 = (kt > 0 || kk > 0) ? 1u : 0u;
-          tc::mma_tf32(dt, dah, dbh, idesc, acc0);
-          tc::mma_tf32(dt, dah, dbl, idesc, 1u);
-          tc::mma_tf32(dt, dal, dbh, idesc, 1u);
+          tc::mma_tf32(dh, dah, dbh, idesc, (kt % kGroup != 0 || kk > 0) ? 1u : 0u);
+          tc::mma_tf32(dx, dah, dbl, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_tf32(dx, dal, dbh, idesc, 1u);
         }
-        tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+        tc::mma_commit(&empty[s]);   // frees the stage once these MMAs have read it
+        if (kt % kGroup == kGroup - 1 || kt == ktiles - 1) {
+          tc::mma_commit(&hfull[hb]);  // the head sum of this group is complete
+          ++hg;
+        }
       }
-      tc::mma_commit(&tfull[b]);    // accumulator complete (or abandoned after a timeout)
+      if (!ok) break;
+      tc::mma_commit(&xfull[xb]);      // the tile's cross sum is complete
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int rl = q * 32 + lane;      // row within the tile
     const bool leader = (warp == 2 && lane == 0);
-    int it = 0;
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
-      const int b = it & 1;
-      if (leader) *epi_ok = tc::mbar_wait(&tfull[b], (it / 2) & 1, st) ? 1 : 0;
-      tc::named_barrier(1, 128);
-      if (!*epi_ok) break;             // same value for all four warps
-      tc::tc_fence_after();
+    const int ngroups = (ktiles + kGroup - 1) / kGroup;
+    int hg = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
+      float acc[BN];
+#pragma unroll
+      for (int i = 0; i < BN; ++i) acc[i] = 0.f;
+      // this warp's lane quarter of an accumulator -> acc (two loads in flight per wait)
+      auto drain = [&](uint32_t col) {
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + col;
+#pragma unroll
+        for (int c = 0; c < BN / 32; c += 2) {
+          uint32_t r0[32], r1[32];
+          tc::tmem_ld32(ta + (uint32_t)(c * 32), r0);
+          tc::tmem_ld32(ta + (uint32_t)(c * 32 + 32), r1);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            acc[c * 32 + i] += __uint_as_float(r0[i]);
+            acc[c * 32 + 32 + i] += __uint_as_float(r1[i]);
+          }
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+      };
+      // each warp drains its lane quarter on its own; the four agree once per tile
+      for (int gi = 0; gi < ngroups && ok; ++gi, ++hg) {
+        const int hb = hg & 1;
+        int okl = 0;
+        if (lane == 0) okl = tc::mbar_wait(&hfull[hb], (hg / 2) & 1, st) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, okl, 0)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        drain((uint32_t)(hb * BN));
+        if (lane == 0) tc::mbar_arrive(&hempty[hb]);
+      }
+      if (ok) {
+        const int xb = it & 1;
+        int okl = 0;
+        if (lane == 0) okl = tc::mbar_wait(&xfull[xb], (it / 2) & 1, st) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, okl, 0)) {
+          tc::tc_fence_after();
+          drain((uint32_t)((2 + xb) * BN));
+          if (lane == 0) tc::mbar_arrive(&xempty[xb]);
+        } else {
+          ok = false;
+        }
+      }
+      ok = tc::named_barrier_and(1, 128, ok);   // uniform across the four warps
+      if (!ok) break;
       int tm, tn;
       tile_coords(p, t, tm, tn);
       const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
       const int64_t row = m0 + rl;
-#pragma unroll 1
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t r0[32], r1[32];
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + h * 64);
-        tc::tmem_ld32(ta, r0);
-        tc::tmem_ld32(ta + 32, r1);
-        tc::tmem_ld_wait();
-        if (h == 1) {  // this warp's reads of the accumulator are done: release it
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&tempty[b]);
-        }
+        const float *r0 = acc + h * 64, *r1 = acc + h * 64 + 32;
         if (p.tma_c) {
           uint8_t *rowp0 = staging + rl * 128;
           uint8_t *rowp1 = staging + BM * 128 + rl * 128;
@@ -203,11 +266,11 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
           for (int u = 0; u < 8; ++u) {
             const int su = (u ^ (rl & 7)) * 16;
             *reinterpret_cast<float4 *>(rowp0 + su) =
-                make_float4(p.alpha * __uint_as_float(r0[4 * u]), p.alpha * __uint_as_float(r0[4 * u + 1]),
-                            p.alpha * __uint_as_float(r0[4 * u + 2]), p.alpha * __uint_as_float(r0[4 * u + 3]));
+                make_float4(p.alpha * r0[4 * u], p.alpha * r0[4 * u + 1],
+                            p.alpha * r0[4 * u + 2], p.alpha * r0[4 * u + 3]);
             *reinterpret_cast<float4 *>(rowp1 + su) =
-                make_float4(p.alpha * __uint_as_float(r1[4 * u]), p.alpha * __uint_as_float(r1[4 * u + 1]),
-                            p.alpha * __uint_as_float(r1[4 * u + 2]), p.alpha * __uint_as_float(r1[4 * u + 3]));
+                make_float4(p.alpha * r1[4 * u], p.alpha * r1[4 * u + 1],
+                            p.alpha * r1[4 * u + 2], p.alpha * r1[4 * u + 3]);
           }
           tc::fence_proxy_async_smem();
           tc::named_barrier(1, 128);
@@ -223,8 +286,8 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int64_t c0 = n0 + h * 64 + i, c1 = c0 + 32;
-            if (c0 < p.N) p.c[row * p.ldc + c0] = fmaf(p.alpha, __uint_as_float(r0[i]), p.c[row * p.ldc + c0]);
-            if (c1 < p.N) p.c[row * p.ldc + c1] = fmaf(p.alpha, __uint_as_float(r1[i]), p.c[row * p.ldc + c1]);
+            if (c0 < p.N) p.c[row * p.ldc + c0] = fmaf(p.alpha, r0[i], p.c[row * p.ldc + c0]);
+            if (c1 < p.N) p.c[row * p.ldc + c1] = fmaf(p.alpha, r1[i], p.c[row * p.ldc + c1]);
           }
         }
       }
@@ -302,8 +365,10 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   const int cap = g.max_ctas < 0 ? p.n_tiles
                   : (g.max_ctas > 0 && g.max_ctas < num_sms) ? g.max_ctas : num_sms;
   const int grid = p.n_tiles < cap ? p.n_tiles : cap;
-  tc_gemm_3xtf32_kernel<<<grid, kThreads, kSmemBytes, s>>>(mah, mal, mbh, mbl, mc, p, st);
-  GPTQ_LAUNCH_CHECK();
+  // no programmatic early launch: a persistent GEMM's CTAs (225 KB of shared memory each)
+  // waiting for their predecessor would hold SMs that a concurrent stream's kernels need
+  GPTQ_TRY(launch_kernel(tc_gemm_3xtf32_kernel, grid, kThreads, kSmemBytes, s, false, mah,
+                         mal, mbh, mbl, mc, p, st));
   return GPTQ_OK;
 }
 

@@ -66,6 +66,9 @@ _SIGS = {
                                                _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                                _c.c_void_p, _c.c_void_p]),
     "gptq_noalloc_status": (_c.c_int, [_c.c_void_p]),
+    "gptq_debug_hessian_lost_stage": (_c.c_int, [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+                                                 _c.c_int64, _c.c_void_p, _c.c_int64,
+                                                 _c.c_uint64, _c.c_void_p, _c.c_void_p]),
 }
 NOALLOC_SCRATCH_BYTES = 32 << 20  # GPTQ_NOALLOC_SCRATCH_BYTES in include/gptq.h
 OBQ_MAX_D_IN = 128                # GPTQ_OBQ_MAX_D_IN in include/gptq.h
@@ -202,6 +205,12 @@ def gptq_quantize_layer_noalloc(W, wdtype, d_out, d_in, ldw, U, dead_mask, bits,
 
 def gptq_noalloc_status(stream):
     return load().gptq_noalloc_status(stream)
+
+
+def gptq_debug_hessian_lost_stage(X, xdtype, n_tok, d_in, ldx, H, lost_stage, wait_ns, status_ws,
+                                  stream):
+    return load().gptq_debug_hessian_lost_stage(X, xdtype, n_tok, d_in, ldx, H, lost_stage,
+                                                wait_ns, status_ws, stream)
 
 
 # ---------------------------------------------------------------------------------------

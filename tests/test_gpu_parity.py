@@ -53,7 +53,10 @@ def _codes(qpacked, bits, d):
 # ---------------------------------------------------------------------------------------
 
 @pytest.mark.parametrize("d,n,dtype,dead,outl", [
-    (256, 512, "f32", 0, 0),        # the 256 x 256, 512-token fp32 layer
+    (256, 512, "f32", 0, 0),        # the 256 x 256, 512-token fp32 layer (3xTF32 tensor cores)
+    (300, 777, "f32", 3, 2),        # fp32: ragged channels (a partial 128-wide tile) and tokens
+    (1024, 4096, "f32", 10, 8),     # fp32: several segments of 512 tokens, 36 tiles
+    (40, 100, "f32", 1, 1),         # fp32: one tile, mostly zero fill
     (300, 777, "f16", 3, 2),        # ragged channels and tokens
     (512, 2048, "bf16", 5, 4),
     (1024, 4096, "f16", 10, 8),
@@ -87,8 +90,9 @@ def test_hessian_long_token_sum():
     assert np.max(np.abs(dg[live] - dr[live]) / dr[live]) <= 1e-5
 
 
-def test_hessian_accumulates_over_chunks():
-    spec = S.ActivationSpec(d_in=384, n_tok=6144, dtype="f16", n_dead=2, seed=77)
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_hessian_accumulates_over_chunks(dtype):
+    spec = S.ActivationSpec(d_in=384, n_tok=6144, dtype=dtype, n_dead=2, seed=77)
     X = _x(spec).to(DEV)
     H = gptq.hessian(X[:2048])
     gptq.hessian(X[2048:4096], H, accumulate=True)
