@@ -51,32 +51,16 @@ gptq_status device_sm_count(int *out);
 
 static inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Programmatic dependent launch.  Kernels on the critical chains (factorization panels,
-// blocked sweep) start with pdl_launch_next() -- the next kernel on the stream may then be
-// launched and scheduled while this one runs -- and pdl_wait() -- which returns once the
-// previous kernel on the stream has completed and its writes are visible -- before any
-// global memory access.  Both are no-ops for a kernel launched without the attribute.
-__device__ __forceinline__ void pdl_launch_next() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// Launches `kern` on `s`, with the programmatic-stream-serialization attribute when `pdl`
-// (the kernel must then begin with pdl_wait() before touching global memory); counts the
+// Launches `kern` on `s` (arguments converted to the kernel's parameter types), counts the
 // launch and maps a launch error to GPTQ_ERR_CUDA.
 template <typename... KArgs, typename... Args>
 gptq_status launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t s, bool pdl, Args &&...args) {
+                          cudaStream_t s, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = pdl ? attr : nullptr;
-  cfg.numAttrs = pdl ? 1 : 0;
   count_launch();
   if (cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -159,6 +143,10 @@ struct GemmArgs {
   int trans_c;
   int max_ctas;   // tensor-core path: at most this many persistent CTAs (0 = one per SM;
                   // -1 = one CTA per tile, so SMs free up tile by tile for other streams)
+  int one_sum;    // tensor-core path: 1 = all three products of a tile in one TMEM sum
+                  // (the sweep's updates); 0 = head products in sums of two 32-wide K
+                  // stages and the cross products apart (the factorization's updates,
+                  // whose accuracy needs the short sums)
 };
 gptq_status launch_gemm_nt(const GemmArgs &g, DevStatus *st, cudaStream_t s);
 // tc_gemm.cu: the tcgen05 3xTF32 kernel; UNSUPPORTED when the operands do not meet its

@@ -399,8 +399,6 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
   __shared__ __align__(16) float4 cb[64];   // the leaf's row exchange (two buffers)
   __shared__ int s_skip, s_bad;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  pdl_launch_next();
-  pdl_wait();
   if (tid == 0) { s_skip = st->status != 0; s_bad = -1; }
   __syncthreads();
   if (s_skip) return;
@@ -548,8 +546,6 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
   extern __shared__ __align__(16) float sm[];
   float *Bs = sm;                    // 32 NCQ x LD: the CTA's Bm rows (output columns, K)
   float *Is = sm + 32 * NCQ * LD;    // RM_ROWS x LD: the CTA's input rows
-  pdl_launch_next();
-  pdl_wait();
   if (st->status != 0) return;
   const int kz = KS > 1 ? KC * (int)blockIdx.z : 0;   // first K of the chunk
   const int tid = threadIdx.x;
@@ -832,7 +828,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
     if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->eb[par], 0));
-    GPTQ_TRY(launch_kernel(potrf_kernel, 1, PF_THREADS, potrf_smem, c, true, A, d, k0, n,
+    GPTQ_TRY(launch_kernel(potrf_kernel, 1, PF_THREADS, potrf_smem, c, A, d, k0, n,
                            w.Linv[par], w.st));
     if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->ep[par], c));
     // the previous column update's rows below the diagonal block (second critical stream)
@@ -841,11 +837,9 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     if (k1 < d) {
       const int nn = (int)std::min<int64_t>(NB, d - k1);
       // trsm: rows [r0, r1) of panel k -> L panel (hi/lo)
-      // programmatic early launch only on the critical stream (its kernels are small); on
-      // the other streams CTAs waiting for their predecessor would hold SMs
       auto trsm = [&](int64_t r0, int64_t r1, cudaStream_t st) {
         dim3 g((unsigned)ceil_div(r1 - r0, RM_ROWS), 4);
-        return launch_kernel(rowmul_kernel<1>, g, RM_THREADS, rmq_smem, st, st == c, A + k0,
+        return launch_kernel(rowmul_kernel<1>, g, RM_THREADS, rmq_smem, st, A + k0,
                              (const float *)nullptr, d, (float *)nullptr, (int64_t)0, r0, r1,
                              w.Linv[par], (const float *)nullptr, (int64_t)NB, n, n, 0,
                              w.Lhi[par], w.Llo[par], w.st);
@@ -855,7 +849,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
       // adds here too)
       auto next_col = [&](int64_t r0, int64_t r1, cudaStream_t st) {
         dim3 g2((unsigned)ceil_div(r1 - r0, RM_ROWS), (unsigned)ceil_div(nn, 32));
-        return launch_kernel(rowmul_kernel<1>, g2, RM_THREADS, rmq_smem, st, st == c,
+        return launch_kernel(rowmul_kernel<1>, g2, RM_THREADS, rmq_smem, st,
                              w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
                              A + k1 * d + k1, d, r0, r1, w.Lhi[par] + k1 * NB,
                              w.Llo[par] + k1 * NB, (int64_t)NB, n, nn, 1, (float *)nullptr,
@@ -875,7 +869,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
         {
           // the next potrf's block, in four K chunks (64 CTAs; atomic adds)
           dim3 g2((unsigned)ceil_div(nn, RM_ROWS), (unsigned)ceil_div(nn, 32), 4);
-          GPTQ_TRY(launch_kernel(rowmul_kernel<1, 4>, g2, RM_THREADS, rmk_smem, c, true,
+          GPTQ_TRY(launch_kernel(rowmul_kernel<1, 4>, g2, RM_THREADS, rmk_smem, c,
                                  w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
                                  A + k1 * d + k1, d, (int64_t)0, (int64_t)nn,
                                  w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB, n, nn,
@@ -898,7 +892,7 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     // inverse step a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
     {
       const unsigned g = (unsigned)ceil_div(k1, RM_ROWS);
-      GPTQ_TRY(launch_kernel(rowmul_kernel<4>, g, RM_THREADS, rm_smem, b, false,
+      GPTQ_TRY(launch_kernel(rowmul_kernel<4>, g, RM_THREADS, rm_smem, b,
                              (const float *)(w.Yt + k0), (const float *)nullptr, d, w.Yt + k0, d,
                              (int64_t)0, k1, (const float *)w.Linv[par], (const float *)nullptr,
                              (int64_t)NB, n, n, 0, w.Yhi, w.Ylo, w.st));

@@ -256,16 +256,12 @@ sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, 
   __shared__ __align__(8) uint64_t bar;
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
-  pdl_launch_next();
-  // the packed U block was written before the sweeps began (it depends on U alone): its
-  // copy starts before the wait for the previous kernel on the stream
   if (tid == 0) {
     tc::mbar_init(&bar, 1);
     tc::mbar_fence_init();
     tc::mbar_arrive_expect_tx(&bar, UD_FLOATS * 4);
     tc::bulk_load(Us, Ud, UD_FLOATS * 4, &bar);
   }
-  pdl_wait();
   __syncthreads();
   // working weights, coalesced; float4 when the tile rows are 16-byte aligned
   if ((b0 % 4) == 0 && (ldwf % 4) == 0) {
@@ -888,10 +884,11 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       g.c = q.Wf + c0; g.ldc = q.ldwf;
       g.M = m; g.N = c1 - c0; g.K = K;
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
+      g.one_sum = 1;   // one TMEM sum per tile: the codes need no shorter sums
       return launch_gemm_nt(g, q.st, st);
     };
     auto sweep = [&](int64_t b0, int nb, int e, int h, cudaStream_t st) -> gptq_status {
-      return launch_kernel(sweep_kernel, sweep_grid, SW_THREADS, sweep_smem, st, true,
+      return launch_kernel(sweep_kernel, sweep_grid, SW_THREADS, sweep_smem, st,
                            (const float *)q.Wf, q.ldwf, m, b0, nb,
                            (const float *)(q.Ud + (b0 / block) * UD_FLOATS),
                            (const float *)scale, (const int32_t *)zero, maxq,

@@ -6,19 +6,23 @@
 // reproduces fp32 products to about 2^-21 relative.
 //
 // The tensor core's fp32 accumulation truncates (rounds toward zero), so a long running
-// sum in TMEM drifts.  The head products therefore go to an accumulator of their own that
-// the epilogue drains into round-to-nearest fp32 registers every kGroup K stages, and the
-// two cross products (about 2^-11 of the head product) to a second accumulator drained once
-// per tile.  (One accumulator per 128-deep tile left the factor U of a 28672-wide layer
+// sum in TMEM drifts.  Two kernels:
+//   tc_gemm_short_sums_kernel (the factorization's updates, whose accuracy needs it): the
+//     head products go to an accumulator of their own that the epilogue drains into
+//     round-to-nearest fp32 registers every kHeadGroup K stages, and the two cross products
+//     (about 2^-11 of the head product) to a second accumulator drained once per tile;
+//   tc_gemm_one_sum_kernel (the sweep's updates, whose codes need no more): all three
+//     products of a tile in one TMEM sum, drained once.  (One accumulator per 128-deep tile left the factor U of a 28672-wide layer
 // with row errors up to 2e-4 against the fp64 oracle; short head sums bring it to the
 // fp32 storage floor, about 7e-5.)
 //
-// Persistent: each CTA walks a static list of 128 x 128 output tiles; warp roles:
+// Both are persistent: each CTA walks a static list of 128 x 128 output tiles; warp roles
+// (short sums; the one-sum kernel alternates two 128-column tile accumulators instead):
 //   warp 0      : TMA producer (one lane): 4 operand tiles per 32-wide K stage, running
 //                 ahead across tile boundaries through a 3-stage ring
 //   warp 1      : TMEM allocator + MMA issuer (one lane): head products into two alternating
-//                 128-column accumulators (kGroup stages each), cross products into two
-//                 more, alternating by tile
+//                 128-column accumulators (kHeadGroup stages each, or the whole tile), cross
+//                 products into two more, alternating by tile (or with the head products)
 //   warps 2..5  : epilogue: TMEM -> registers (the tile's running sum, one row per thread);
 //                 per tile alpha * sum staged in shared memory in the 128-byte-swizzled box
 //                 layout (two 64-column halves) -> TMA reduce-add into C (the add happens in
@@ -42,8 +46,8 @@ constexpr uint32_t kTileA = BM * BK * 4;  // 16 KB
 constexpr uint32_t kTileB = BN * BK * 4;  // 16 KB
 constexpr uint32_t kStageBytes = 2 * kTileA + 2 * kTileB;
 constexpr uint32_t kStagingBytes = 2 * BM * 128;  // two 32-column boxes (one 64-col half)
-constexpr int kGroup = 2;                         // K stages per head-product sum
 constexpr uint32_t kTmemCols = 4 * BN;            // 2 head + 2 cross accumulators: 512
+constexpr int kHeadGroup = 2;                     // K stages per head-product TMEM sum
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 
 struct TcGemmParams {
@@ -71,8 +75,76 @@ __device__ __forceinline__ void tile_coords(const TcGemmParams &p, int t, int &t
   }
 }
 
+// TMA producer (one lane): 4 operand tiles per 32-wide K stage, running ahead across tile
+// boundaries through the kStages ring.
+__device__ __forceinline__ void produce(const CUtensorMap *ma_hi, const CUtensorMap *ma_lo,
+                                        const CUtensorMap *mb_hi, const CUtensorMap *mb_lo,
+                                        const TcGemmParams &p, uint8_t *smem, uint64_t *full,
+                                        uint64_t *empty, int ktiles, DevStatus *st) {
+  tc::tma_prefetch_desc(ma_hi);
+  tc::tma_prefetch_desc(ma_lo);
+  tc::tma_prefetch_desc(mb_hi);
+  tc::tma_prefetch_desc(mb_lo);
+  int g = 0;
+  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    int tm, tn;
+    tile_coords(p, t, tm, tn);
+    const int32_t m0 = tm * BM, n0 = tn * BN;
+    for (int kt = 0; kt < ktiles; ++kt, ++g) {
+      const int s = g % kStages;
+      if (g >= kStages && !tc::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, st)) return;
+      uint8_t *base = smem + s * kStageBytes;
+      tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+      const int32_t k0 = kt * BK;
+      tc::tma_load_2d(base, ma_hi, k0, m0, &full[s]);
+      tc::tma_load_2d(base + kTileA, ma_lo, k0, m0, &full[s]);
+      tc::tma_load_2d(base + 2 * kTileA, mb_hi, k0, n0, &full[s]);
+      tc::tma_load_2d(base + 2 * kTileA + kTileB, mb_lo, k0, n0, &full[s]);
+    }
+  }
+}
+
+// Epilogue of one 64-column half h of a tile (four warps, thread = row rl of the tile):
+// alpha * (r0 | r1) into C, by TMA reduce-add through the 128-byte-swizzled staging boxes,
+// or by read-modify-write when C has no tensor map.
+__device__ __forceinline__ void store_half(const TcGemmParams &p, const CUtensorMap *mc,
+                                           uint8_t *staging, const float *r0, const float *r1,
+                                           int rl, int64_t row, int64_t m0, int64_t n0, int h,
+                                           bool leader) {
+  if (p.tma_c) {
+    uint8_t *rowp0 = staging + rl * 128;
+    uint8_t *rowp1 = staging + BM * 128 + rl * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int su = (u ^ (rl & 7)) * 16;
+      *reinterpret_cast<float4 *>(rowp0 + su) =
+          make_float4(p.alpha * r0[4 * u], p.alpha * r0[4 * u + 1], p.alpha * r0[4 * u + 2],
+                      p.alpha * r0[4 * u + 3]);
+      *reinterpret_cast<float4 *>(rowp1 + su) =
+          make_float4(p.alpha * r1[4 * u], p.alpha * r1[4 * u + 1], p.alpha * r1[4 * u + 2],
+                      p.alpha * r1[4 * u + 3]);
+    }
+    tc::fence_proxy_async_smem();
+    tc::named_barrier(1, 128);
+    if (leader) {
+      tc::tma_reduce_add_2d(mc, (int32_t)(n0 + h * 64), (int32_t)m0, staging);
+      tc::tma_reduce_add_2d(mc, (int32_t)(n0 + h * 64 + 32), (int32_t)m0, staging + BM * 128);
+      tc::bulk_commit();
+      tc::bulk_wait_read_all();  // staging may be overwritten after the next barrier
+    }
+    tc::named_barrier(1, 128);
+  } else if (row < p.M) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int64_t c0 = n0 + h * 64 + i, c1 = c0 + 32;
+      if (c0 < p.N) p.c[row * p.ldc + c0] = fmaf(p.alpha, r0[i], p.c[row * p.ldc + c0]);
+      if (c1 < p.N) p.c[row * p.ldc + c1] = fmaf(p.alpha, r1[i], p.c[row * p.ldc + c1]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
+tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
                       const __grid_constant__ CUtensorMap ma_lo,
                       const __grid_constant__ CUtensorMap mb_hi,
                       const __grid_constant__ CUtensorMap mb_lo,
@@ -91,8 +163,6 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
 
   __shared__ int s_skip;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  pdl_launch_next();
-  pdl_wait();
   if (threadIdx.x == 0) s_skip = (st && st->status != 0);
   __syncthreads();
   if (s_skip) return;  // uniform for the whole CTA, before any barrier or TMEM use
@@ -118,32 +188,7 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- producer ----------------
-    tc::tma_prefetch_desc(&ma_hi);
-    tc::tma_prefetch_desc(&ma_lo);
-    tc::tma_prefetch_desc(&mb_hi);
-    tc::tma_prefetch_desc(&mb_lo);
-    int g = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-      int tm, tn;
-      tile_coords(p, t, tm, tn);
-      const int32_t m0 = tm * BM, n0 = tn * BN;
-      for (int kt = 0; kt < ktiles; ++kt, ++g) {
-        const int s = g % kStages;
-        if (g >= kStages && !tc::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, st)) {
-          ok = false;
-          break;
-        }
-        uint8_t *base = smem + s * kStageBytes;
-        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
-        const int32_t k0 = kt * BK;
-        tc::tma_load_2d(base, &ma_hi, k0, m0, &full[s]);
-        tc::tma_load_2d(base + kTileA, &ma_lo, k0, m0, &full[s]);
-        tc::tma_load_2d(base + 2 * kTileA, &mb_hi, k0, n0, &full[s]);
-        tc::tma_load_2d(base + 2 * kTileA + kTileB, &mb_lo, k0, n0, &full[s]);
-      }
-    }
+    produce(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
@@ -159,7 +204,7 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
       const uint32_t dx = tmem + (uint32_t)((2 + xb) * BN);
       for (int kt = 0; kt < ktiles; ++kt, ++g) {
         const int s = g % kStages;
-        if (kt % kGroup == 0) {
+        if (kt % kHeadGroup == 0) {
           hb = hg & 1;
           if (hg >= 2) {
             ok = tc::mbar_wait(&hempty[hb], ((hg / 2) - 1) & 1, st);
@@ -182,12 +227,12 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
           const uint64_t dal = tc::smem_desc_sw128(a_lo + off, 16, 1024);
           const uint64_t dbh = tc::smem_desc_sw128(b_hi + off, 16, 1024);
           const uint64_t dbl = tc::smem_desc_sw128(b_lo + off, 16, 1024);
-          tc::mma_tf32(dh, dah, dbh, idesc, (kt % kGroup != 0 || kk > 0) ? 1u : 0u);
+          tc::mma_tf32(dh, dah, dbh, idesc, (kt % kHeadGroup != 0 || kk > 0) ? 1u : 0u);
           tc::mma_tf32(dx, dah, dbl, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
           tc::mma_tf32(dx, dal, dbh, idesc, 1u);
         }
         tc::mma_commit(&empty[s]);   // frees the stage once these MMAs have read it
-        if (kt % kGroup == kGroup - 1 || kt == ktiles - 1) {
+        if (kt % kHeadGroup == kHeadGroup - 1 || kt == ktiles - 1) {
           tc::mma_commit(&hfull[hb]);  // the head sum of this group is complete
           ++hg;
         }
@@ -200,7 +245,7 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int rl = q * 32 + lane;      // row within the tile
     const bool leader = (warp == 2 && lane == 0);
-    const int ngroups = (ktiles + kGroup - 1) / kGroup;
+    const int ngroups = (ktiles + kHeadGroup - 1) / kHeadGroup;
     int hg = 0, it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
@@ -257,46 +302,140 @@ tc_gemm_3xtf32_kernel(const __grid_constant__ CUtensorMap ma_hi,
       const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
       const int64_t row = m0 + rl;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float *r0 = acc + h * 64, *r1 = acc + h * 64 + 32;
-        if (p.tma_c) {
-          uint8_t *rowp0 = staging + rl * 128;
-          uint8_t *rowp1 = staging + BM * 128 + rl * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int su = (u ^ (rl & 7)) * 16;
-            *reinterpret_cast<float4 *>(rowp0 + su) =
-                make_float4(p.alpha * r0[4 * u], p.alpha * r0[4 * u + 1],
-                            p.alpha * r0[4 * u + 2], p.alpha * r0[4 * u + 3]);
-            *reinterpret_cast<float4 *>(rowp1 + su) =
-                make_float4(p.alpha * r1[4 * u], p.alpha * r1[4 * u + 1],
-                            p.alpha * r1[4 * u + 2], p.alpha * r1[4 * u + 3]);
-          }
-          tc::fence_proxy_async_smem();
-          tc::named_barrier(1, 128);
-          if (leader) {
-            tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + h * 64), (int32_t)m0, staging);
-            tc::tma_reduce_add_2d(&mc, (int32_t)(n0 + h * 64 + 32), (int32_t)m0,
-                                  staging + BM * 128);
-            tc::bulk_commit();
-            tc::bulk_wait_read_all();  // staging may be overwritten after the next barrier
-          }
-          tc::named_barrier(1, 128);
-        } else if (row < p.M) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int64_t c0 = n0 + h * 64 + i, c1 = c0 + 32;
-            if (c0 < p.N) p.c[row * p.ldc + c0] = fmaf(p.alpha, r0[i], p.c[row * p.ldc + c0]);
-            if (c1 < p.N) p.c[row * p.ldc + c1] = fmaf(p.alpha, r1[i], p.c[row * p.ldc + c1]);
-          }
-        }
-      }
+      for (int h = 0; h < 2; ++h)
+        store_half(p, &mc, staging, acc + h * 64, acc + h * 64 + 32, rl, row, m0, n0, h, leader);
     }
     if (leader) tc::bulk_wait_all();
   }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// One TMEM sum per tile (the sweep's updates): two 128-column tile accumulators used in
+// turn, so the next tile's MMAs overlap this tile's epilogue; the epilogue stages each
+// 64-column half straight from its TMEM loads and releases the accumulator after the second.
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
+                       const __grid_constant__ CUtensorMap ma_lo,
+                       const __grid_constant__ CUtensorMap mb_hi,
+                       const __grid_constant__ CUtensorMap mb_lo,
+                       const __grid_constant__ CUtensorMap mc, TcGemmParams p, DevStatus *st) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *staging = smem + kStages * kStageBytes;
+  uint64_t *full = (uint64_t *)(staging + kStagingBytes);
+  uint64_t *empty = full + kStages;
+  uint64_t *tfull = empty + kStages;   // [2] accumulator ready
+  uint64_t *tempty = tfull + 2;        // [2] accumulator drained
+  uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+  int *epi_ok = (int *)(tmem_slot + 1);
+
+  __shared__ int s_skip;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) s_skip = (st && st->status != 0);
+  __syncthreads();
+  if (s_skip) return;  // uniform for the whole CTA, before any barrier or TMEM use
+  const int ktiles = (int)((p.K + BK - 1) / BK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
+    tc::mbar_fence_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * BN);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    produce(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
+    int g = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      if (it >= 2) {
+        ok = tc::mbar_wait(&tempty[b], ((it / 2) - 1) & 1, st);
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
+      const uint32_t dt = tmem + (uint32_t)(b * BN);
+      for (int kt = 0; kt < ktiles; ++kt, ++g) {
+        const int s = g % kStages;
+        ok = tc::mbar_wait(&full[s], (g / kStages) & 1, st);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t a_hi = tc::smem_u32(smem + s * kStageBytes);
+        const uint32_t a_lo = a_hi + kTileA;
+        const uint32_t b_hi = a_hi + 2 * kTileA;
+        const uint32_t b_lo = b_hi + kTileB;
+#pragma unroll
+        for (int kk = 0; kk < BK / 8; ++kk) {  // 8 tf32 = 32 bytes per MMA
+          const uint32_t off = kk * 32;
+          const uint64_t dah = tc::smem_desc_sw128(a_hi + off, 16, 1024);
+          const uint64_t dal = tc::smem_desc_sw128(a_lo + off, 16, 1024);
+          const uint64_t dbh = tc::smem_desc_sw128(b_hi + off, 16, 1024);
+          const uint64_t dbl = tc::smem_desc_sw128(b_lo + off, 16, 1024);
+          tc::mma_tf32(dt, dah, dbh, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_tf32(dt, dah, dbl, idesc, 1u);
+          tc::mma_tf32(dt, dal, dbh, idesc, 1u);
+        }
+        tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+      }
+      tc::mma_commit(&tfull[b]);    // accumulator complete (or abandoned after a timeout)
+    }
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int rl = q * 32 + lane;      // row within the tile
+    const bool leader = (warp == 2 && lane == 0);
+    int it = 0;
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      if (leader) *epi_ok = tc::mbar_wait(&tfull[b], (it / 2) & 1, st) ? 1 : 0;
+      tc::named_barrier(1, 128);
+      if (!*epi_ok) break;             // same value for all four warps
+      tc::tc_fence_after();
+      int tm, tn;
+      tile_coords(p, t, tm, tn);
+      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
+      const int64_t row = m0 + rl;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32];
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + h * 64);
+        tc::tmem_ld32(ta, r0);
+        tc::tmem_ld32(ta + 32, r1);
+        tc::tmem_ld_wait();
+        if (h == 1) {  // this warp's reads of the accumulator are done: release it
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[b]);
+        }
+        float v0[32], v1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v0[i] = __uint_as_float(r0[i]);
+          v1[i] = __uint_as_float(r1[i]);
+        }
+        store_half(p, &mc, staging, v0, v1, rl, row, m0, n0, h, leader);
+      }
+    }
+    if (leader) tc::bulk_wait_all();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * BN);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -340,7 +479,8 @@ bool tc::make_tmap_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, 
 gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPTQ_OK;
   if (!g.a_lo || !g.b_lo) return GPTQ_ERR_UNSUPPORTED;
-  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_3xtf32_kernel, (int)kSmemBytes));
+  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_short_sums_kernel, (int)kSmemBytes));
+  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_one_sum_kernel, (int)kSmemBytes));
   CUtensorMap mah, mal, mbh, mbl;
   // maps cover exactly the [M, K] / [N, K] operand windows: out-of-range reads are zero
   if (!make_tmap_f32(&mah, g.a_hi, g.M, g.K, g.lda, BM) ||
@@ -365,10 +505,8 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   const int cap = g.max_ctas < 0 ? p.n_tiles
                   : (g.max_ctas > 0 && g.max_ctas < num_sms) ? g.max_ctas : num_sms;
   const int grid = p.n_tiles < cap ? p.n_tiles : cap;
-  // no programmatic early launch: a persistent GEMM's CTAs (225 KB of shared memory each)
-  // waiting for their predecessor would hold SMs that a concurrent stream's kernels need
-  GPTQ_TRY(launch_kernel(tc_gemm_3xtf32_kernel, grid, kThreads, kSmemBytes, s, false, mah,
-                         mal, mbh, mbl, mc, p, st));
+  GPTQ_TRY(launch_kernel(g.one_sum ? tc_gemm_one_sum_kernel : tc_gemm_short_sums_kernel, grid,
+                         kThreads, kSmemBytes, s, mah, mal, mbh, mbl, mc, p, st));
   return GPTQ_OK;
 }
 
