@@ -130,7 +130,7 @@ def stage_rooflines(m, d, n, bits, w_es, block, ms, peaks, peak_src, clk, layers
     a = p_flops / (ms["prepare"] / 1e3) / 1e12
     panels = -(-d // 128)
     out.append({"stage": "prepare", "kernel": "potrf_kernel + rowmul_kernel + "
-                "tc_gemm_3xtf32_kernel (panel loop)", "bound": "tensor",
+                "tc_gemm_short_sums_kernel (panel loop)", "bound": "tensor",
                 "achieved": round(a, 3), "peak": round(tf32, 1), "unit": "TFLOP/s",
                 "frac": round(a / tf32, 4), "ms": round(ms["prepare"], 4),
                 "work": f"2 d^3 / 3 = {p_flops:.4e} useful flop (3xTF32 executes three TF32 "
@@ -141,16 +141,20 @@ def stage_rooflines(m, d, n, bits, w_es, block, ms, peaks, peak_src, clk, layers
     q_bytes = float(m) * d * (w_es + 8 + 8 + bits / 8.0) + 4.0 * d * d
     a = q_bytes / (ms["quantize"] / 1e3) / 1e9
     blocks = -(-d // block)
-    out.append({"stage": "quantize", "kernel": "grid_kernel + sweep_kernel + "
-                "tc_gemm_3xtf32_kernel + pack_kernel", "bound": "hbm",
+    pairs = -(-blocks // 2) if block > 1 else blocks
+    out.append({"stage": "quantize", "kernel": ("grid_kernel + sweep_pair_kernel + "
+                "tc_gemm_one_sum_kernel + pack_kernel") if block > 1 else
+                "grid_kernel + eager_column_kernel + pack_kernel", "bound": "hbm",
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(a / hbm, 4), "ms": round(ms["quantize"], 4),
                 "work": f"{q_bytes:.4e} bytes: per weight W read ({w_es} B), fp32 working "
                         f"copy written and read (8 B), E head/tail written (8 B), packed "
                         f"codes ({bits / 8:g} B); U read once (4 d^2 B)",
                 "peak_source": f"{peak_src} copy bandwidth",
-                "chain": {"blocks": blocks,
-                          "us_per_block": round(ms["quantize"] * 1e3 / blocks, 2)}})
+                "chain": ({"pairs of blocks": pairs,
+                           "us_per_pair": round(ms["quantize"] * 1e3 / pairs, 2)} if block > 1
+                          else {"columns": blocks,
+                                "us_per_column": round(ms["quantize"] * 1e3 / blocks, 2)})})
     if layers != 1:
         for r in out:
             r["layers"] = layers

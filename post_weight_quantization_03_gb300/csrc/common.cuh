@@ -131,8 +131,8 @@ gptq_status launch_recon(const void *X, int xdtype, int64_t n, int64_t d, int64_
 
 // gemm.cu: C[m, n] (+)= alpha * sum_k A[m, k] * B[n, k], operands given as a TF32 head
 // and tail pair each (tail may be null = 0).  lower_only skips tiles strictly above the
-// diagonal of C (C square, row/col offsets equal).  trans_c stores C(m, n) at
-// C[n * ldc + m].
+// diagonal of C (C's row and column offsets equal, M >= N: a lower trapezoid; tiles on the
+// diagonal are computed whole).  trans_c stores C(m, n) at C[n * ldc + m].
 struct GemmArgs {
   const float *a_hi, *a_lo; int64_t lda;
   const float *b_hi, *b_lo; int64_t ldb;

@@ -26,6 +26,8 @@ namespace gptq {
 namespace {
 
 constexpr int NB = 128;            // panel width
+constexpr int kGroup = 4;          // panels per group (the deferred updates' K = 512)
+constexpr int64_t GW = kGroup * NB;
 
 // ---------------------------------------------------------------------------------------
 // Dead columns and damping (one CTA): dead = {i : H_ii == 0}; H_ii <- 1 for dead i;
@@ -523,7 +525,7 @@ potrf_kernel(const float *A, int64_t d, int64_t k0, int n, float *Linv, DevStatu
 // j < nj, with In and Bm optionally given as TF32 head + tail pairs (In_lo, Bm_lo summed on
 // load: the exact fp32 value).  Out[r][j] = P (sub = 0) or Out[r][j] -= P by atomic adds
 // (sub = 1: another stream may be adding into the same block).  Optionally also writes the
-// TF32 head/tail split of P into (hi, lo) panels (row r -> hi[r * NB + j]).  A CTA takes
+// TF32 head/tail split of P into (hi, lo) panels (row r -> hi[r * ldh + j]).  A CTA takes
 // RM_ROWS rows and NCQ of the four 32-column quarters of the output (blockIdx.y selects
 // which); with NCQ = 4 a CTA owns whole rows, stages its input rows before writing, and
 // Out may alias In.
@@ -541,7 +543,7 @@ template <int NCQ, int KS = 1>
 __global__ void __launch_bounds__(RM_THREADS)
 rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int64_t ldo,
               int64_t r0, int64_t r1, const float *Bm, const float *Bm_lo, int64_t ldb, int n,
-              int nj, int sub, float *hi, float *lo, const DevStatus *st) {
+              int nj, int sub, float *hi, float *lo, int64_t ldh, const DevStatus *st) {
   constexpr int KC = NB / KS, LD = KC + 4;   // K chunk and its shared row stride
   extern __shared__ __align__(16) float sm[];
   float *Bs = sm;                    // 32 NCQ x LD: the CTA's Bm rows (output columns, K)
@@ -635,8 +637,8 @@ rowmul_kernel(const float *In, const float *In_lo, int64_t ldi, float *Out, int6
       }
       if (hi) {
         const float h = tf32_head(v);
-        hi[gr * NB + j] = h;
-        lo[gr * NB + j] = v - h;
+        hi[gr * ldh + j] = h;
+        lo[gr * ldh + j] = v - h;
       }
     }
   }
@@ -699,10 +701,14 @@ __global__ void __launch_bounds__(256) assemble_u_kernel(const float *Yt, float 
   }
 }
 
+// A group's L panels (rows of L, TF32 head + tail) and inverse panels (rows c of Yt) side by
+// side, d x GW each, panel k in columns (k % kGroup) NB; both double buffered by group
+// parity.  Linv (the inverted diagonal block) by panel parity.
 struct PrepWs {
   DevStatus *st;
-  float *Yt, *Yhi, *Ylo;
-  float *Lhi[2], *Llo[2], *Linv[2];   // double buffered by panel parity
+  float *Yt;
+  float *Yhi[2], *Ylo[2], *Lhi[2], *Llo[2];
+  float *Linv[2];
 };
 
 PrepWs carve_prepare(void *ws, int64_t d) {
@@ -711,25 +717,42 @@ PrepWs carve_prepare(void *ws, int64_t d) {
   w.st = (DevStatus *)p;
   p += 256;
   w.Yt = (float *)p;  p += round_up((size_t)d * d * 4, 256);
-  w.Yhi = (float *)p; p += round_up((size_t)d * NB * 4, 256);
-  w.Ylo = (float *)p; p += round_up((size_t)d * NB * 4, 256);
   for (int b = 0; b < 2; ++b) {
-    w.Lhi[b] = (float *)p; p += round_up((size_t)d * NB * 4, 256);
-    w.Llo[b] = (float *)p; p += round_up((size_t)d * NB * 4, 256);
+    w.Yhi[b] = (float *)p; p += round_up((size_t)d * GW * 4, 256);
+    w.Ylo[b] = (float *)p; p += round_up((size_t)d * GW * 4, 256);
+    w.Lhi[b] = (float *)p; p += round_up((size_t)d * GW * 4, 256);
+    w.Llo[b] = (float *)p; p += round_up((size_t)d * GW * 4, 256);
     w.Linv[b] = (float *)p; p += round_up((size_t)NB * NB * 4, 256);
   }
   return w;
 }
 
-// Two streams and their events per device, created once and kept for the process: the
+// Rows [S + NB, E) of a group's inverse panels are zero in the columns of the group's
+// panels that end at or above the row (panel p covers rows c < S + (p + 1) NB only), so the
+// group's deferred product can take all its panels over rows [0, E).
+__global__ void __launch_bounds__(128) zero_group_tail_kernel(float *hi, float *lo, int64_t S,
+                                                              int64_t E) {
+  const int64_t r = S + NB + blockIdx.x;
+  if (r >= E) return;
+  const int ncols = (int)(NB * ((r - S) / NB));
+  float4 *h = reinterpret_cast<float4 *>(hi + r * GW), *l = reinterpret_cast<float4 *>(lo + r * GW);
+  for (int c = threadIdx.x; c < ncols / 4; c += blockDim.x) {
+    h[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    l[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Four streams and their events per device, created once and kept for the process: the
 // panel loop runs its critical chain on `crit` (the device's highest stream priority, so its
-// blocks are dispatched first whenever an SM has room) and the rest beside it on `s`.
+// blocks are dispatched first whenever an SM has room) and `crit2`, the panels' near updates
+// beside it on `s`, and the groups' deferred far updates on `far` (the lowest priority).
 struct SideStream {
   std::mutex enqueue;  // one panel loop at a time enqueues on these events
-  cudaStream_t s = nullptr, crit = nullptr, crit2 = nullptr;
+  cudaStream_t s = nullptr, crit = nullptr, crit2 = nullptr, far = nullptr;
   cudaEvent_t ea[2] = {nullptr, nullptr}, eb[2] = {nullptr, nullptr}, en[2] = {nullptr, nullptr},
-              ep[2] = {nullptr, nullptr}, ed[2] = {nullptr, nullptr}, e0 = nullptr, e1 = nullptr,
-              e_in = nullptr, e_out = nullptr;
+              ep[2] = {nullptr, nullptr}, ed[2] = {nullptr, nullptr}, eg[2] = {nullptr, nullptr},
+              ef[2] = {nullptr, nullptr}, e0 = nullptr, e1 = nullptr, e_in = nullptr,
+              e_out = nullptr;
   int num_sms = 0;
   GraphCache graphs;   // the panel loop captured per buffer set
 };
@@ -746,11 +769,13 @@ gptq_status side_stream(SideStream **out) {
   if (!ss.s) {
     int lo = 0, hi = 0;
     GPTQ_CUDA_CHECK(cudaDeviceGetStreamPriorityRange(&lo, &hi));
-    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, lo));
+    // priorities run from lo down to hi: crit, then crit2 one level below it, then the near
+    // updates, then the far updates at the lowest
+    const int p2 = hi < lo ? hi + 1 : hi, p3 = p2 < lo ? p2 + 1 : p2;
     GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit, cudaStreamNonBlocking, hi));
-    // one level below the critical chain (priorities run from lo down to hi)
-    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit2, cudaStreamNonBlocking,
-                                                 hi < lo ? hi + 1 : hi));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.crit2, cudaStreamNonBlocking, p2));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, p3));
+    GPTQ_CUDA_CHECK(cudaStreamCreateWithPriority(&ss.far, cudaStreamNonBlocking, lo));
     GPTQ_CUDA_CHECK(cudaDeviceGetAttribute(&ss.num_sms, cudaDevAttrMultiProcessorCount, dev));
     for (int b = 0; b < 2; ++b) {
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ea[b], cudaEventDisableTiming));
@@ -758,6 +783,8 @@ gptq_status side_stream(SideStream **out) {
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.en[b], cudaEventDisableTiming));
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ep[b], cudaEventDisableTiming));
       GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ed[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.eg[b], cudaEventDisableTiming));
+      GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.ef[b], cudaEventDisableTiming));
     }
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e0, cudaEventDisableTiming));
     GPTQ_CUDA_CHECK(cudaEventCreateWithFlags(&ss.e1, cudaEventDisableTiming));
@@ -771,28 +798,34 @@ gptq_status side_stream(SideStream **out) {
 }  // namespace
 
 size_t prepare_ws_bytes(int64_t d) {
-  return 256 + round_up((size_t)d * d * 4, 256) + 6 * round_up((size_t)d * NB * 4, 256) +
+  return 256 + round_up((size_t)d * d * 4, 256) + 8 * round_up((size_t)d * GW * 4, 256) +
          2 * round_up((size_t)NB * NB * 4, 256);
 }
 
 // Panel loop.  On the critical stream (highest priority; the caller's stream when the
-// side stream cannot be used):
+// side streams cannot be used):
 //   potrf(k) -> trsm(k) for the next NB rows -> the next panel column's update on its
 //   diagonal block (rows [k1, k1 + NB)) -> potrf(k + 1) ...
 // On a second critical stream, once potrf(k) is done: trsm(k) for the rows below, then (once
 // the critical stream's NB rows of L exist) the next column's update for those rows, beside
 // potrf(k + 1), which leaves all but one SM idle; trsm(k + 1) waits for it.  On the side
 // stream, once panel k's factor and L panel exist:
-//   inverse step a(k) -> the rest of the trailing update (the lower square from
-//   k1 + NB) -> inverse step b(k).
-// potrf(k) waits for the side stream's panel k - 2, which last wrote its diagonal block
-// and read the panel buffers it is about to overwrite.  Updates of one column block by
-// two streams are atomic adds (L2 reduce-adds in the tensor-core epilogue, red.add in the
-// next-column update); where C is not 16-byte aligned everything runs on the caller's
-// stream.  The caller's stream waits for all of them at the end.
+//   inverse step a(k) -> the rest of the trailing update (the lower trapezoid from
+//   k1 + NB) -> inverse step b(k),
+// both updates over the columns up to the end of the next group of kGroup panels only (the
+// near columns).  Once a group's last inverse panel exists, the far stream applies the
+// group's updates to the columns beyond (the far columns) as two K = GW products: the
+// output is read and written once per group instead of once per panel.  potrf(k) waits for
+// the side stream's panel k - 2, which last wrote its diagonal block and read the panel
+// buffers it is about to overwrite; a group's first potrf also waits for the far update of
+// the group two before it, the last to write its columns and to read the group buffers it
+// is about to overwrite.  Updates of one column block by several streams are atomic adds
+// (L2 reduce-adds in the tensor-core epilogue, red.add in the next-column update); where C
+// is not 16-byte aligned everything runs on the caller's stream, without deferral.  The
+// caller's stream waits for all of them at the end.
 namespace {
 
-// The panel loop's launches (no set-up, no locking): on `s`, and with `ss` on its two
+// The panel loop's launches (no set-up, no locking): on `s`, and with `ss` on its four
 // streams as well.
 gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *dead_mask,
                             void *ws, cudaStream_t s, SideStream *ss) {
@@ -802,10 +835,15 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   const size_t potrf_smem = kPotrfSmem;
   PrepWs w = carve_prepare(ws, d);
   const bool overlap = ss != nullptr;
+  const bool defer = overlap;
   cudaStream_t b = overlap ? ss->s : s;
+  cudaStream_t f = overlap ? ss->far : s;
   // the side stream's persistent GEMMs leave 16 SMs to the critical chain (measured: better
   // than all SMs, than one CTA per tile, and the same as 32)
   const int side_ctas = overlap ? std::max(1, ss->num_sms - 16) : 0;
+  // the far products are persistent too (measured: 95 against 116 ms for one CTA per tile
+  // on a 28672-wide layer, 8.3 against 9.0 ms at 11008)
+  const int far_ctas = side_ctas;
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
   // vector path: rows of H, Yt and U start 16-byte aligned (the workspace is)
   const bool vec = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0 && (((uintptr_t)U) % 16) == 0;
@@ -823,11 +861,24 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   float *A = H;  // reversed, damped Hessian; lower triangle is the Cholesky workspace
   int k = 0;
   bool next_rest = false;   // the last panel's column update left rows to the second stream
+  bool far_pending[2] = {false, false};   // by group parity: ef recorded, not yet waited on
+  bool far_any[2] = {false, false};       // by group parity: ef recorded in this call
   for (int64_t k0 = 0; k0 < d; k0 += NB, ++k) {
     const int par = k & 1;
     const int n = (int)std::min<int64_t>(NB, d - k0);
     const int64_t k1 = k0 + n;
+    const int64_t grp = k / kGroup, S = grp * GW;
+    const int gp = (int)(grp & 1), slot = k % kGroup;
+    // the near columns end with the next group; with deferral off, all columns are near
+    const int64_t near_end = defer ? std::min(d, S + 2 * GW) : d;
+    const bool far_after = defer && slot == kGroup - 1 && S + 2 * GW < d;
+    float *lhi = w.Lhi[gp] + slot * NB, *llo = w.Llo[gp] + slot * NB;
+    float *yhi = w.Yhi[gp] + slot * NB, *ylo = w.Ylo[gp] + slot * NB;
     if (overlap && k >= 2) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->eb[par], 0));
+    if (slot == 0 && far_pending[gp]) {
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, ss->ef[gp], 0));
+      far_pending[gp] = false;
+    }
     GPTQ_TRY(launch_kernel(potrf_kernel, 1, PF_THREADS, potrf_smem, c, A, d, k0, n,
                            w.Linv[par], w.st));
     if (overlap) GPTQ_CUDA_CHECK(cudaEventRecord(ss->ep[par], c));
@@ -841,19 +892,18 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
         dim3 g((unsigned)ceil_div(r1 - r0, RM_ROWS), 4);
         return launch_kernel(rowmul_kernel<1>, g, RM_THREADS, rmq_smem, st, A + k0,
                              (const float *)nullptr, d, (float *)nullptr, (int64_t)0, r0, r1,
-                             w.Linv[par], (const float *)nullptr, (int64_t)NB, n, n, 0,
-                             w.Lhi[par], w.Llo[par], w.st);
+                             w.Linv[par], (const float *)nullptr, (int64_t)NB, n, n, 0, lhi,
+                             llo, GW, w.st);
       };
       // next panel column, rows k1 + [r0, r1): A[., k1:k1+NB] -= L[.] L[k1:k1+NB]^T (fp32
       // from the head + tail panels; atomic adds: the side stream's previous trailing update
       // adds here too)
       auto next_col = [&](int64_t r0, int64_t r1, cudaStream_t st) {
         dim3 g2((unsigned)ceil_div(r1 - r0, RM_ROWS), (unsigned)ceil_div(nn, 32));
-        return launch_kernel(rowmul_kernel<1>, g2, RM_THREADS, rmq_smem, st,
-                             w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
-                             A + k1 * d + k1, d, r0, r1, w.Lhi[par] + k1 * NB,
-                             w.Llo[par] + k1 * NB, (int64_t)NB, n, nn, 1, (float *)nullptr,
-                             (float *)nullptr, w.st);
+        return launch_kernel(rowmul_kernel<1>, g2, RM_THREADS, rmq_smem, st, lhi + k1 * GW,
+                             llo + k1 * GW, GW, A + k1 * d + k1, d, r0, r1, lhi + k1 * GW,
+                             llo + k1 * GW, GW, n, nn, 1, (float *)nullptr, (float *)nullptr,
+                             (int64_t)0, w.st);
       };
       if (overlap && d - k1 > nn) {
         cudaStream_t c2 = ss->crit2;
@@ -870,10 +920,9 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
           // the next potrf's block, in four K chunks (64 CTAs; atomic adds)
           dim3 g2((unsigned)ceil_div(nn, RM_ROWS), (unsigned)ceil_div(nn, 32), 4);
           GPTQ_TRY(launch_kernel(rowmul_kernel<1, 4>, g2, RM_THREADS, rmk_smem, c,
-                                 w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB,
-                                 A + k1 * d + k1, d, (int64_t)0, (int64_t)nn,
-                                 w.Lhi[par] + k1 * NB, w.Llo[par] + k1 * NB, (int64_t)NB, n, nn,
-                                 1, (float *)nullptr, (float *)nullptr, w.st));
+                                 lhi + k1 * GW, llo + k1 * GW, GW, A + k1 * d + k1, d,
+                                 (int64_t)0, (int64_t)nn, lhi + k1 * GW, llo + k1 * GW, GW, n,
+                                 nn, 1, (float *)nullptr, (float *)nullptr, (int64_t)0, w.st));
         }
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ed[par], 0));
@@ -889,32 +938,63 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
       GPTQ_CUDA_CHECK(cudaEventRecord(ss->ea[par], c));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(b, ss->ea[par], 0));
     }
+    if (slot == 0 && defer && S + 2 * GW < d) {
+      // this group will have a far update: its inverse panels' rows below each panel are zero
+      const int64_t E = std::min(d, S + GW);
+      if (E > S + NB)
+        GPTQ_TRY(launch_kernel(zero_group_tail_kernel, (unsigned)(E - S - NB), 128, 0, b,
+                               w.Yhi[gp], w.Ylo[gp], S, E));
+    }
     // inverse step a: Yt[c][k0:k1] = Bt[c][k0:k1] Linv^T for c in [0, k1), in place
     {
       const unsigned g = (unsigned)ceil_div(k1, RM_ROWS);
       GPTQ_TRY(launch_kernel(rowmul_kernel<4>, g, RM_THREADS, rm_smem, b,
                              (const float *)(w.Yt + k0), (const float *)nullptr, d, w.Yt + k0, d,
                              (int64_t)0, k1, (const float *)w.Linv[par], (const float *)nullptr,
-                             (int64_t)NB, n, n, 0, w.Yhi, w.Ylo, w.st));
+                             (int64_t)NB, n, n, 0, yhi, ylo, GW, w.st));
+    }
+    if (far_after) {
+      // the group's far columns [S + 2 GW, d): the rest of its trailing update (lower
+      // square) and of its inverse step b (rows c < S + GW), K = GW
+      const int64_t r0 = S + 2 * GW;
+      GPTQ_CUDA_CHECK(cudaEventRecord(ss->eg[gp], b));
+      GPTQ_CUDA_CHECK(cudaStreamWaitEvent(f, ss->eg[gp], 0));
+      GemmArgs t{};
+      t.a_hi = w.Lhi[gp] + r0 * GW; t.a_lo = w.Llo[gp] + r0 * GW; t.lda = GW;
+      t.b_hi = w.Lhi[gp] + r0 * GW; t.b_lo = w.Llo[gp] + r0 * GW; t.ldb = GW;
+      t.c = A + r0 * d + r0; t.ldc = d;
+      t.M = d - r0; t.N = d - r0; t.K = GW;
+      t.alpha = -1.0f; t.lower_only = 1; t.trans_c = 0; t.max_ctas = far_ctas;
+      GPTQ_TRY(launch_gemm_nt(t, w.st, f));
+      GemmArgs v{};
+      v.a_hi = w.Yhi[gp]; v.a_lo = w.Ylo[gp]; v.lda = GW;
+      v.b_hi = w.Lhi[gp] + r0 * GW; v.b_lo = w.Llo[gp] + r0 * GW; v.ldb = GW;
+      v.c = w.Yt + r0; v.ldc = d;
+      v.M = S + GW; v.N = d - r0; v.K = GW;
+      v.alpha = -1.0f; v.lower_only = 0; v.trans_c = 0; v.max_ctas = far_ctas;
+      GPTQ_TRY(launch_gemm_nt(v, w.st, f));
+      GPTQ_CUDA_CHECK(cudaEventRecord(ss->ef[gp], f));
+      far_pending[gp] = far_any[gp] = true;
     }
     if (k1 < d) {
-      if (d - k1 > NB) {
-        // the rest of the trailing update: lower square from (k1 + NB, k1 + NB)
+      if (near_end - k1 > NB) {
+        // the rest of the trailing update: lower trapezoid from (k1 + NB, k1 + NB), near
+        // columns
         const int64_t r0 = k1 + NB;
         GemmArgs g2{};
-        g2.a_hi = w.Lhi[par] + r0 * NB; g2.a_lo = w.Llo[par] + r0 * NB; g2.lda = NB;
-        g2.b_hi = w.Lhi[par] + r0 * NB; g2.b_lo = w.Llo[par] + r0 * NB; g2.ldb = NB;
+        g2.a_hi = lhi + r0 * GW; g2.a_lo = llo + r0 * GW; g2.lda = GW;
+        g2.b_hi = lhi + r0 * GW; g2.b_lo = llo + r0 * GW; g2.ldb = GW;
         g2.c = A + r0 * d + r0; g2.ldc = d;
-        g2.M = d - r0; g2.N = d - r0; g2.K = n;
+        g2.M = d - r0; g2.N = near_end - r0; g2.K = n;
         g2.alpha = -1.0f; g2.lower_only = 1; g2.trans_c = 0; g2.max_ctas = side_ctas;
         GPTQ_TRY(launch_gemm_nt(g2, w.st, b));
       }
-      // inverse step b: Bt[c][k1:] -= Yp[c] Lp[k1:]^T for c < k1
+      // inverse step b: Bt[c][k1:near_end] -= Yp[c] Lp[k1:near_end]^T for c < k1
       GemmArgs h{};
-      h.a_hi = w.Yhi; h.a_lo = w.Ylo; h.lda = NB;
-      h.b_hi = w.Lhi[par] + k1 * NB; h.b_lo = w.Llo[par] + k1 * NB; h.ldb = NB;
+      h.a_hi = yhi; h.a_lo = ylo; h.lda = GW;
+      h.b_hi = lhi + k1 * GW; h.b_lo = llo + k1 * GW; h.ldb = GW;
       h.c = w.Yt + k1; h.ldc = d;
-      h.M = k1; h.N = d - k1; h.K = n;
+      h.M = k1; h.N = near_end - k1; h.K = n;
       h.alpha = -1.0f; h.lower_only = 0; h.trans_c = 0; h.max_ctas = side_ctas;
       GPTQ_TRY(launch_gemm_nt(h, w.st, b));
     }
@@ -926,6 +1006,8 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
     GPTQ_CUDA_CHECK(cudaEventRecord(ss->e1, c));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->e1, 0));
     for (int p = 0; p < std::min(k, 2); ++p) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->eb[p], 0));
+    for (int p = 0; p < 2; ++p)
+      if (far_any[p]) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(s, ss->ef[p], 0));
   }
   dim3 tg((unsigned)ceil_div(d, AU_T), (unsigned)ceil_div(d, AU_T));
   if (vec) assemble_u_kernel<true><<<tg, 256, 0, s>>>(w.Yt, U, d);

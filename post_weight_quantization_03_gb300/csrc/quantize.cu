@@ -2,12 +2,13 @@
 // "Greedy quantization with error compensation" and "GPTQ's speedups: fixed order and
 // lazy batches"; "GPTQ Hessian", "GPTQ: Block Structure in Quantization").
 //
-// Per block of B columns [b0, b1):
-//   sweep    : every row (one thread each, the row's B working weights in registers)
-//              quantizes columns b0..b1-1 in order, spreading each column's scaled error
-//              e_j = (w_j - q_j) / U_jj along row j of U inside the block at once;
-//              writes the codes and E = [e_b0 .. e_b1-1] (as a TF32 head/tail pair)
-//   trailing : W[:, b1:] -= E U[b0:b1, b1:]   (the deferred lazy-batch product, run as
+// Per pair of blocks of B columns [b0, b1) and [b1, b2):
+//   sweep    : every row (one thread each, the row's working weights in registers)
+//              quantizes columns b0..b2-1 in order, spreading each column's scaled error
+//              e_j = (w_j - q_j) / U_jj along row j of U inside the pair at once (the
+//              first block's errors reach the second through U[b0:b1, b1:b2]);
+//              writes the codes and E = [e_b0 .. e_b2-1] (as a TF32 head/tail pair)
+//   trailing : W[:, b2:] -= E U[b0:b2, b2:]   (the deferred lazy-batch product, run as
 //              C -= A B^T with B = U^T rows, i.e. Lt = U^T split into head/tail)
 // then one pass packs the codes and writes W_hat.
 #include <algorithm>
@@ -22,13 +23,16 @@ namespace gptq {
 namespace {
 
 constexpr int SB = 128;          // maximum block width held by one thread
-constexpr int SW_ROWS = 64;      // rows (threads) per sweep CTA
-constexpr int LDU = SB + 4;      // leading dimension of a packed U diagonal block
-constexpr int LDW = SB + 4;      // smem leading dimension of the staging tile (float4 rows
-                                 // of consecutive threads fall in distinct bank groups)
+constexpr int SW_ROWS = 64;      // rows per sweep CTA
+constexpr int LDU = SB + 4;      // leading dimension of a packed U block
+constexpr int LDW = 2 * SB + 4;  // smem leading dimension of the staging tile (a pair of
+                                 // blocks; float4 rows of consecutive threads fall in
+                                 // distinct bank groups)
 // One packed diagonal block: U[b0:b0+nb, b0:b0+nb] upper part in SB x LDU (identity
 // padding), then the SB reciprocal pivots 1 / U_jj.
 constexpr int UD_FLOATS = SB * LDU + SB;
+// One packed off-diagonal block of a pair: U[b0:b1, b1:b2] in SB x LDU (zero padding).
+constexpr int UO_FLOATS = SB * LDU;
 
 // ---------------------------------------------------------------------------------------
 // Grid: per-row asymmetric min-max with 0 in the range; fp32 working copy of W with dead
@@ -183,6 +187,27 @@ diag_blocks_kernel(const float *__restrict__ U, int64_t d, int block, float *__r
       out[SB * LDU + j] = (j < nb) ? 1.0f / U[(b0 + j) * d + (b0 + j)] : 1.0f;
 }
 
+// Packs the off-diagonal block of each pair of blocks (2p, 2p + 1) that has a second block:
+// U[a0 + i][b0 + j] for i < block, j < nbB (a0 = 2p block, b0 = a0 + block), zero
+// elsewhere in SB x LDU.  Same CTA layout as diag_blocks_kernel.
+__global__ void __launch_bounds__(256)
+offdiag_blocks_kernel(const float *__restrict__ U, int64_t d, int block, float *__restrict__ Uo) {
+  const int64_t a0 = (int64_t)blockIdx.x * 2 * block, b0 = a0 + block;
+  const int nbB = (int)((d - b0) < block ? (d - b0) : block);
+  float *out = Uo + (int64_t)blockIdx.x * UO_FLOATS;
+  constexpr int Q = LDU / 4;
+  for (int t = threadIdx.x; t < DB_ROWS * Q; t += 256) {
+    const int i = DB_ROWS * blockIdx.y + t / Q, j4 = 4 * (t % Q);
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j4 + e;
+      v[e] = (i < block && j < nbB) ? U[(a0 + i) * d + (b0 + j)] : 0.f;
+    }
+    *reinterpret_cast<float4 *>(out + i * LDU + j4) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // One column step of the in-block sweep within a 32-column sub-block, unrolled at compile
 // time over the sub-block so its working weights stay in registers:
@@ -226,183 +251,274 @@ struct SweepStep<SUB> {
 };
 
 // ---------------------------------------------------------------------------------------
-// In-block sweep over columns [b0, b0 + nb) for SW_ROWS rows per CTA, two threads per row:
-//   chain  (warps 0-1): quantizes one 32-column sub-block at a time, its working weights
-//                       in registers, and leaves the sub-block's scaled errors in the row
-//   update (warps 2-3): applies those errors to the later sub-blocks of the row: the next
-//                       sub-block first (then signals it ready), the farther ones while the
-//                       chain thread already works on the next sub-block
-// Hand-offs are named barriers (1: errors of a sub-block ready, 2: a sub-block fully
-// updated), each an arrive on one side and a sync on the other.  The packed U block
-// arrives by one bulk copy while the threads stage the working-weight tile.
+// In-block sweep over a pair of blocks, A = columns [a0, a0 + nbA) and B = [a0 + block,
+// a0 + block + nbB) (nbB = 0: A alone), for SW_ROWS rows per CTA:
+//   chain  (warps 0-1, one thread per row): quantizes one 32-column sub-block at a time, A's
+//          then B's, its working weights in registers, and leaves the sub-block's errors
+//          and codes in the row.  Then, while the update threads already take those errors
+//          on, it applies them to the next sub-block itself, as a register delta added when
+//          it loads that sub-block: the next sub-block is ready as soon as the errors two
+//          and more sub-blocks back have reached it.
+//   update (warps 2, 3, 6, 7, 10, 11, 14, 15, four threads per row, all on the two
+//          schedulers that the chain warps do not use): apply each sub-block's errors to
+//          the sub-blocks two and more ahead, the nearest first (then signal it ready), and
+//          store the sub-block's E and codes.  Errors of A reach B through the off-diagonal
+//          block U[A, B], so B is swept in the same launch with no trailing product in
+//          between.  Thread u of a row owns float4 columns u and u + 4 of every sub-block,
+//          so each column receives its updates in one fixed order.
+// The other six warps only help stage the tile.  Hand-offs are named barriers, each an arrive on
+// one side and a sync on the other; every role alternates between two ids, so the chain,
+// which may run a sub-block ahead, never arrives at an instance that is still open:
+//   1 + S % 2: errors of sub-block S ready        3 + T % 2: sub-block T has the errors of
+//                                                            all sub-blocks before T - 1
+//   5: the chain's last read of the rows of A's block that B's first copy replaces
+// A's diagonal block and the off-diagonal block arrive by bulk copies while the threads
+// stage the tile.  B's diagonal block replaces A's in two bulk copies: its leading rows once
+// only the chain's last sub-block of A still reads A's block, the rest once that is done.
 // ---------------------------------------------------------------------------------------
-constexpr int SW_THREADS = 2 * SW_ROWS;
+constexpr int SW_THREADS = 8 * SW_ROWS;   // 16 warps: 2 chain, 8 update, 6 staging only
+constexpr int SW_BAR = 5 * SW_ROWS;       // threads in each named barrier (chain + update)
+constexpr int CW = 2 * SB / 4 + 1;        // staged code words per row
 
 __device__ __forceinline__ void bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__global__ void __launch_bounds__(SW_THREADS)
-sweep_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t b0, int nb,
-             const float *__restrict__ Ud, const float *__restrict__ scale,
-             const int32_t *__restrict__ zero, float maxq, float *__restrict__ Ehi,
-             float *__restrict__ Elo, int64_t lde, uint8_t *__restrict__ codes, int64_t ldc,
-             DevStatus *st) {
+// Two float4s of a row's working weights, wa and wb: w -= sum_{k < SUB} e_k U[k][.], the U
+// rows at stride LDU from ua and ub (the float4s' columns); paired fp32 FMAs in k order.
+__device__ __forceinline__ void update2(float *wa, float *wb, const float *ua, const float *ub,
+                                        const float (&e)[SUB]) {
+  const float4 a = *reinterpret_cast<const float4 *>(wa);
+  const float4 b = *reinterpret_cast<const float4 *>(wb);
+  float2 a0 = make_float2(a.x, a.y), a1 = make_float2(a.z, a.w);
+  float2 b0 = make_float2(b.x, b.y), b1 = make_float2(b.z, b.w);
+#pragma unroll
+  for (int k = 0; k < SUB; ++k) {
+    const float4 x = *reinterpret_cast<const float4 *>(ua + k * LDU);
+    const float4 y = *reinterpret_cast<const float4 *>(ub + k * LDU);
+    const float2 ne = make_float2(-e[k], -e[k]);
+    a0 = __ffma2_rn(ne, make_float2(x.x, x.y), a0);
+    a1 = __ffma2_rn(ne, make_float2(x.z, x.w), a1);
+    b0 = __ffma2_rn(ne, make_float2(y.x, y.y), b0);
+    b1 = __ffma2_rn(ne, make_float2(y.z, y.w), b1);
+  }
+  *reinterpret_cast<float4 *>(wa) = make_float4(a0.x, a0.y, a1.x, a1.y);
+  *reinterpret_cast<float4 *>(wb) = make_float4(b0.x, b0.y, b1.x, b1.y);
+}
+
+__global__ void __launch_bounds__(SW_THREADS, 1)
+sweep_pair_kernel(const float *__restrict__ Wf, int64_t ldwf, int64_t m, int64_t a0, int nbA,
+                  int nbB, int block, const float *__restrict__ UdA,
+                  const float *__restrict__ UdB, const float *__restrict__ Uo,
+                  const float *__restrict__ scale, const int32_t *__restrict__ zero,
+                  float maxq, float *__restrict__ Ehi, float *__restrict__ Elo, int64_t lde,
+                  uint8_t *__restrict__ codes, int64_t ldc, DevStatus *st) {
   extern __shared__ __align__(16) float sm[];
-  float *Us = sm;                        // SB x LDU, then SB reciprocals
-  float *rdiag = sm + SB * LDU;
-  float *stage = sm + UD_FLOATS;         // SW_ROWS x LDW
-  uint32_t *cstage = (uint32_t *)(stage + SW_ROWS * LDW);  // SW_ROWS x (SB/4 + 1) words
-  __shared__ __align__(8) uint64_t bar;
-  const int tid = threadIdx.x;
+  float *Us = sm;                        // SB x LDU: A's diagonal block, then B's
+  float *rdA = sm + SB * LDU;            // A's SB reciprocal pivots
+  float *Uos = sm + UD_FLOATS;           // SB x LDU: U[A, B]
+  float *stage = Uos + UO_FLOATS;        // SW_ROWS x LDW: A from column 0, B from column SB
+  uint32_t *cstage = (uint32_t *)(stage + SW_ROWS * LDW);  // SW_ROWS x CW words
+  float *rdB = (float *)(cstage + SW_ROWS * CW);           // B's SB reciprocal pivots
+  __shared__ __align__(8) uint64_t bar[3];   // A's blocks; B's leading rows; B's other rows
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int64_t r0 = (int64_t)blockIdx.x * SW_ROWS;
+  const int nsA = (nbA + SUB - 1) / SUB, nsB = (nbB + SUB - 1) / SUB, nS = nsA + nsB;
+  const int R1 = (nsA - 1) * SUB;        // B's leading rows: those the first copy brings
   if (tid == 0) {
-    tc::mbar_init(&bar, 1);
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&bar[i], 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(&bar, UD_FLOATS * 4);
-    tc::bulk_load(Us, Ud, UD_FLOATS * 4, &bar);
+    tc::mbar_arrive_expect_tx(&bar[0], (UD_FLOATS + (nsB ? UO_FLOATS : 0)) * 4);
+    tc::bulk_load(Us, UdA, UD_FLOATS * 4, &bar[0]);
+    if (nsB) tc::bulk_load(Uos, Uo, UO_FLOATS * 4, &bar[0]);
   }
   __syncthreads();
-  // working weights, coalesced; float4 when the tile rows are 16-byte aligned
-  if ((b0 % 4) == 0 && (ldwf % 4) == 0) {
-#pragma unroll 8
-    for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
-      const int e = it * SW_THREADS + tid;   // float4 index in the tile
-      const int r = e / (SB / 4), q = e % (SB / 4);
+  // working weights, coalesced, zero beyond each block's width; float4 when the tile rows
+  // and both blocks start on 16-byte boundaries
+  if ((a0 % 4) == 0 && (ldwf % 4) == 0 && (block % 4) == 0) {
+#pragma unroll 4
+    for (int e = tid; e < SW_ROWS * (2 * SB / 4); e += SW_THREADS) {
+      const int r = e / (2 * SB / 4), q = e % (2 * SB / 4);
+      const int h = q / (SB / 4), c = 4 * (q % (SB / 4));   // block of the pair, column
+      const int nb = h ? nbB : nbA;
       const int64_t gr = r0 + r;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (gr < m && 4 * q < nb) v = *reinterpret_cast<const float4 *>(Wf + gr * ldwf + b0 + 4 * q);
-      if (4 * q + 4 > nb) {  // ragged last block: clear columns >= nb
-        if (4 * q + 0 >= nb) v.x = 0.f;
-        if (4 * q + 1 >= nb) v.y = 0.f;
-        if (4 * q + 2 >= nb) v.z = 0.f;
-        if (4 * q + 3 >= nb) v.w = 0.f;
+      if (gr < m && c < nb) {
+        v = *reinterpret_cast<const float4 *>(Wf + gr * ldwf + a0 + h * block + c);
+        if (c + 1 >= nb) v.y = 0.f;
+        if (c + 2 >= nb) v.z = 0.f;
+        if (c + 3 >= nb) v.w = 0.f;
       }
-      *reinterpret_cast<float4 *>(stage + r * LDW + 4 * q) = v;
+      *reinterpret_cast<float4 *>(stage + r * LDW + h * SB + c) = v;
     }
   } else {
-#pragma unroll 16
-    for (int it = 0; it < SW_ROWS * SB / SW_THREADS; ++it) {
-      const int e = it * SW_THREADS + tid;
-      const int r = e / SB, j = e % SB;
+#pragma unroll 4
+    for (int e = tid; e < SW_ROWS * 2 * SB; e += SW_THREADS) {
+      const int r = e / (2 * SB), q = e % (2 * SB);
+      const int h = q / SB, j = q % SB;
       const int64_t gr = r0 + r;
-      stage[r * LDW + j] = (gr < m && j < nb) ? Wf[gr * ldwf + b0 + j] : 0.f;
+      stage[r * LDW + q] =
+          (gr < m && j < (h ? nbB : nbA)) ? Wf[gr * ldwf + a0 + h * block + j] : 0.f;
     }
   }
-  const int got = tc::mbar_wait(&bar, 0, st) ? 1 : 0;
+  const int got = tc::mbar_wait(&bar[0], 0, st) ? 1 : 0;
   if (!__syncthreads_and(got)) return;  // CTA-uniform: later barriers stay matched
-  const int role = tid / SW_ROWS, rl = tid % SW_ROWS;
-  float *my = stage + rl * LDW;         // this row of the block
-  if (role == 0) {
+  int ok = 1;                           // every wait for B's diagonal block succeeded
+  if (warp < 2) {
     // ---------------- chain ----------------
-    const int64_t row = r0 + rl;
+    float *my = stage + tid * LDW;      // this row of the pair
+    const int64_t row = r0 + tid;
     const float s = row < m ? scale[row] : 1.f;
     const float z = row < m ? (float)zero[row] : 0.f;
-#pragma unroll 1
-    for (int sb = 0; sb < SB / SUB; ++sb) {
-      const int c0 = sb * SUB;
-      if (sb > 0) tc::named_barrier(2, SW_THREADS);  // sub-block sb fully updated
-      float2 wp[SUB / 2];
+    float2 wp[SUB / 2], dn[SUB / 2];
 #pragma unroll
-      for (int q = 0; q < SUB / 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
-        wp[2 * q] = make_float2(v.x, v.y);
-        wp[2 * q + 1] = make_float2(v.z, v.w);
+    for (int i = 0; i < SUB / 2; ++i) wp[i] = *reinterpret_cast<const float2 *>(my + 2 * i);
+#pragma unroll 1
+    for (int S = 0; S < nS; ++S) {
+      const int h = S >= nsA, sb = h ? S - nsA : S, c0 = sb * SUB;
+      float *w = my + h * SB + c0;
+      if (S > 0) {
+        if (S >= 2) tc::named_barrier(3 + S % 2, SW_BAR);   // errors up to S - 2 applied
+        if (h && sb == 0 && nsA >= 2) ok &= tc::mbar_wait(&bar[1], 0, st) ? 1 : 0;
+        if (h && (sb == nsA - 1 || sb == nsB - 1)) ok &= tc::mbar_wait(&bar[2], 0, st) ? 1 : 0;
+        // the stage's sub-block plus the delta of the errors of sub-block S - 1
+#pragma unroll
+        for (int i = 0; i < SUB / 2; ++i) {
+          const float2 v = *reinterpret_cast<const float2 *>(w + 2 * i);
+          wp[i] = make_float2(v.x + dn[i].x, v.y + dn[i].y);
+        }
       }
       uint32_t cw[SUB / 4];
 #pragma unroll
       for (int i = 0; i < SUB / 4; ++i) cw[i] = 0u;
-      SweepStep<0>::run(wp, cw, Us + c0 * LDU + c0, rdiag + c0, s, z, maxq);
+      SweepStep<0>::run(wp, cw, Us + c0 * LDU + c0, (h ? rdB : rdA) + c0, s, z, maxq);
 #pragma unroll
-      for (int q = 0; q < SUB / 4; ++q)
-        *reinterpret_cast<float4 *>(my + c0 + 4 * q) =
-            make_float4(wp[2 * q].x, wp[2 * q].y, wp[2 * q + 1].x, wp[2 * q + 1].y);
+      for (int i = 0; i < SUB / 2; ++i) *reinterpret_cast<float2 *>(w + 2 * i) = wp[i];
 #pragma unroll
-      for (int i = 0; i < SUB / 4; ++i) cstage[rl * (SB / 4 + 1) + sb * (SUB / 4) + i] = cw[i];
-      bar_arrive(1, SW_THREADS);                   // errors of sub-block sb ready
-    }
-  } else {
-    // ---------------- update ----------------
-#pragma unroll 1
-    for (int sb = 0; sb < SB / SUB; ++sb) {
-      tc::named_barrier(1, SW_THREADS);            // errors of sub-block sb
-      if (sb == SB / SUB - 1) break;
-      const int c0 = sb * SUB;
-      float e[SUB];
+      for (int i = 0; i < SUB / 4; ++i) cstage[tid * CW + h * (SB / 4) + c0 / 4 + i] = cw[i];
+      bar_arrive(1 + S % 2, SW_BAR);                 // errors of sub-block S ready
+      if (S + 1 < nS) {
+        // the next sub-block's delta: dn_k = -sum_J e_J U[J][k], J in order
+        const int hn = (S + 1) >= nsA, cn = (hn ? S + 1 - nsA : S + 1) * SUB;
+        const float *Un = (hn == h ? Us : Uos) + c0 * LDU + cn;
 #pragma unroll
-      for (int q = 0; q < SUB / 4; ++q) {
-        const float4 v = *reinterpret_cast<const float4 *>(my + c0 + 4 * q);
-        e[4 * q] = v.x; e[4 * q + 1] = v.y; e[4 * q + 2] = v.z; e[4 * q + 3] = v.w;
-      }
-      //   w_c -= sum_k e_k U[c0 + k][c], next sub-block first (paired fp32 FMAs)
-#pragma unroll 1
-      for (int c = c0 + SUB; c < SB; c += 4) {
-        const float4 a = *reinterpret_cast<const float4 *>(my + c);
-        float2 lo = make_float2(a.x, a.y), hi = make_float2(a.z, a.w);
+        for (int i = 0; i < SUB / 2; ++i) dn[i] = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int J = 0; J < SUB; ++J) {
+          const float e = w[J];                       // the error just stored
+          const float2 ne = make_float2(-e, -e);
 #pragma unroll
-        for (int k = 0; k < SUB; ++k) {
-          const float4 u = *reinterpret_cast<const float4 *>(Us + (c0 + k) * LDU + c);
-          const float2 ne = make_float2(-e[k], -e[k]);
-          lo = __ffma2_rn(ne, make_float2(u.x, u.y), lo);
-          hi = __ffma2_rn(ne, make_float2(u.z, u.w), hi);
+          for (int k = 0; k < SUB; k += 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(Un + J * LDU + k);
+            dn[k >> 1] = __ffma2_rn(ne, make_float2(x.x, x.y), dn[k >> 1]);
+            dn[(k >> 1) + 1] = __ffma2_rn(ne, make_float2(x.z, x.w), dn[(k >> 1) + 1]);
+          }
         }
-        *reinterpret_cast<float4 *>(my + c) = make_float4(lo.x, lo.y, hi.x, hi.y);
-        if (c + 4 == c0 + 2 * SUB) bar_arrive(2, SW_THREADS);  // sub-block sb + 1 ready
+        // that delta read the last rows of A's block that B's first copy replaces
+        if (nsB && S == nsA - 2) bar_arrive(5, SW_ROWS + 32);
+      }
+    }
+  } else if ((warp & 3) >= 2) {
+    // ---------------- update ----------------
+    const int v = 2 * (warp >> 2) + (warp & 1);      // 0 .. 7
+    const int rl = 32 * (v & 1) + lane, u = v >> 1, ut = 32 * v + lane;
+    float *my = stage + rl * LDW;
+    const bool evec = ((uintptr_t)Ehi % 16) == 0 && ((uintptr_t)Elo % 16) == 0 &&
+                      (lde % 4) == 0 && (block % 4) == 0;
+    const bool cvec = (a0 % 4) == 0 && (ldc % 4) == 0 && (block % 4) == 0;
+    bool waited = false;
+#pragma unroll 1
+    for (int S = 0; S < nS; ++S) {
+      tc::named_barrier(1 + S % 2, SW_BAR);          // errors of sub-block S ready
+      const int h = S >= nsA, sb = h ? S - nsA : S, c0 = sb * SUB, nb = h ? nbB : nbA;
+      if (nsB && S == nsA - 2 && warp == 2) tc::named_barrier(5, SW_ROWS + 32);  // chain's delta
+      if (nsB && ut == 0 && (S == nsA - 2 || S == nsA - 1)) {
+        // every read of these rows of A's diagonal block is done: B's replace them
+        tc::fence_proxy_async_smem();
+        if (S == nsA - 2) {
+          tc::mbar_arrive_expect_tx(&bar[1], (R1 * LDU + SB) * 4);
+          tc::bulk_load(Us, UdB, R1 * LDU * 4, &bar[1]);
+          tc::bulk_load(rdB, UdB + SB * LDU, SB * 4, &bar[1]);
+        } else {
+          tc::mbar_arrive_expect_tx(&bar[2], ((SB - R1) * LDU + (nsA == 1 ? SB : 0)) * 4);
+          tc::bulk_load(Us + R1 * LDU, UdB + R1 * LDU, (SB - R1) * LDU * 4, &bar[2]);
+          if (nsA == 1) tc::bulk_load(rdB, UdB + SB * LDU, SB * 4, &bar[2]);
+        }
+      }
+      if (S + 2 < nS) {
+        if (h && !waited) {                          // B's leading rows of its block
+          ok &= tc::mbar_wait(&bar[1], 0, st) ? 1 : 0;
+          waited = true;
+        }
+        float e[SUB];
+#pragma unroll
+        for (int q = 0; q < SUB / 4; ++q) {
+          const float4 x = *reinterpret_cast<const float4 *>(my + h * SB + c0 + 4 * q);
+          e[4 * q] = x.x; e[4 * q + 1] = x.y; e[4 * q + 2] = x.z; e[4 * q + 3] = x.w;
+        }
+#pragma unroll 1
+        for (int T = S + 2; T < nS; ++T) {
+          const int ht = T >= nsA, t0 = (ht ? T - nsA : T) * SUB;
+          const float *Ub = (ht == h ? Us : Uos) + c0 * LDU + t0;
+          float *wt = my + ht * SB + t0;
+          update2(wt + 4 * u, wt + 4 * (u + 4), Ub + 4 * u, Ub + 4 * (u + 4), e);
+          if (T == S + 2) bar_arrive(3 + S % 2, SW_BAR);   // sub-block S + 2 ready
+        }
+      }
+      // sub-block S's E (a TF32 head/tail pair, at column h * block + c0 of the pair
+      // buffer) and codes, coalesced: float4 / whole words when aligned
+      if (evec) {
+#pragma unroll
+        for (int i = 0; i < SW_ROWS * (SUB / 4) / 256; ++i) {
+          const int qi = ut + 256 * i, r = qi / (SUB / 4), c = c0 + 4 * (qi % (SUB / 4));
+          const int64_t gr = r0 + r;
+          if (gr < m && c < nb) {
+            float4 x = *reinterpret_cast<const float4 *>(stage + r * LDW + h * SB + c);
+            if (c + 1 >= nb) x.y = 0.f;
+            if (c + 2 >= nb) x.z = 0.f;
+            if (c + 3 >= nb) x.w = 0.f;
+            const float4 hd = make_float4(tf32_head(x.x), tf32_head(x.y), tf32_head(x.z), tf32_head(x.w));
+            *reinterpret_cast<float4 *>(Ehi + gr * lde + h * block + c) = hd;
+            *reinterpret_cast<float4 *>(Elo + gr * lde + h * block + c) =
+                make_float4(x.x - hd.x, x.y - hd.y, x.z - hd.z, x.w - hd.w);
+          }
+        }
+      } else {
+        for (int i = ut; i < SW_ROWS * SUB; i += 256) {
+          const int r = i / SUB, c = c0 + i % SUB;
+          const int64_t gr = r0 + r;
+          if (gr < m && c < nb) {
+            const float x = stage[r * LDW + h * SB + c], hd = tf32_head(x);
+            Ehi[gr * lde + h * block + c] = hd;
+            Elo[gr * lde + h * block + c] = x - hd;
+          }
+        }
+      }
+      if (cvec) {
+#pragma unroll
+        for (int i = 0; i < SW_ROWS * (SUB / 4) / 256; ++i) {
+          const int wi = ut + 256 * i, r = wi / (SUB / 4), wq = wi % (SUB / 4), c = c0 + 4 * wq;
+          const int64_t gr = r0 + r;
+          if (gr < m && c < nb) {
+            uint32_t x = cstage[r * CW + h * (SB / 4) + c / 4];
+            if (c + 4 > nb) x &= (1u << (8 * (nb - c))) - 1u;   // ragged block end
+            *reinterpret_cast<uint32_t *>(codes + gr * ldc + a0 + h * block + c) = x;
+          }
+        }
+      } else {
+        const uint8_t *cb = (const uint8_t *)cstage;
+        for (int i = ut; i < SW_ROWS * SUB; i += 256) {
+          const int r = i / SUB, c = c0 + i % SUB;
+          const int64_t gr = r0 + r;
+          if (gr < m && c < nb) codes[gr * ldc + a0 + h * block + c] = cb[r * CW * 4 + h * SB + c];
+        }
       }
     }
   }
-  __syncthreads();
-  // E (now in the stage rows) -> global as a TF32 head/tail pair, coalesced: its nb columns
-  // (float4 stores when E's rows start on 16-byte boundaries, single floats otherwise)
-  if (((uintptr_t)Ehi % 16) != 0 || ((uintptr_t)Elo % 16) != 0 || (lde % 4) != 0) {
-    for (int e = tid; e < SW_ROWS * SB; e += SW_THREADS) {
-      const int r = e / SB, j = e % SB;
-      const int64_t gr = r0 + r;
-      if (gr < m && j < nb) {
-        const float v = stage[r * LDW + j], h = tf32_head(v);
-        Ehi[gr * lde + j] = h;
-        Elo[gr * lde + j] = v - h;
-      }
-    }
-  } else
-#pragma unroll 4
-  for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
-    const int e = it * SW_THREADS + tid;
-    const int r = e / (SB / 4), q = e % (SB / 4);
-    const int64_t gr = r0 + r;
-    if (gr < m && 4 * q < nb) {
-      float4 v = *reinterpret_cast<const float4 *>(stage + r * LDW + 4 * q);
-      if (4 * q + 0 >= nb) v.x = 0.f;
-      if (4 * q + 1 >= nb) v.y = 0.f;
-      if (4 * q + 2 >= nb) v.z = 0.f;
-      if (4 * q + 3 >= nb) v.w = 0.f;
-      const float4 h = make_float4(tf32_head(v.x), tf32_head(v.y), tf32_head(v.z), tf32_head(v.w));
-      *reinterpret_cast<float4 *>(Ehi + gr * lde + 4 * q) = h;
-      *reinterpret_cast<float4 *>(Elo + gr * lde + 4 * q) =
-          make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
-    }
-  }
-  // codes: staged as words (4 codes each), stored coalesced; whole words when the block
-  // starts on a 4-column boundary, bytes otherwise
-  if ((b0 % 4) == 0 && (ldc % 4) == 0) {
-#pragma unroll 4
-    for (int it = 0; it < SW_ROWS * SB / 4 / SW_THREADS; ++it) {
-      const int e = it * SW_THREADS + tid;
-      const int r = e / (SB / 4), wq = e % (SB / 4);
-      const int64_t gr = r0 + r;
-      if (gr < m && 4 * wq < nb) {
-        uint32_t v = cstage[r * (SB / 4 + 1) + wq];
-        if (4 * wq + 4 > nb) v &= (1u << (8 * (nb - 4 * wq))) - 1u;  // ragged block end
-        *reinterpret_cast<uint32_t *>(codes + gr * ldc + b0 + 4 * wq) = v;
-      }
-    }
-  } else {
-    const uint8_t *cb = (const uint8_t *)cstage;
-    for (int e = tid; e < SW_ROWS * SB; e += SW_THREADS) {
-      const int r = e / SB, j = e % SB;
-      const int64_t gr = r0 + r;
-      if (gr < m && j < nb) codes[gr * ldc + b0 + j] = cb[r * (SB / 4 + 1) * 4 + j];
-    }
+  if (!__syncthreads_and(ok) && tid == 0 && nsB) {
+    // a wait ran out (TIMEOUT recorded): give the copies in flight one more bounded wait
+    if (nsA >= 2) tc::mbar_wait(&bar[1], 0, nullptr);
+    tc::mbar_wait(&bar[2], 0, nullptr);
   }
 }
 
@@ -657,10 +773,15 @@ gptq_status launch_lt_split(const float *U, int64_t d, float *hi, float *lo, int
   return GPTQ_OK;
 }
 
-gptq_status launch_diag_blocks(const float *U, int64_t d, int block, float *Ud, cudaStream_t s) {
-  diag_blocks_kernel<<<dim3((unsigned)ceil_div(d, block), SB / DB_ROWS), 256, 0, s>>>(U, d, block,
-                                                                                     Ud);
+gptq_status launch_diag_blocks(const float *U, int64_t d, int block, float *Ud, float *Uo,
+                               cudaStream_t s) {
+  const int64_t nblk = ceil_div(d, block);
+  diag_blocks_kernel<<<dim3((unsigned)nblk, SB / DB_ROWS), 256, 0, s>>>(U, d, block, Ud);
   GPTQ_LAUNCH_CHECK();
+  if (nblk >= 2) {
+    offdiag_blocks_kernel<<<dim3((unsigned)(nblk / 2), SB / DB_ROWS), 256, 0, s>>>(U, d, block, Uo);
+    GPTQ_LAUNCH_CHECK();
+  }
   return GPTQ_OK;
 }
 
@@ -695,7 +816,7 @@ struct QuantWs {
   float *Ehi, *Elo;
   float *Lhi, *Llo; int64_t ldl;
   uint8_t *codes; int64_t ldc;
-  float *Ud;
+  float *Ud, *Uo;       // packed diagonal blocks; off-diagonal block of each pair
   float *Ehi2, *Elo2;   // second E pair buffer
   int64_t lde;          // E row stride: two blocks side by side (a pair of blocks)
 };
@@ -717,6 +838,8 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   q.Ud = (float *)p;
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
   p += block > 1 ? nblk * UD_FLOATS * 4 : 0;
+  q.Uo = (float *)p;
+  p += block > 1 ? (nblk / 2) * UO_FLOATS * 4 : 0;
   q.Ehi2 = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
   q.Elo2 = (float *)p;
   return q;
@@ -732,8 +855,9 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
   const size_t lde = block > 1 ? 2 * SB : SB;
   return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * lde * 4, 256) +
          2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
-         (block > 1 ? nblk * UD_FLOATS * 4 + 2 * round_up((size_t)m * lde * 4, 256)
-                    : 0);   // B = 1 needs neither packed diagonal blocks nor a second E pair
+         (block > 1 ? nblk * UD_FLOATS * 4 + (nblk / 2) * UO_FLOATS * 4 +
+                          2 * round_up((size_t)m * lde * 4, 256)
+                    : 0);   // B = 1 needs neither packed U blocks nor a second E pair
 }
 
 namespace {
@@ -818,7 +942,7 @@ size_t quantize_layers_ws_bytes(const int64_t *m, int n, int64_t d, int bits, in
 // outputs.  With one layer the per-row scale and zero are written in place.
 namespace {
 
-constexpr size_t kSweepSmem = (UD_FLOATS + SW_ROWS * LDW + SW_ROWS * (SB / 4 + 1)) * sizeof(float);
+constexpr size_t kSweepSmem = (UD_FLOATS + UO_FLOATS + SW_ROWS * LDW + SW_ROWS * CW + SB) * sizeof(float);
 
 // The sweep's launches (no set-up, no locking): on `s`, and with `qs` the blocked sweep's
 // far updates on qs->side and the rest on qs->crit (which is `s` itself when the whole
@@ -844,7 +968,7 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
   if (overlap) {
     GPTQ_CUDA_CHECK(cudaEventRecord(qs->fork, s));
     GPTQ_CUDA_CHECK(cudaStreamWaitEvent(qs->side, qs->fork, 0));
-    GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, qs->side));
+    GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, q.Uo, qs->side));
     GPTQ_CUDA_CHECK(cudaEventRecord(qs->ud_done, qs->side));
     GPTQ_TRY(launch_lt_split(U, d, q.Lhi, q.Llo, q.ldl, qs->side));
     GPTQ_CUDA_CHECK(cudaEventRecord(qs->lt_done, qs->side));
@@ -863,18 +987,17 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       GPTQ_LAUNCH_CHECK();
     }
   } else {
-    // blocked: in-block sweep, then one rank-B trailing update per block
+    // blocked: the pairs of blocks, each swept in one launch, then one trailing update of
+    // depth up to 2B per pair
     if (!overlap) {
       GPTQ_TRY(launch_lt_split(U, d, q.Lhi, q.Llo, q.ldl, s));
-      GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, s));
+      GPTQ_TRY(launch_diag_blocks(U, d, block, q.Ud, q.Uo, s));
     }
     const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
-    // Blocks are taken in pairs (2p, 2p + 1) for the trailing update: the E of both blocks
-    // of pair p sit side by side in buffer p % 2 (block 2p + h at column h * block), so one
-    // product of depth up to 2B applies the pair to every column past it.  Block 2p's own
-    // update reaches only the next block (2p + 1), which is swept before the pair's product.
-    // Every column thus receives the contributions of earlier blocks in the same order and
-    // grouping in both schedules below (the results are bit for bit the same).
+    // The E of both blocks of pair p sit side by side in buffer p % 2 (block 2p + h at
+    // column h * block), so one product of depth up to 2B applies the pair to every column
+    // past it.  Every column thus receives the contributions of earlier pairs in the same
+    // order and grouping in both schedules below (the results are bit for bit the same).
     // W[:, c0:c1] -= E U[kb0:kb0+K, c0:c1] with E the first K columns of pair buffer e
     auto update = [&](int e, int64_t kb0, int K, int64_t c0, int64_t c1, int max_ctas,
                       cudaStream_t st) -> gptq_status {
@@ -887,30 +1010,36 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       g.one_sum = 1;   // one TMEM sum per tile: the codes need no shorter sums
       return launch_gemm_nt(g, q.st, st);
     };
-    auto sweep = [&](int64_t b0, int nb, int e, int h, cudaStream_t st) -> gptq_status {
-      return launch_kernel(sweep_kernel, sweep_grid, SW_THREADS, sweep_smem, st,
-                           (const float *)q.Wf, q.ldwf, m, b0, nb,
-                           (const float *)(q.Ud + (b0 / block) * UD_FLOATS),
+    // pair p: blocks 2p ([a0, a0 + nbA)) and 2p + 1 ([a0 + block, + nbB), nbB = 0 if none)
+    auto sweep = [&](int64_t p, int nbA, int nbB, cudaStream_t st) -> gptq_status {
+      const int64_t a0 = 2 * p * block;
+      const int e = (int)(p & 1);
+      return launch_kernel(sweep_pair_kernel, sweep_grid, SW_THREADS, sweep_smem, st,
+                           (const float *)q.Wf, q.ldwf, m, a0, nbA, nbB, block,
+                           (const float *)(q.Ud + 2 * p * UD_FLOATS),
+                           (const float *)(q.Ud + (nbB ? 2 * p + 1 : 2 * p) * UD_FLOATS),
+                           (const float *)(q.Uo + (nbB ? p : 0) * UO_FLOATS),
                            (const float *)scale, (const int32_t *)zero, maxq,
-                           (e ? q.Ehi2 : q.Ehi) + h * block, (e ? q.Elo2 : q.Elo) + h * block,
-                           q.lde, q.codes, q.ldc, q.st);
+                           e ? q.Ehi2 : q.Ehi, e ? q.Elo2 : q.Elo, q.lde, q.codes, q.ldc, q.st);
     };
+    auto widths = [&](int64_t p, int &nbA, int &nbB) {
+      const int64_t a0 = 2 * p * block, b0 = a0 + block;
+      nbA = (int)std::min<int64_t>(block, d - a0);
+      nbB = b0 < d ? (int)std::min<int64_t>(block, d - b0) : 0;
+    };
+    const int64_t npairs = ceil_div(d, 2 * (int64_t)block);
     if (!overlap) {
-      int k = 0;
-      for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
-        const int e = (k >> 1) & 1, h = k & 1;
-        const int nb = (int)((d - b0) < block ? (d - b0) : block);
-        const int64_t b1 = b0 + nb;
-        GPTQ_TRY(sweep(b0, nb, e, h, s));
-        if (b1 < d) {
-          if (h == 0) GPTQ_TRY(update(e, b0, nb, b1, std::min<int64_t>(b1 + block, d), 0, s));
-          else GPTQ_TRY(update(e, b0 - block, block + nb, b1, d, 0, s));
-        }
+      for (int64_t p = 0; p < npairs; ++p) {
+        int nbA, nbB;
+        widths(p, nbA, nbB);
+        const int64_t a0 = 2 * p * block, pe = a0 + (nbB ? block + nbB : nbA);
+        GPTQ_TRY(sweep(p, nbA, nbB, s));
+        if (pe < d) GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), pe, d, 0, s));
       }
     } else {
       // After pair p its product splits two blocks on: those two blocks' columns on the
       // critical stream right after the sweep, the far columns on the side stream, where they
-      // have two sweeps and two near updates' time before the sweep that needs them.  Pair
+      // have a pair sweep and a near update's time before the sweep that needs them.  Pair
       // p's near update waits for pair p - 1's far update, which keeps each column's
       // contributions in the single-stream order and frees the pair buffer pair p + 1 reuses.
       cudaStream_t c = qs->crit, sd = qs->side;
@@ -924,27 +1053,23 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->start, 0));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->ud_done, 0));   // the first sweep
       bool lt_waited = false;                                     // the first update on c
-      int k = 0;
-      for (int64_t b0 = 0; b0 < d; b0 += block, ++k) {
-        const int p = k >> 1, e = p & 1, h = k & 1;
-        const int nb = (int)((d - b0) < block ? (d - b0) : block);
-        const int64_t b1 = b0 + nb;
-        GPTQ_TRY(sweep(b0, nb, e, h, c));
-        if (b1 >= d) break;
+      for (int64_t p = 0; p < npairs; ++p) {
+        int nbA, nbB;
+        widths(p, nbA, nbB);
+        const int e = (int)(p & 1);
+        const int64_t a0 = 2 * p * block, pe = a0 + (nbB ? block + nbB : nbA);
+        GPTQ_TRY(sweep(p, nbA, nbB, c));
+        if (pe >= d) break;
         if (!lt_waited) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->lt_done, 0));
         lt_waited = true;
-        if (h == 0) {
-          // block 2p -> block 2p + 1
-          GPTQ_TRY(update(e, b0, nb, b1, std::min<int64_t>(b1 + block, d), 0, c));
-        } else {
-          const int64_t f0 = std::min<int64_t>(b1 + 2 * block, d);   // far columns [f0, d)
-          GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
-          if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
-          GPTQ_TRY(update(e, b0 - block, block + nb, b1, f0, 0, c));   // the next two blocks
-          GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
-          if (f0 < d) GPTQ_TRY(update(e, b0 - block, block + nb, f0, d, far_ctas, sd));
-          GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
-        }
+        const int K = (int)(pe - a0);
+        const int64_t f0 = std::min<int64_t>(pe + 2 * block, d);   // far columns [f0, d)
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
+        if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
+        GPTQ_TRY(update(e, a0, K, pe, f0, 0, c));                  // the next two blocks
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
+        if (f0 < d) GPTQ_TRY(update(e, a0, K, f0, d, far_ctas, sd));
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
       }
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->crit_done, c));
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->side_done, sd));
@@ -973,7 +1098,7 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
 gptq_status launch_quantize_layers(const QLayer *L, int n, int64_t d, const float *U,
                                    const uint8_t *dead_mask, int bits, int block, void *ws,
                                    cudaStream_t s, bool allow_overlap) {
-  GPTQ_TRY(ensure_smem_attr((const void *)sweep_kernel, (int)kSweepSmem));
+  GPTQ_TRY(ensure_smem_attr((const void *)sweep_pair_kernel, (int)kSweepSmem));
   if (!allow_overlap || block == 1 || d <= 2 * (int64_t)block)
     return enqueue_quantize_layers(L, n, d, U, dead_mask, bits, block, ws, s, nullptr);
   QuantStreams *qs = nullptr;

@@ -60,10 +60,18 @@ struct TcGemmParams {
   int n_tiles;          // tiles to process (lower ones only when lower_only)
 };
 
-// Linear tile index -> (tm, tn): row-major over the tile grid, or over its lower
-// triangle (tm >= tn) when lower_only.
+// Linear tile index -> (tm, tn): row-major over the tile grid, or, when lower_only, over
+// its lower trapezoid (tm >= tn): the triangle of the first n_n tile rows, then the whole
+// tile rows below it.
 __device__ __forceinline__ void tile_coords(const TcGemmParams &p, int t, int &tm, int &tn) {
   if (p.lower_only) {
+    const int tri = p.n_n * (p.n_n + 1) / 2;
+    if (t >= tri) {
+      t -= tri;
+      tm = p.n_n + t / p.n_n;
+      tn = t % p.n_n;
+      return;
+    }
     int r = (int)((sqrtf(8.0f * (float)t + 1.0f) - 1.0f) * 0.5f);
     while (r * (r + 1) / 2 > t) --r;
     while ((r + 1) * (r + 2) / 2 <= t) ++r;
@@ -500,8 +508,8 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   p.c = g.c; p.ldc = g.ldc; p.alpha = g.alpha;
   p.n_m = (int)ceil_div(g.M, BM);
   p.n_n = (int)ceil_div(g.N, BN);
-  p.lower_only = g.lower_only && g.M == g.N;
-  p.n_tiles = p.lower_only ? p.n_n * (p.n_n + 1) / 2 : p.n_m * p.n_n;
+  p.lower_only = g.lower_only && g.M >= g.N;
+  p.n_tiles = p.lower_only ? p.n_n * (p.n_n + 1) / 2 + (p.n_m - p.n_n) * p.n_n : p.n_m * p.n_n;
   const int cap = g.max_ctas < 0 ? p.n_tiles
                   : (g.max_ctas > 0 && g.max_ctas < num_sms) ? g.max_ctas : num_sms;
   const int grid = p.n_tiles < cap ? p.n_tiles : cap;
