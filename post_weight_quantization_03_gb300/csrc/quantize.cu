@@ -1045,9 +1045,12 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       cudaStream_t c = qs->crit, sd = qs->side;
       int nsm = 0;
       GPTQ_TRY(device_sm_count(&nsm));
-      // the far update (persistent) leaves one SM per sweep CTA: measured better than
-      // sharing SMs two sweep CTAs each, and than one CTA per tile over all SMs
-      const int far_ctas = std::max(1, nsm - (int)std::min<unsigned>(sweep_grid, nsm / 2));
+      // the far update (persistent): up to d_in = 4096 it leaves one SM per sweep CTA, which
+      // measured better than sharing SMs two sweep CTAs each and than one CTA per tile over
+      // all SMs; on wide layers the far products are most of the work and take every SM
+      // (measured at d_in = 28672: 35.9 against 56.9 ms; 11008: 3.83 against 3.95 ms)
+      const int far_ctas = d >= 8192 ? 0
+                                     : std::max(1, nsm - (int)std::min<unsigned>(sweep_grid, nsm / 2));
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->start, s));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->start, 0));
       GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->start, 0));
