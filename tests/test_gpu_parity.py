@@ -61,6 +61,11 @@ def _codes(qpacked, bits, d):
     (512, 2048, "bf16", 5, 4),
     (1024, 4096, "f16", 10, 8),
     (130, 64, "f16", 0, 0),
+    # more tiles than SMs: the last round's tiles are cut into token ranges that add to H
+    (3200, 2048, "f16", 4, 3),      # 169 tiles, 17 of them split
+    (4096, 1000, "bf16", 0, 0),     # 272 tiles, 16 stages: one stage per token range
+    (4000, 640, "f16", 2, 1),       # ragged channels; 10 stages: some token ranges empty
+    (3998, 512, "f16", 0, 0),       # rows of H not 16-byte aligned: scalar adds
 ])
 def test_hessian_parity(d, n, dtype, dead, outl):
     spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=dead, n_outlier=outl, seed=d + n)
@@ -99,6 +104,19 @@ def test_hessian_accumulates_over_chunks(dtype):
     gptq.hessian(X[4096:], H, accumulate=True)
     Hr = O.hessian(X.cpu().float().numpy())
     assert PT.rel_fro(H.cpu().numpy(), Hr) <= PT.TOL_H
+
+
+def test_hessian_token_ranges_accumulate_over_chunks():
+    # 182 tiles of 128 x 256: 30 of them in token ranges, added onto the earlier chunks' H
+    spec = S.ActivationSpec(d_in=3328, n_tok=3000, dtype="f16", n_dead=3, n_outlier=2, seed=78)
+    X = _x(spec).to(DEV)
+    H = gptq.hessian(X[:1024])
+    gptq.hessian(X[1024:2500], H, accumulate=True)
+    gptq.hessian(X[2500:], H, accumulate=True)
+    Hr = O.hessian(X.cpu().float().numpy())
+    Hg = H.cpu().numpy()
+    assert PT.rel_fro(Hg, Hr) <= PT.TOL_H
+    assert np.array_equal(Hg, Hg.T)
 
 
 def test_hessian_zero_tokens():
