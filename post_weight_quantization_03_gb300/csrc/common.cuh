@@ -147,6 +147,8 @@ struct GemmArgs {
                   // (the sweep's updates); 0 = head products in sums of two 32-wide K
                   // stages and the cross products apart (the factorization's updates,
                   // whose accuracy needs the short sums)
+  int wide;       // tensor-core path, one-sum products that are not triangles: 256-wide
+                  // output tiles (fewer operand bytes per product; half the tiles)
 };
 gptq_status launch_gemm_nt(const GemmArgs &g, DevStatus *st, cudaStream_t s);
 // tc_gemm.cu: the tcgen05 3xTF32 kernel; UNSUPPORTED when the operands do not meet its

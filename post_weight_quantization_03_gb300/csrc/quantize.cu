@@ -995,12 +995,13 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
     }
     const unsigned sweep_grid = (unsigned)ceil_div(m, SW_ROWS);
     // The E of both blocks of pair p sit side by side in buffer p % 2 (block 2p + h at
-    // column h * block), so one product of depth up to 2B applies the pair to every column
-    // past it.  Every column thus receives the contributions of earlier pairs in the same
-    // order and grouping in both schedules below (the results are bit for bit the same).
+    // column h * block), so one product of depth up to 2B applies the pair to the columns
+    // past it: the next two blocks' columns in 128-wide tiles, the rest in 256-wide ones.
+    // Every column thus receives the contributions of earlier pairs in the same order,
+    // grouping and kernel in both schedules below (the results are bit for bit the same).
     // W[:, c0:c1] -= E U[kb0:kb0+K, c0:c1] with E the first K columns of pair buffer e
     auto update = [&](int e, int64_t kb0, int K, int64_t c0, int64_t c1, int max_ctas,
-                      cudaStream_t st) -> gptq_status {
+                      cudaStream_t st, int wide) -> gptq_status {
       GemmArgs g{};
       g.a_hi = e ? q.Ehi2 : q.Ehi; g.a_lo = e ? q.Elo2 : q.Elo; g.lda = q.lde;
       g.b_hi = q.Lhi + c0 * q.ldl + kb0; g.b_lo = q.Llo + c0 * q.ldl + kb0; g.ldb = q.ldl;
@@ -1008,6 +1009,7 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       g.M = m; g.N = c1 - c0; g.K = K;
       g.alpha = -1.0f; g.lower_only = 0; g.trans_c = 0; g.max_ctas = max_ctas;
       g.one_sum = 1;   // one TMEM sum per tile: the codes need no shorter sums
+      g.wide = wide;
       return launch_gemm_nt(g, q.st, st);
     };
     // pair p: blocks 2p ([a0, a0 + nbA)) and 2p + 1 ([a0 + block, + nbB), nbB = 0 if none)
@@ -1034,7 +1036,12 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
         widths(p, nbA, nbB);
         const int64_t a0 = 2 * p * block, pe = a0 + (nbB ? block + nbB : nbA);
         GPTQ_TRY(sweep(p, nbA, nbB, s));
-        if (pe < d) GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), pe, d, 0, s));
+        if (pe < d) {
+          // the same column split and kernels as the two-stream schedule below
+          const int64_t f0 = std::min<int64_t>(pe + 2 * block, d);
+          GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), pe, f0, 0, s, 0));
+          if (f0 < d) GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), f0, d, 0, s, 1));
+        }
       }
     } else {
       // After pair p its product splits two blocks on: those two blocks' columns on the
@@ -1069,9 +1076,10 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
         const int64_t f0 = std::min<int64_t>(pe + 2 * block, d);   // far columns [f0, d)
         GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
         if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
-        GPTQ_TRY(update(e, a0, K, pe, f0, 0, c));                  // the next two blocks
+        GPTQ_TRY(update(e, a0, K, pe, f0, 0, c, 0));               // the next two blocks
         GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
-        if (f0 < d) GPTQ_TRY(update(e, a0, K, f0, d, far_ctas, sd));
+        // the far columns in 256-wide tiles
+        if (f0 < d) GPTQ_TRY(update(e, a0, K, f0, d, far_ctas, sd, 1));
         GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
       }
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->crit_done, c));

@@ -84,11 +84,13 @@ __device__ __forceinline__ void tile_coords(const TcGemmParams &p, int t, int &t
 }
 
 // TMA producer (one lane): 4 operand tiles per 32-wide K stage, running ahead across tile
-// boundaries through the kStages ring.
+// boundaries through the STAGES ring; output tiles BM x BNT.
+template <int BNT, int STAGES>
 __device__ __forceinline__ void produce(const CUtensorMap *ma_hi, const CUtensorMap *ma_lo,
                                         const CUtensorMap *mb_hi, const CUtensorMap *mb_lo,
                                         const TcGemmParams &p, uint8_t *smem, uint64_t *full,
                                         uint64_t *empty, int ktiles, DevStatus *st) {
+  constexpr uint32_t tile_b = BNT * BK * 4, stage_bytes = 2 * kTileA + 2 * tile_b;
   tc::tma_prefetch_desc(ma_hi);
   tc::tma_prefetch_desc(ma_lo);
   tc::tma_prefetch_desc(mb_hi);
@@ -97,17 +99,17 @@ __device__ __forceinline__ void produce(const CUtensorMap *ma_hi, const CUtensor
   for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
     int tm, tn;
     tile_coords(p, t, tm, tn);
-    const int32_t m0 = tm * BM, n0 = tn * BN;
+    const int32_t m0 = tm * BM, n0 = tn * BNT;
     for (int kt = 0; kt < ktiles; ++kt, ++g) {
-      const int s = g % kStages;
-      if (g >= kStages && !tc::mbar_wait(&empty[s], ((g / kStages) - 1) & 1, st)) return;
-      uint8_t *base = smem + s * kStageBytes;
-      tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+      const int s = g % STAGES;
+      if (g >= STAGES && !tc::mbar_wait(&empty[s], ((g / STAGES) - 1) & 1, st)) return;
+      uint8_t *base = smem + s * stage_bytes;
+      tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
       const int32_t k0 = kt * BK;
       tc::tma_load_2d(base, ma_hi, k0, m0, &full[s]);
       tc::tma_load_2d(base + kTileA, ma_lo, k0, m0, &full[s]);
       tc::tma_load_2d(base + 2 * kTileA, mb_hi, k0, n0, &full[s]);
-      tc::tma_load_2d(base + 2 * kTileA + kTileB, mb_lo, k0, n0, &full[s]);
+      tc::tma_load_2d(base + 2 * kTileA + tile_b, mb_lo, k0, n0, &full[s]);
     }
   }
 }
@@ -196,7 +198,7 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    produce(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
+    produce<BN, kStages>(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
@@ -320,21 +322,27 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
   if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
-// One TMEM sum per tile (the sweep's updates): two 128-column tile accumulators used in
+// One TMEM sum per tile (the sweep's updates): two BNT-column tile accumulators used in
 // turn, so the next tile's MMAs overlap this tile's epilogue; the epilogue stages each
-// 64-column half straight from its TMEM loads and releases the accumulator after the second.
+// 64-column part straight from its TMEM loads and releases the accumulator after the last.
+// BNT = 128 (three stages of 64 KB) or 256 (two of 96 KB: per MMA the same A tile feeds
+// twice the columns, so a quarter fewer operand bytes cross shared memory per product).
+template <int BNT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
                        const __grid_constant__ CUtensorMap ma_lo,
                        const __grid_constant__ CUtensorMap mb_hi,
                        const __grid_constant__ CUtensorMap mb_lo,
                        const __grid_constant__ CUtensorMap mc, TcGemmParams p, DevStatus *st) {
+  constexpr int STAGES = BNT == 256 ? 2 : kStages;
+  constexpr uint32_t tile_b = BNT * BK * 4, stage_bytes = 2 * kTileA + 2 * tile_b;
+  static_assert(1024 + STAGES * stage_bytes + kStagingBytes + 256 <= kSmemBytes, "smem");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *staging = smem + kStages * kStageBytes;
+  uint8_t *staging = smem + STAGES * stage_bytes;
   uint64_t *full = (uint64_t *)(staging + kStagingBytes);
-  uint64_t *empty = full + kStages;
-  uint64_t *tfull = empty + kStages;   // [2] accumulator ready
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;    // [2] accumulator ready
   uint64_t *tempty = tfull + 2;        // [2] accumulator drained
   uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
   int *epi_ok = (int *)(tmem_slot + 1);
@@ -347,7 +355,7 @@ tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
   const int ktiles = (int)((p.K + BK - 1) / BK);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -357,17 +365,17 @@ tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
     }
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * BN);
+  if (warp == 1) tc::tmem_alloc(tmem_slot, 2 * BNT);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    produce(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
+    produce<BNT, STAGES>(&ma_hi, &ma_lo, &mb_hi, &mb_lo, p, smem, full, empty, ktiles, st);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BN, 0, 0);
+    constexpr uint32_t idesc = tc::instr_desc(2, 2, BM, BNT, 0, 0);
     int g = 0, it = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
@@ -377,16 +385,16 @@ tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
         if (!ok) break;
         tc::tc_fence_after();
       }
-      const uint32_t dt = tmem + (uint32_t)(b * BN);
+      const uint32_t dt = tmem + (uint32_t)(b * BNT);
       for (int kt = 0; kt < ktiles; ++kt, ++g) {
-        const int s = g % kStages;
-        ok = tc::mbar_wait(&full[s], (g / kStages) & 1, st);
+        const int s = g % STAGES;
+        ok = tc::mbar_wait(&full[s], (g / STAGES) & 1, st);
         if (!ok) break;
         tc::tc_fence_after();
-        const uint32_t a_hi = tc::smem_u32(smem + s * kStageBytes);
+        const uint32_t a_hi = tc::smem_u32(smem + s * stage_bytes);
         const uint32_t a_lo = a_hi + kTileA;
         const uint32_t b_hi = a_hi + 2 * kTileA;
-        const uint32_t b_lo = b_hi + kTileB;
+        const uint32_t b_lo = b_hi + tile_b;
 #pragma unroll
         for (int kk = 0; kk < BK / 8; ++kk) {  // 8 tf32 = 32 bytes per MMA
           const uint32_t off = kk * 32;
@@ -416,16 +424,16 @@ tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
       tc::tc_fence_after();
       int tm, tn;
       tile_coords(p, t, tm, tn);
-      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BN;
+      const int64_t m0 = (int64_t)tm * BM, n0 = (int64_t)tn * BNT;
       const int64_t row = m0 + rl;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < BNT / 64; ++h) {
         uint32_t r0[32], r1[32];
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + h * 64);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BNT + h * 64);
         tc::tmem_ld32(ta, r0);
         tc::tmem_ld32(ta + 32, r1);
         tc::tmem_ld_wait();
-        if (h == 1) {  // this warp's reads of the accumulator are done: release it
+        if (h == BNT / 64 - 1) {  // this warp's reads of the accumulator are done: release it
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&tempty[b]);
@@ -443,7 +451,7 @@ tc_gemm_one_sum_kernel(const __grid_constant__ CUtensorMap ma_hi,
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 2 * BN);
+  if (warp == 1) tc::tmem_dealloc(tmem, 2 * BNT);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -488,13 +496,18 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return GPTQ_OK;
   if (!g.a_lo || !g.b_lo) return GPTQ_ERR_UNSUPPORTED;
   GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_short_sums_kernel, (int)kSmemBytes));
-  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_one_sum_kernel, (int)kSmemBytes));
+  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_one_sum_kernel<BN>, (int)kSmemBytes));
+  GPTQ_TRY(ensure_smem_attr((const void *)tc_gemm_one_sum_kernel<2 * BN>, (int)kSmemBytes));
+  // 256-wide tiles for one-sum products that ask for them (not for triangles: their
+  // diagonal tiles are square)
+  const bool wide = g.one_sum && g.wide && !g.lower_only;
+  const int bnt = wide ? 2 * BN : BN;
   CUtensorMap mah, mal, mbh, mbl;
   // maps cover exactly the [M, K] / [N, K] operand windows: out-of-range reads are zero
   if (!make_tmap_f32(&mah, g.a_hi, g.M, g.K, g.lda, BM) ||
       !make_tmap_f32(&mal, g.a_lo, g.M, g.K, g.lda, BM) ||
-      !make_tmap_f32(&mbh, g.b_hi, g.N, g.K, g.ldb, BN) ||
-      !make_tmap_f32(&mbl, g.b_lo, g.N, g.K, g.ldb, BN))
+      !make_tmap_f32(&mbh, g.b_hi, g.N, g.K, g.ldb, bnt) ||
+      !make_tmap_f32(&mbl, g.b_lo, g.N, g.K, g.ldb, bnt))
     return GPTQ_ERR_UNSUPPORTED;
   CUtensorMap mc;
   memset(&mc, 0, sizeof(mc));
@@ -507,14 +520,16 @@ gptq_status launch_gemm_nt_tc(const GemmArgs &g, DevStatus *st, cudaStream_t s) 
   p.M = g.M; p.N = g.N; p.K = g.K;
   p.c = g.c; p.ldc = g.ldc; p.alpha = g.alpha;
   p.n_m = (int)ceil_div(g.M, BM);
-  p.n_n = (int)ceil_div(g.N, BN);
+  p.n_n = (int)ceil_div(g.N, bnt);
   p.lower_only = g.lower_only && g.M >= g.N;
   p.n_tiles = p.lower_only ? p.n_n * (p.n_n + 1) / 2 + (p.n_m - p.n_n) * p.n_n : p.n_m * p.n_n;
   const int cap = g.max_ctas < 0 ? p.n_tiles
                   : (g.max_ctas > 0 && g.max_ctas < num_sms) ? g.max_ctas : num_sms;
   const int grid = p.n_tiles < cap ? p.n_tiles : cap;
-  GPTQ_TRY(launch_kernel(g.one_sum ? tc_gemm_one_sum_kernel : tc_gemm_short_sums_kernel, grid,
-                         kThreads, kSmemBytes, s, mah, mal, mbh, mbl, mc, p, st));
+  GPTQ_TRY(launch_kernel(!g.one_sum ? tc_gemm_short_sums_kernel
+                         : wide     ? tc_gemm_one_sum_kernel<2 * BN>
+                                    : tc_gemm_one_sum_kernel<BN>,
+                         grid, kThreads, kSmemBytes, s, mah, mal, mbh, mbl, mc, p, st));
   return GPTQ_OK;
 }
 
