@@ -514,6 +514,10 @@ def main():
                              f" GB per step",
                        "parallelism": f"replicas x{world} (independent layers)"},
             "stages_ms": {"hessian": st_h, "prepare": st_p, "quantize": st_q},
+            # the quantize-only time (dead columns and damping through packing, the Hessian
+            # left out: it is usually spread over the calibration passes)
+            "quantize_only": {"ms": st_p + st_q, "unit": UNIT,
+                              "value": whole_job_value(weights, world, st_p + st_q)},
             "roofline": roofline, "roofline_stages": stages, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(launches), "clocks": clk,
         }
