@@ -20,10 +20,15 @@ namespace {
 
 constexpr size_t kChunkBytes = (size_t)64 << 20;
 
+// Default chunk: about kChunkBytes of X, but at least kMinChunkTokens tokens: every chunk's
+// products read and write all of H, so wide layers need long chunks (at d_in = 28672, 64 MiB
+// would be 1024 tokens, and H's 6.6 GB of traffic per chunk would outweigh its products).
+constexpr int64_t kMinChunkTokens = 8192;
+
 int64_t chunk_tokens(size_t row_bytes, int64_t chunk_tok) {
   if (chunk_tok > 0) return chunk_tok;
   const int64_t t = (int64_t)(kChunkBytes / row_bytes) / 512 * 512;
-  return t < 512 ? 512 : t;
+  return t < kMinChunkTokens ? kMinChunkTokens : t;
 }
 
 struct CopyStream {
