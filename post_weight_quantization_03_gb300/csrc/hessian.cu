@@ -94,32 +94,52 @@ hessian_simt_kernel(const T *__restrict__ X, int64_t n_tok, int64_t d, int64_t l
 
 
 // ---------------------------------------------------------------------------------------
-// tcgen05 SYRK: one CTA per 128 x 256 tile of H on or below the diagonal.
-//   operand tiles are token-major slices of X (MN-major for the MMA: channels contiguous)
-//   warp 0      : TMA producer, 64 tokens per stage (2 + 4 boxes of 64 ch x 64 tok)
-//   warp 1      : TMEM allocator (2 x 256 columns) + MMA issuer
-//   warps 2..9  : drain TMEM segments into fp32 registers, then write H and its mirror
-// All CTAs of a wave walk the tokens in the same order, so each chunk of X is fetched from
-// HBM about once per wave and served to the other tiles from L2.
+// tcgen05 SYRK on CTA pairs: one cluster of two CTAs (two SMs) per 256 x 256 tile of H on
+// or below the diagonal, one cta_group::2 MMA stream for the pair.  CTA r of the pair holds
+// the tile's rows 128 r .. 128 r + 127 (its A half) and columns 128 r .. 128 r + 127 (its B
+// half) of each 64-token stage, and its half of the accumulator (128 rows x 256 columns) in
+// its own TMEM.  Per SM and stage that is 32 KB of X written into shared memory and 8 KB
+// read by the tensor core per 16 tokens, against 48 KB and 12 KB for a 128 x 256 tile on
+// one SM with the same output per SM.
+//   warp 0      : TMA producer of this CTA's halves; both CTAs' copies complete on the
+//                 even CTA's stage barrier
+//   warp 1      : TMEM allocator (2 x 256 columns, both SMs); in the even CTA the MMA
+//                 issuer, whose commits arrive on the barriers of both CTAs
+//   warps 2..9  : drain this SM's TMEM segments into fp32 registers (the accumulator
+//                 buffer is free again once both CTAs' drains have arrived on the even
+//                 CTA's barrier), then write H and its mirror
+// All clusters of a wave walk the tokens in the same order, so each chunk of X is fetched
+// from HBM about once per wave and served to the other tiles from L2.
+//
+// Balanced last round: when the tiles do not fill a whole number of rounds of the SM pairs,
+// each tile of the last, partial round is cut at one token stage into a head and a tail.
+// The heads run beside the first batch of tails on the pairs the partial round leaves idle,
+// the later batches of tails follow on the same pairs, and the cut is placed so that the
+// heads and the k batches of tails end together: a round of about k/(k+1) tile-times
+// instead of one.  The heads walk the same tokens in step, and so does each batch of tails, so X stays
+// shared through L2.  Head and tail add into H, which the launcher zeroes first (only
+// calls that overwrite H are cut, so the sum 0 + head + tail is the same in either order).
 // ---------------------------------------------------------------------------------------
-constexpr int TB_M = 128, TB_N = 256, TB_K = 64;
-constexpr int T_STAGES = 4;
-constexpr uint32_t T_BOX = 64 * TB_K * 2;                 // 8 KB
-constexpr uint32_t T_TILE_A = 2 * T_BOX;                  // 16 KB
-constexpr uint32_t T_TILE_B = 4 * T_BOX;                  // 32 KB
-constexpr uint32_t T_STAGE = T_TILE_A + T_TILE_B;         // 48 KB
+constexpr int TB_M = 128, TB_N = 256, TB_K = 64;      // per-CTA rows, tile columns, tokens
+constexpr int T_STAGES = 6;
+constexpr uint32_t T_BOX = 64 * TB_K * 2;                 // 8 KB: 64 channels x 64 tokens
+constexpr uint32_t T_HALF = 2 * T_BOX;                    // 16 KB: 128 channels
+constexpr uint32_t T_STAGE = 2 * T_HALF;                  // A half + B half: 32 KB
 constexpr int T_EPI_WARPS = 8;
 constexpr int T_THREADS = 64 + 32 * T_EPI_WARPS;          // 320
 constexpr size_t T_SMEM = 1024 + T_STAGES * T_STAGE + 256;
 
 struct HessTcParams {
   int64_t d, n_tok;
-  int n_row_blocks;   // ceil(d / 128)
+  int n_blocks;       // ceil(d / 256)
   int seg_stages;     // stages (of 64 tokens) per accumulation segment
   float *H;
   int accumulate;
   uint64_t wait_ns;   // budget of every mbarrier wait
-  int lost_stage;     // test hook: the producer issues nothing for this stage (-1: none)
+  int lost_stage;     // test hook: the producers issue nothing for this stage (-1: none)
+  int full_tiles;     // units [0, full_tiles): whole tiles, written with plain stores
+  int cut_tiles;      // then cut_tiles heads and cut_tiles tails (atomic adds)
+  int cut_stage;      // first token stage of a tail
 };
 
 template <int FMT>  // 0 = fp16, 1 = bf16
@@ -127,25 +147,40 @@ __global__ void __launch_bounds__(T_THREADS, 1)
 hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevStatus *st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t *full = (uint64_t *)(smem + T_STAGES * T_STAGE);
-  uint64_t *empty = full + T_STAGES;
-  uint64_t *tfull = empty + T_STAGES;   // [2]: accumulator buffer ready to drain
-  uint64_t *tempty = tfull + 2;         // [2]: accumulator buffer drained
-  uint32_t *tmem_slot = (uint32_t *)(tempty + 2);
+  uint64_t *full = (uint64_t *)(smem + T_STAGES * T_STAGE);   // even CTA's: both halves in
+  uint64_t *empty = full + T_STAGES;    // each CTA's: stage consumed by the pair's MMAs
+  uint64_t *tfull = empty + T_STAGES;   // [2] each CTA's: accumulator buffer ready to drain
+  uint64_t *tempty = tfull + 2;         // [2] even CTA's: buffer drained by both CTAs
+  uint64_t *mdone = tempty + 2;         // even CTA's: every MMA it issued has completed
+  uint32_t *tmem_slot = (uint32_t *)(mdone + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // tile index -> (row block ib, column block jb): column blocks in order, rows 2jb..
-  int ib = 0, jb = 0;
+  const uint32_t rank = tc::cluster_ctarank();
+  // unit -> tile and token stages [g0, g1)
+  const int total_all = (int)((p.n_tok + TB_K - 1) / TB_K);
+  int tile = blockIdx.x / 2, g0 = 0, g1 = total_all;
+  bool add = false;
+  if (tile >= p.full_tiles + p.cut_tiles) {
+    tile -= p.cut_tiles;
+    g0 = p.cut_stage;
+    add = true;
+  } else if (tile >= p.full_tiles) {
+    g1 = p.cut_stage;
+    add = true;
+  }
+  // tile index -> (row block I, column block J), I >= J: column blocks in order
+  int I = 0, J = 0;
   {
-    int idx = blockIdx.x;
-    for (jb = 0;; ++jb) {
-      const int cnt = p.n_row_blocks - 2 * jb;
-      if (idx < cnt) { ib = 2 * jb + idx; break; }
+    int idx = tile;
+    for (J = 0;; ++J) {
+      const int cnt = p.n_blocks - J;
+      if (idx < cnt) { I = J + idx; break; }
       idx -= cnt;
     }
   }
-  const int64_t m0 = (int64_t)ib * TB_M, n0 = (int64_t)jb * TB_N;
-  const int total = (int)((p.n_tok + TB_K - 1) / TB_K);
+  const int64_t m0 = (int64_t)I * 2 * TB_M + rank * TB_M;      // this CTA's rows
+  const int64_t n0 = (int64_t)J * TB_N;                        // the tile's columns
+  const int total = g1 - g0;   // stages of this unit
   const int nseg = (total + p.seg_stages - 1) / p.seg_stages;
 
   if (threadIdx.x == 0) {
@@ -155,18 +190,20 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], T_EPI_WARPS);
+      tc::mbar_init(&tempty[b], 2 * T_EPI_WARPS);
     }
+    tc::mbar_init(mdone, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, 512);
+  if (warp == 1) tc::tmem_alloc_pair(tmem_slot, 512);
   tc::tc_fence_before();
-  __syncthreads();
+  tc::cluster_sync();          // both CTAs' barriers initialised, TMEM allocated
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&mx);
+    const uint32_t full0 = tc::mapa_shared(tc::smem_u32(full), 0);
     for (int g = 0; g < total; ++g) {
       const int s = g % T_STAGES;
       if (g >= T_STAGES &&
@@ -174,23 +211,24 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
         break;
       if (g == p.lost_stage) continue;   // test hook: no copy and no arrival for this stage
       uint8_t *a = smem + s * T_STAGE;
-      uint8_t *b = a + T_TILE_A;
-      const int32_t t0 = g * TB_K;
-      tc::mbar_arrive_expect_tx(&full[s], T_STAGE);
-      tc::tma_load_2d(a, &mx, (int32_t)m0, t0, &full[s]);
-      tc::tma_load_2d(a + T_BOX, &mx, (int32_t)m0 + 64, t0, &full[s]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        tc::tma_load_2d(b + q * T_BOX, &mx, (int32_t)n0 + 64 * q, t0, &full[s]);
+      uint8_t *b = a + T_HALF;
+      const int32_t t0 = (g0 + g) * TB_K;
+      const int32_t nb = (int32_t)(n0 + rank * TB_M);
+      const uint32_t bar = full0 + (uint32_t)(s * sizeof(uint64_t));
+      if (rank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * T_STAGE);
+      tc::tma_load_2d_pair(a, &mx, (int32_t)m0, t0, bar);
+      tc::tma_load_2d_pair(a + T_BOX, &mx, (int32_t)m0 + 64, t0, bar);
+      tc::tma_load_2d_pair(b, &mx, nb, t0, bar);
+      tc::tma_load_2d_pair(b + T_BOX, &mx, nb + 64, t0, bar);
     }
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = tc::instr_desc(FMT, FMT, TB_M, TB_N, 1, 1);
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    constexpr uint32_t idesc = tc::instr_desc(FMT, FMT, 2 * TB_M, TB_N, 1, 1);
     int g = 0;
     bool ok = true;
     for (int sg = 0; sg < nseg && ok; ++sg) {
       const int buf = sg & 1;
       if (sg >= 2) {
-        ok = tc::mbar_wait(&tempty[buf], ((sg / 2) - 1) & 1, st, p.wait_ns);
+        ok = tc::mbar_wait_cluster(&tempty[buf], ((sg / 2) - 1) & 1, st, p.wait_ns);
         if (!ok) break;
         tc::tc_fence_after();
       }
@@ -202,19 +240,23 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
         if (!ok) break;
         tc::tc_fence_after();
         const uint32_t a = tc::smem_u32(smem + s * T_STAGE);
-        const uint32_t b = a + T_TILE_A;
+        const uint32_t b = a + T_HALF;
 #pragma unroll
         for (int kk = 0; kk < TB_K / 16; ++kk) {  // 16 tokens = 2048 bytes per MMA
           const uint64_t da = tc::smem_desc_sw128(a + kk * 2048, T_BOX, 1024);
           const uint64_t db = tc::smem_desc_sw128(b + kk * 2048, T_BOX, 1024);
-          tc::mma_f16(dt, da, db, idesc, (first && kk == 0) ? 0u : 1u);
+          tc::mma_f16_pair(dt, da, db, idesc, (first && kk == 0) ? 0u : 1u);
         }
-        tc::mma_commit(&empty[s]);
+        tc::mma_commit_pair(&empty[s], 3);
       }
-      tc::mma_commit(&tfull[buf]);   // segment complete (or abandoned after a timeout)
+      tc::mma_commit_pair(&tfull[buf], 3);   // segment complete (or abandoned after a timeout)
     }
+    // nothing of this CTA's MMAs may still be running when the pair's TMEM is released
+    tc::mma_commit_pair(mdone, 1);
+    tc::mbar_wait(mdone, 0, st, p.wait_ns);
   } else if (warp >= 2) {
     const int e = warp - 2, q = warp & 3, h = e / 4;
+    const uint32_t tempty0 = tc::mapa_shared(tc::smem_u32(tempty), 0);
     float acc[128];
 #pragma unroll
     for (int i = 0; i < 128; ++i) acc[i] = 0.f;
@@ -238,11 +280,21 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+      if (lane == 0) tc::mbar_arrive_cluster(tempty0 + (uint32_t)(buf * sizeof(uint64_t)));
     }
     const int64_t r = m0 + q * 32 + lane;
     const int64_t d = p.d;
-    if (ok && r < d) {
+    if (ok && r < d && add) {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const int64_t c = n0 + h * 128 + i;
+        if (c < d && c <= r) {
+          const float v = 2.0f * acc[i];
+          atomicAdd(&p.H[r * d + c], v);
+          if (c != r) atomicAdd(&p.H[c * d + r], v);
+        }
+      }
+    } else if (ok && r < d) {
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
         const int64_t c = n0 + h * 128 + i;
@@ -255,9 +307,11 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
       }
     }
   }
+  __syncwarp();
   tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  tc::cluster_sync();          // neither CTA leaves while the other may still signal it
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc_pair(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -507,20 +561,58 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
   HessTcParams p{};
   p.d = d;
   p.n_tok = n_tok;
-  p.n_row_blocks = (int)ceil_div(d, TB_M);
+  p.n_blocks = (int)ceil_div(d, TB_N);
   p.seg_stages = kSegTokens / TB_K;
   p.H = H;
   p.accumulate = accumulate;
   p.wait_ns = wait_ns;
   p.lost_stage = lost_stage;
-  const int ncb = (int)ceil_div(d, TB_N);
-  int64_t tiles = 0;
-  for (int j = 0; j < ncb; ++j) tiles += std::max(0, p.n_row_blocks - 2 * j);
-  if (xdtype == GPTQ_F16)
-    hessian_tc_kernel<0><<<(unsigned)tiles, T_THREADS, T_SMEM, s>>>(mx, p, st);
-  else
-    hessian_tc_kernel<1><<<(unsigned)tiles, T_THREADS, T_SMEM, s>>>(mx, p, st);
-  GPTQ_LAUNCH_CHECK();
+  const int64_t tiles = (int64_t)p.n_blocks * (p.n_blocks + 1) / 2;
+  const int total = (int)ceil_div(n_tok, TB_K);
+  p.full_tiles = (int)tiles;
+  p.cut_tiles = 0;
+  p.cut_stage = total;
+  if (!accumulate && lost_stage < 0) {
+    int nsm = 0;
+    GPTQ_TRY(device_sm_count(&nsm));
+    const int64_t pairs = nsm / 2;
+    const int64_t r = tiles % pairs, rounds = tiles / pairs + (r ? 1 : 0);
+    if (r > 0 && pairs > r) {
+      const int64_t k = ceil_div(r, pairs - r);     // batches of tails per idle pair
+      // heads and k batches of tails end together: head = k rho / (1 + k rho) of the tokens,
+      // in whole accumulation segments, where rho = 1.1 is the time of a tail's token stage
+      // relative to a head's (measured at d = 4096: 429 against 390 ns; the tails share
+      // their tokens through L2 with fewer tiles)
+      const int64_t nsegs = ceil_div(total, p.seg_stages);
+      const int64_t head_segs = (nsegs * 11 * k + (10 + 11 * k) / 2) / (10 + 11 * k);
+      // worth it when the last round shrinks by at least 2 % of the whole call
+      if (head_segs >= 1 && head_segs < nsegs && nsegs >= 8 && 50 * (nsegs - head_segs) >= rounds * nsegs) {
+        p.full_tiles = (int)(tiles - r);
+        p.cut_tiles = (int)r;
+        p.cut_stage = (int)(head_segs * p.seg_stages);
+        GPTQ_CUDA_CHECK(cudaMemsetAsync(H, 0, (size_t)(d * d) * sizeof(float), s));
+      }
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * (tiles + p.cut_tiles)));
+  cfg.blockDim = dim3(T_THREADS);
+  cfg.dynamicSmemBytes = T_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = xdtype == GPTQ_F16 ? cudaLaunchKernelEx(&cfg, hessian_tc_kernel<0>, mx, p, st)
+                                           : cudaLaunchKernelEx(&cfg, hessian_tc_kernel<1>, mx, p, st);
+  count_launch();
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GPTQ_ERR_CUDA;
+  }
   return GPTQ_OK;
 }
 

@@ -46,8 +46,9 @@ constexpr uint32_t kTileA = BM * BK * 4;  // 16 KB
 constexpr uint32_t kTileB = BN * BK * 4;  // 16 KB
 constexpr uint32_t kStageBytes = 2 * kTileA + 2 * kTileB;
 constexpr uint32_t kStagingBytes = 2 * BM * 128;  // two 32-column boxes (one 64-col half)
-constexpr uint32_t kTmemCols = 4 * BN;            // 2 head + 2 cross accumulators: 512
+constexpr uint32_t kTmemCols = 4 * BN;            // 3 head + 1 cross accumulators: 512
 constexpr int kHeadGroup = 2;                     // K stages per head-product TMEM sum
+constexpr int kHeadBufs = 3;                      // head-product accumulators used in turn
 constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + kStagingBytes + 256;
 
 struct TcGemmParams {
@@ -165,11 +166,11 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
   uint8_t *staging = smem + kStages * kStageBytes;
   uint64_t *full = (uint64_t *)(staging + kStagingBytes);
   uint64_t *empty = full + kStages;
-  uint64_t *hfull = empty + kStages;    // [2] head-product accumulator ready
-  uint64_t *hempty = hfull + 2;         // [2] head-product accumulator drained
-  uint64_t *xfull = hempty + 2;         // [2] cross-product accumulator ready (per tile)
-  uint64_t *xempty = xfull + 2;         // [2] cross-product accumulator drained
-  uint32_t *tmem_slot = (uint32_t *)(xempty + 2);
+  uint64_t *hfull = empty + kStages;        // [3] head-product accumulator ready
+  uint64_t *hempty = hfull + kHeadBufs;     // [3] head-product accumulator drained
+  uint64_t *xfull = hempty + kHeadBufs;     // cross-product accumulator ready (per tile)
+  uint64_t *xempty = xfull + 1;             // cross-product accumulator drained
+  uint32_t *tmem_slot = (uint32_t *)(xempty + 1);
 
   __shared__ int s_skip;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -183,12 +184,12 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kHeadBufs; ++b) {
       tc::mbar_init(&hfull[b], 1);
       tc::mbar_init(&hempty[b], 4);  // one arrival per epilogue warp
-      tc::mbar_init(&xfull[b], 1);
-      tc::mbar_init(&xempty[b], 4);
     }
+    tc::mbar_init(xfull, 1);
+    tc::mbar_init(xempty, 4);
     tc::mbar_fence_init();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -205,19 +206,18 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
     int g = 0, hg = 0, it = 0, hb = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++it) {
-      const int xb = it & 1;
-      if (it >= 2) {
-        ok = tc::mbar_wait(&xempty[xb], ((it / 2) - 1) & 1, st);
+      if (it >= 1) {   // the previous tile's cross sum drained
+        ok = tc::mbar_wait(xempty, (it - 1) & 1, st);
         if (!ok) break;
         tc::tc_fence_after();
       }
-      const uint32_t dx = tmem + (uint32_t)((2 + xb) * BN);
+      const uint32_t dx = tmem + (uint32_t)(kHeadBufs * BN);
       for (int kt = 0; kt < ktiles; ++kt, ++g) {
         const int s = g % kStages;
         if (kt % kHeadGroup == 0) {
-          hb = hg & 1;
-          if (hg >= 2) {
-            ok = tc::mbar_wait(&hempty[hb], ((hg / 2) - 1) & 1, st);
+          hb = hg % kHeadBufs;
+          if (hg >= kHeadBufs) {
+            ok = tc::mbar_wait(&hempty[hb], ((hg / kHeadBufs) - 1) & 1, st);
             if (!ok) break;
             tc::tc_fence_after();
           }
@@ -248,7 +248,7 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
         }
       }
       if (!ok) break;
-      tc::mma_commit(&xfull[xb]);      // the tile's cross sum is complete
+      tc::mma_commit(xfull);           // the tile's cross sum is complete
     }
   } else if (warp >= 2) {
     // ---------------- epilogue ----------------
@@ -282,9 +282,9 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
       };
       // each warp drains its lane quarter on its own; the four agree once per tile
       for (int gi = 0; gi < ngroups && ok; ++gi, ++hg) {
-        const int hb = hg & 1;
+        const int hb = hg % kHeadBufs;
         int okl = 0;
-        if (lane == 0) okl = tc::mbar_wait(&hfull[hb], (hg / 2) & 1, st) ? 1 : 0;
+        if (lane == 0) okl = tc::mbar_wait(&hfull[hb], (hg / kHeadBufs) & 1, st) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, okl, 0)) {
           ok = false;
           break;
@@ -294,13 +294,12 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
         if (lane == 0) tc::mbar_arrive(&hempty[hb]);
       }
       if (ok) {
-        const int xb = it & 1;
         int okl = 0;
-        if (lane == 0) okl = tc::mbar_wait(&xfull[xb], (it / 2) & 1, st) ? 1 : 0;
+        if (lane == 0) okl = tc::mbar_wait(xfull, it & 1, st) ? 1 : 0;
         if (__shfl_sync(0xffffffffu, okl, 0)) {
           tc::tc_fence_after();
-          drain((uint32_t)((2 + xb) * BN));
-          if (lane == 0) tc::mbar_arrive(&xempty[xb]);
+          drain((uint32_t)(kHeadBufs * BN));
+          if (lane == 0) tc::mbar_arrive(xempty);
         } else {
           ok = false;
         }

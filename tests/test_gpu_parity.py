@@ -61,11 +61,14 @@ def _codes(qpacked, bits, d):
     (512, 2048, "bf16", 5, 4),
     (1024, 4096, "f16", 10, 8),
     (130, 64, "f16", 0, 0),
-    # more tiles than SMs: the last round's tiles are cut into token ranges that add to H
-    (3200, 2048, "f16", 4, 3),      # 169 tiles, 17 of them split
-    (4096, 1000, "bf16", 0, 0),     # 272 tiles, 16 stages: one stage per token range
-    (4000, 640, "f16", 2, 1),       # ragged channels; 10 stages: some token ranges empty
-    (3998, 512, "f16", 0, 0),       # rows of H not 16-byte aligned: scalar adds
+    # more 256 x 256 tiles than SM pairs: a partial last round
+    (3200, 2048, "f16", 4, 3),      # 91 tiles; 4 segments: the last round is not cut
+    (4096, 1000, "bf16", 0, 0),     # 136 tiles, 16 stages
+    (4000, 640, "f16", 2, 1),       # ragged channels: the last rows of a pair beyond d
+    (3998, 512, "f16", 0, 0),       # rows of H not 16-byte aligned
+    # the last round's tiles cut into a head and a tail that add onto a zeroed H
+    (4096, 4096, "f16", 0, 0),      # 60 cut tiles, heads of 7 of 8 segments, 4 tail batches
+    (3000, 4100, "bf16", 3, 2),     # ragged channels and tokens: 2 cut tiles, tail ends ragged
 ])
 def test_hessian_parity(d, n, dtype, dead, outl):
     spec = S.ActivationSpec(d_in=d, n_tok=n, dtype=dtype, n_dead=dead, n_outlier=outl, seed=d + n)
@@ -107,16 +110,32 @@ def test_hessian_accumulates_over_chunks(dtype):
 
 
 def test_hessian_token_ranges_accumulate_over_chunks():
-    # 182 tiles of 128 x 256: 30 of them in token ranges, added onto the earlier chunks' H
-    spec = S.ActivationSpec(d_in=3328, n_tok=3000, dtype="f16", n_dead=3, n_outlier=2, seed=78)
+    # 91 tiles of 256 x 256: the first chunk's last round cut into heads and tails, the
+    # later chunks (accumulating) uncut
+    spec = S.ActivationSpec(d_in=3328, n_tok=6000, dtype="f16", n_dead=3, n_outlier=2, seed=78)
     X = _x(spec).to(DEV)
-    H = gptq.hessian(X[:1024])
-    gptq.hessian(X[1024:2500], H, accumulate=True)
-    gptq.hessian(X[2500:], H, accumulate=True)
+    H = gptq.hessian(X[:4096])
+    gptq.hessian(X[4096:5000], H, accumulate=True)
+    gptq.hessian(X[5000:], H, accumulate=True)
     Hr = O.hessian(X.cpu().float().numpy())
     Hg = H.cpu().numpy()
     assert PT.rel_fro(Hg, Hr) <= PT.TOL_H
     assert np.array_equal(Hg, Hg.T)
+
+
+def test_hessian_cut_round_matches_uncut():
+    # the same Hessian with the last round cut (overwrite) and uncut (accumulating onto
+    # zeros): equal up to the grouping of the fp32 segment sums
+    spec = S.ActivationSpec(d_in=4096, n_tok=4096, dtype="bf16", n_dead=2, n_outlier=2, seed=79)
+    X = _x(spec).to(DEV)
+    Hc = gptq.hessian(X)
+    Hu = torch.zeros_like(Hc)
+    gptq.hessian(X, Hu, accumulate=True)
+    torch.cuda.synchronize()
+    assert torch.equal(Hc, Hc.T)
+    assert ((Hc - Hu).abs().max() / Hu.abs().max()).item() <= 1e-6
+    # a repeat of the cut call is bit-identical
+    assert torch.equal(gptq.hessian(X), Hc)
 
 
 def test_hessian_zero_tokens():
