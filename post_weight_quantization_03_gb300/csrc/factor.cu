@@ -226,27 +226,20 @@ struct LeafBlock {
     const float l32 = fmaf(-l31, l21, fmaf(-l30, l20, b32)) * r2;
     const float t33 = fmaf(-l32, l32, fmaf(-l31, l31, fmaf(-l30, l30, b33)));
     const float r3 = t33 > 0.0f ? rsqrtf(t33) : 0.0f;
-    // this lane's row in the block's columns
+    // this lane's row in the block's columns, without branches (a divergent chain of cases
+    // costs hundreds of cycles per block): the general solve gives, in the block's own rows
+    // rr = 0..3, exactly the block factor's operations (x_j = l_rr,j for j < rr and
+    // x_rr = t_rr,rr r_rr), and entries right of the diagonal (j > rr) are set to zero
     const int rr = lane - JB;
-    float x0 = 0.0f, x1 = 0.0f, x2 = 0.0f, x3 = 0.0f;
-    if (rr >= 4) {
-      x0 = a[JB] * r0;
-      x1 = fmaf(-x0, l10, a[JB + 1]) * r1;
-      x2 = fmaf(-x1, l21, fmaf(-x0, l20, a[JB + 2])) * r2;
-      x3 = fmaf(-x2, l32, fmaf(-x1, l31, fmaf(-x0, l30, a[JB + 3]))) * r3;
-    } else if (rr == 0) {
-      x0 = b00 * r0;
-      rdl = r0;
-    } else if (rr == 1) {
-      x0 = l10; x1 = t11 * r1;
-      rdl = r1;
-    } else if (rr == 2) {
-      x0 = l20; x1 = l21; x2 = t22 * r2;
-      rdl = r2;
-    } else if (rr == 3) {
-      x0 = l30; x1 = l31; x2 = l32; x3 = t33 * r3;
-      rdl = r3;
-    }
+    float x0 = a[JB] * r0;
+    float x1 = fmaf(-x0, l10, a[JB + 1]) * r1;
+    float x2 = fmaf(-x1, l21, fmaf(-x0, l20, a[JB + 2])) * r2;
+    float x3 = fmaf(-x2, l32, fmaf(-x1, l31, fmaf(-x0, l30, a[JB + 3]))) * r3;
+    x0 = rr >= 0 ? x0 : 0.0f;
+    x1 = rr >= 1 ? x1 : 0.0f;
+    x2 = rr >= 2 ? x2 : 0.0f;
+    x3 = rr >= 3 ? x3 : 0.0f;
+    rdl = rr == 0 ? r0 : rr == 1 ? r1 : rr == 2 ? r2 : rr == 3 ? r3 : rdl;
     M[(JB + 0) * PL + lane] = x0 * r0;   // L[i][j] / L[j][j]
     M[(JB + 1) * PL + lane] = x1 * r1;
     M[(JB + 2) * PL + lane] = x2 * r2;
