@@ -89,25 +89,6 @@ def measured_peaks():
             "fallback"
 
 
-def profiled_traffic(profile, source, n_tok):
-    """DRAM bytes per launch (read + write) that a committed ncu summary records for a kernel,
-    scaled there to a launch over `n_tok` tokens; None unless the summary was taken on the
-    kernel source as it stands (its sha256 prefix matches) and for this token count."""
-    import hashlib
-    try:
-        with open(os.path.join(ROOT, "profiles", profile)) as f:
-            lines = f.read().splitlines()
-        with open(os.path.join(ROOT, "post_weight_quantization_03_gb300", "csrc", source), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    except OSError:
-        return None
-    kv = dict(l.split(": ", 1) for l in lines if ": " in l and not l.startswith(("|", "#", "*")))
-    key = f"traffic_bytes_per_launch_{n_tok}"
-    if kv.get("source_sha256_16") != sha or key not in kv:
-        return None
-    return int(kv[key])
-
-
 # nominal dense tensor rates of the part (bf16 2.25 PFLOP/s, TF32 1.1 PFLOP/s): a TF32
 # peak is the measured bf16 peak times their ratio
 TF32_PER_BF16 = 1.1 / 2.25
@@ -435,15 +416,10 @@ def main():
     # timed by events on the stream it runs on); with B = 1 the eager column updates
     roofline = dict(stages[0])
     roofline["kernel"] = "hessian_tc_kernel (gptq_hessian_accumulate: one launch per step)"
-    traffic = (profiled_traffic("hessian_tc_layer4096.md", "hessian.cu", n)
-               if (m, d) == (4096, 4096) and layer.act.dtype == "f16" else None)
-    roofline["traffic"] = traffic
-    roofline["traffic_note"] = (
-        "dram__bytes_read.sum + dram__bytes_write.sum of one ncu capture of this kernel source "
-        "(profiles/hessian_tc_layer4096.md, 65,536 tokens, reads scaled to this launch's tokens)"
-        if traffic is not None else
-        "not measured for this kernel source and workload: the DRAM bytes of an ncu capture are "
-        "kept with the kernel's profile summary")
+    roofline["traffic"] = None
+    roofline["traffic_note"] = ("not measured in this run (ncu does not run inside the bench): "
+                                "the DRAM bytes of an ncu capture of this kernel, scaled to this "
+                                "launch, are stated with its profile summary")
     if block == 1:
         # the eager sweep dominates (B = 1): each column's update reads and writes the fp32
         # working copy of every later column once
