@@ -206,8 +206,8 @@ static_assert(kPotrfSmemUsed <= kPotrfSmem, "potrf shared memory");
 // diagonal is never read and is cleared at the end.
 template <int JB>
 struct LeafBlock {
-  static __device__ __forceinline__ void run(float (&a)[PW], float &rdl, float4 *xb, float *M,
-                                             int lane) {
+  static __device__ __forceinline__ void run(float (&a)[PW], float &rdl, float &pvl, float4 *xb,
+                                             float *M, int lane) {
     constexpr unsigned F = 0xffffffffu;
     const float b00 = __shfl_sync(F, a[JB], JB);
     const float b10 = __shfl_sync(F, a[JB], JB + 1), b11 = __shfl_sync(F, a[JB + 1], JB + 1);
@@ -215,17 +215,18 @@ struct LeafBlock {
     const float b22 = __shfl_sync(F, a[JB + 2], JB + 2);
     const float b30 = __shfl_sync(F, a[JB], JB + 3), b31 = __shfl_sync(F, a[JB + 1], JB + 3);
     const float b32 = __shfl_sync(F, a[JB + 2], JB + 3), b33 = __shfl_sync(F, a[JB + 3], JB + 3);
-    // the block's factor; a failed pivot leaves r = 0
-    const float r0 = b00 > 0.0f ? rsqrtf(b00) : 0.0f;
+    // the block's factor, with no test on the chain: a non-positive pivot gives an infinite
+    // or NaN r (the factor is then discarded; the pivot itself is recorded below)
+    const float r0 = rsqrtf(b00);
     const float l10 = b10 * r0, l20 = b20 * r0, l30 = b30 * r0;
     const float t11 = fmaf(-l10, l10, b11);
-    const float r1 = t11 > 0.0f ? rsqrtf(t11) : 0.0f;
+    const float r1 = rsqrtf(t11);
     const float l21 = fmaf(-l20, l10, b21) * r1, l31 = fmaf(-l30, l10, b31) * r1;
     const float t22 = fmaf(-l21, l21, fmaf(-l20, l20, b22));
-    const float r2 = t22 > 0.0f ? rsqrtf(t22) : 0.0f;
+    const float r2 = rsqrtf(t22);
     const float l32 = fmaf(-l31, l21, fmaf(-l30, l20, b32)) * r2;
     const float t33 = fmaf(-l32, l32, fmaf(-l31, l31, fmaf(-l30, l30, b33)));
-    const float r3 = t33 > 0.0f ? rsqrtf(t33) : 0.0f;
+    const float r3 = rsqrtf(t33);
     // this lane's row in the block's columns, without branches (a divergent chain of cases
     // costs hundreds of cycles per block): the general solve gives, in the block's own rows
     // rr = 0..3, exactly the block factor's operations (x_j = l_rr,j for j < rr and
@@ -240,6 +241,7 @@ struct LeafBlock {
     x2 = rr >= 2 ? x2 : 0.0f;
     x3 = rr >= 3 ? x3 : 0.0f;
     rdl = rr == 0 ? r0 : rr == 1 ? r1 : rr == 2 ? r2 : rr == 3 ? r3 : rdl;
+    pvl = rr == 0 ? b00 : rr == 1 ? t11 : rr == 2 ? t22 : rr == 3 ? t33 : pvl;
     M[(JB + 0) * PL + lane] = x0 * r0;   // L[i][j] / L[j][j]
     M[(JB + 1) * PL + lane] = x1 * r1;
     M[(JB + 2) * PL + lane] = x2 * r2;
@@ -258,12 +260,13 @@ struct LeafBlock {
         a[k] = fmaf(-x3, v.w, a[k]);
       }
     }
-    LeafBlock<JB + 4>::run(a, rdl, xb, M, lane);
+    LeafBlock<JB + 4>::run(a, rdl, pvl, xb, M, lane);
   }
 };
 template <>
 struct LeafBlock<PW> {
-  static __device__ __forceinline__ void run(float (&)[PW], float &, float4 *, float *, int) {}
+  static __device__ __forceinline__ void run(float (&)[PW], float &, float &, float4 *, float *,
+                                             int) {}
 };
 static_assert(PW % 4 == 0, "the leaf eliminates four columns at a time");
 
@@ -282,8 +285,8 @@ __device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float4
 #pragma unroll
   for (int l = 0; l < PW; ++l)
     if (l > lane || !own) a[l] = 0.0f;
-  float rdl = 0.0f;
-  LeafBlock<0>::run(a, rdl, xb, M, lane);
+  float rdl = 0.0f, pvl = 1.0f;   // this lane's reciprocal pivot and its pivot
+  LeafBlock<0>::run(a, rdl, pvl, xb, M, lane);
   if (own) {
 #pragma unroll
     for (int q = 0; q < PW / 4; ++q)
@@ -292,8 +295,8 @@ __device__ __forceinline__ int leaf_factor(float *S, float *M, float *rd, float4
                       4 * q + 2 <= lane ? a[4 * q + 2] : 0.0f, 4 * q + 3 <= lane ? a[4 * q + 3] : 0.0f);
     rd[lane] = rdl;
   }
-  // a failed pivot left r = 0 in its lane
-  const unsigned badm = __ballot_sync(0xffffffffu, own && !(rdl > 0.0f));
+  // a pivot that is not positive (or is NaN) fails in its lane
+  const unsigned badm = __ballot_sync(0xffffffffu, own && !(pvl > 0.0f));
   return badm ? t0 + __ffs((int)badm) - 1 : -1;
 }
 
