@@ -817,9 +817,18 @@ struct QuantWs {
   float *Lhi, *Llo; int64_t ldl;
   uint8_t *codes; int64_t ldc;
   float *Ud, *Uo;       // packed diagonal blocks; off-diagonal block of each pair
-  float *Ehi2, *Elo2;   // second E pair buffer
-  int64_t lde;          // E row stride: two blocks side by side (a pair of blocks)
+  float *Ehi2, *Elo2;   // second E buffer
+  int64_t lde;          // E row stride: a pair of blocks side by side, or a group of two pairs
 };
+
+// On wide layers the far part of the blocked sweep's trailing update is most of its work; it
+// is then applied once per group of two pairs of blocks, as one product of depth up to 4B
+// (measured faster per flop than two of depth 2B), and each E buffer holds a group.
+constexpr int64_t kGroupedMinD = 8192;
+inline bool sweep_grouped(int64_t d, int block) { return block > 1 && d >= kGroupedMinD; }
+inline int64_t sweep_lde(int64_t d, int block) {
+  return block > 1 ? (sweep_grouped(d, block) ? 4 : 2) * SB : SB;
+}
 
 QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   QuantWs q;
@@ -827,7 +836,7 @@ QuantWs carve_quantize(void *ws, int64_t m, int64_t d, int block) {
   q.st = (DevStatus *)p; p += 256;
   q.ldwf = (int64_t)round_up((size_t)d, 4);
   q.Wf = (float *)p; p += round_up((size_t)m * q.ldwf * 4, 256);
-  q.lde = block > 1 ? 2 * SB : SB;
+  q.lde = sweep_lde(d, block);
   q.Ehi = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
   q.Elo = (float *)p; p += round_up((size_t)m * q.lde * 4, 256);
   q.ldl = (int64_t)round_up((size_t)d, 4);
@@ -852,7 +861,7 @@ size_t quantize_ws_bytes(int64_t m, int64_t d, int bits, int block) {
   const size_t ldwf = round_up((size_t)d, 4), ldl = round_up((size_t)d, 4);
   const size_t ldc = round_up((size_t)d, 16);
   const size_t nblk = (size_t)ceil_div(d, block < 1 ? 1 : block);
-  const size_t lde = block > 1 ? 2 * SB : SB;
+  const size_t lde = (size_t)sweep_lde(d, block);
   return 256 + round_up((size_t)m * ldwf * 4, 256) + 2 * round_up((size_t)m * lde * 4, 256) +
          2 * round_up((size_t)d * ldl * 4, 256) + round_up((size_t)m * ldc, 256) +
          (block > 1 ? nblk * UD_FLOATS * 4 + (nblk / 2) * UO_FLOATS * 4 +
@@ -999,11 +1008,16 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
     // past it: the next two blocks' columns in 128-wide tiles, the rest in 256-wide ones.
     // Every column thus receives the contributions of earlier pairs in the same order,
     // grouping and kernel in both schedules below (the results are bit for bit the same).
-    // W[:, c0:c1] -= E U[kb0:kb0+K, c0:c1] with E the first K columns of pair buffer e
-    auto update = [&](int e, int64_t kb0, int K, int64_t c0, int64_t c1, int max_ctas,
-                      cudaStream_t st, int wide) -> gptq_status {
+    // On wide layers (grouped) pair p writes its E into buffer (p / 2) % 2 at column
+    // (p % 2) 2B, so that a group's two pairs sit side by side; otherwise into buffer p % 2.
+    const bool grouped = sweep_grouped(d, block);
+    auto e_col = [&](int64_t p) -> int64_t { return grouped ? (p & 1) * 2 * block : 0; };
+    auto e_buf = [&](int64_t p) -> int { return (int)((grouped ? p >> 1 : p) & 1); };
+    // W[:, c0:c1] -= E U[kb0:kb0+K, c0:c1] with E the K columns of buffer e from column ec
+    auto update = [&](int e, int64_t ec, int64_t kb0, int K, int64_t c0, int64_t c1,
+                      int max_ctas, cudaStream_t st, int wide) -> gptq_status {
       GemmArgs g{};
-      g.a_hi = e ? q.Ehi2 : q.Ehi; g.a_lo = e ? q.Elo2 : q.Elo; g.lda = q.lde;
+      g.a_hi = (e ? q.Ehi2 : q.Ehi) + ec; g.a_lo = (e ? q.Elo2 : q.Elo) + ec; g.lda = q.lde;
       g.b_hi = q.Lhi + c0 * q.ldl + kb0; g.b_lo = q.Llo + c0 * q.ldl + kb0; g.ldb = q.ldl;
       g.c = q.Wf + c0; g.ldc = q.ldwf;
       g.M = m; g.N = c1 - c0; g.K = K;
@@ -1015,14 +1029,16 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
     // pair p: blocks 2p ([a0, a0 + nbA)) and 2p + 1 ([a0 + block, + nbB), nbB = 0 if none)
     auto sweep = [&](int64_t p, int nbA, int nbB, cudaStream_t st) -> gptq_status {
       const int64_t a0 = 2 * p * block;
-      const int e = (int)(p & 1);
+      const int e = e_buf(p);
+      const int64_t ec = e_col(p);
       return launch_kernel(sweep_pair_kernel, sweep_grid, SW_THREADS, sweep_smem, st,
                            (const float *)q.Wf, q.ldwf, m, a0, nbA, nbB, block,
                            (const float *)(q.Ud + 2 * p * UD_FLOATS),
                            (const float *)(q.Ud + (nbB ? 2 * p + 1 : 2 * p) * UD_FLOATS),
                            (const float *)(q.Uo + (nbB ? p : 0) * UO_FLOATS),
                            (const float *)scale, (const int32_t *)zero, maxq,
-                           e ? q.Ehi2 : q.Ehi, e ? q.Elo2 : q.Elo, q.lde, q.codes, q.ldc, q.st);
+                           (e ? q.Ehi2 : q.Ehi) + ec, (e ? q.Elo2 : q.Elo) + ec, q.lde, q.codes,
+                           q.ldc, q.st);
     };
     auto widths = [&](int64_t p, int &nbA, int &nbB) {
       const int64_t a0 = 2 * p * block, b0 = a0 + block;
@@ -1030,25 +1046,50 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       nbB = b0 < d ? (int)std::min<int64_t>(block, d - b0) : 0;
     };
     const int64_t npairs = ceil_div(d, 2 * (int64_t)block);
+    // The trailing update after pair p (group g = p / 2 when grouped), its columns split by
+    // where they are needed next:
+    //   near: [pe, ne), ne = the end of group g + 1 (grouped) or of the layer, depth = the
+    //         pair: the next pair's columns first (the sweep after waits for them), then the
+    //         rest of the near columns in 256-wide tiles;
+    //   far:  grouped, after a group's last pair, [ne, d) once for the whole group, depth up
+    //         to 4B, in 256-wide tiles.
+    // Every column thus receives the contributions of earlier pairs and groups in one order,
+    // grouping and kernel in both schedules below (the results are bit for bit the same).
+    struct Split {
+      int64_t a0, pe, f0, ne;   // pair start and end; next pair's end; near end
+      bool far;                 // a group's far product follows this pair
+      int64_t g0;               // the group's first column
+    };
+    auto split = [&](int64_t p, int nbA, int nbB) {
+      Split t;
+      t.a0 = 2 * p * block;
+      t.pe = t.a0 + (nbB ? block + nbB : nbA);
+      t.f0 = std::min<int64_t>(t.pe + 2 * block, d);
+      t.g0 = grouped ? (p & ~int64_t(1)) * 2 * block : t.a0;
+      t.ne = grouped ? std::min<int64_t>(t.g0 + 8 * block, d) : d;
+      t.far = grouped && ((p & 1) || p + 1 == npairs) && t.ne < d;
+      return t;
+    };
     if (!overlap) {
       for (int64_t p = 0; p < npairs; ++p) {
         int nbA, nbB;
         widths(p, nbA, nbB);
-        const int64_t a0 = 2 * p * block, pe = a0 + (nbB ? block + nbB : nbA);
+        const Split t = split(p, nbA, nbB);
         GPTQ_TRY(sweep(p, nbA, nbB, s));
-        if (pe < d) {
-          // the same column split and kernels as the two-stream schedule below
-          const int64_t f0 = std::min<int64_t>(pe + 2 * block, d);
-          GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), pe, f0, 0, s, 0));
-          if (f0 < d) GPTQ_TRY(update((int)(p & 1), a0, (int)(pe - a0), f0, d, 0, s, 1));
-        }
+        if (t.pe >= d) break;
+        // the same column split and kernels as the two-stream schedule below
+        const int e = e_buf(p), K = (int)(t.pe - t.a0);
+        GPTQ_TRY(update(e, e_col(p), t.a0, K, t.pe, std::min(t.f0, t.ne), 0, s, 0));
+        if (t.f0 < t.ne) GPTQ_TRY(update(e, e_col(p), t.a0, K, t.f0, t.ne, 0, s, 1));
+        if (t.far) GPTQ_TRY(update(e, 0, t.g0, (int)(t.pe - t.g0), t.ne, d, 0, s, 1));
       }
     } else {
-      // After pair p its product splits two blocks on: those two blocks' columns on the
-      // critical stream right after the sweep, the far columns on the side stream, where they
-      // have a pair sweep and a near update's time before the sweep that needs them.  Pair
-      // p's near update waits for pair p - 1's far update, which keeps each column's
-      // contributions in the single-stream order and frees the pair buffer pair p + 1 reuses.
+      // After pair p: the next pair's columns on the critical stream right after the sweep,
+      // the rest of its near columns and a group's far product on the side stream, where
+      // they have at least a pair sweep and a near update's time before the sweep that needs
+      // them.  Pair p's update on the critical stream waits for the side stream's work of
+      // pair p - 1, which keeps each column's contributions in the single-stream order and
+      // frees the E buffer that the next pair or group reuses.
       cudaStream_t c = qs->crit, sd = qs->side;
       int nsm = 0;
       GPTQ_TRY(device_sm_count(&nsm));
@@ -1066,21 +1107,20 @@ gptq_status enqueue_quantize_layers(const QLayer *L, int n, int64_t d, const flo
       for (int64_t p = 0; p < npairs; ++p) {
         int nbA, nbB;
         widths(p, nbA, nbB);
-        const int e = (int)(p & 1);
-        const int64_t a0 = 2 * p * block, pe = a0 + (nbB ? block + nbB : nbA);
+        const Split t = split(p, nbA, nbB);
+        const int pb = (int)(p & 1);                              // event parity
         GPTQ_TRY(sweep(p, nbA, nbB, c));
-        if (pe >= d) break;
+        if (t.pe >= d) break;
         if (!lt_waited) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->lt_done, 0));
         lt_waited = true;
-        const int K = (int)(pe - a0);
-        const int64_t f0 = std::min<int64_t>(pe + 2 * block, d);   // far columns [f0, d)
-        GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[e], c));
-        if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[e ^ 1], 0));
-        GPTQ_TRY(update(e, a0, K, pe, f0, 0, c, 0));               // the next two blocks
-        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[e], 0));
-        // the far columns in 256-wide tiles
-        if (f0 < d) GPTQ_TRY(update(e, a0, K, f0, d, far_ctas, sd, 1));
-        GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[e], sd));
+        const int e = e_buf(p), K = (int)(t.pe - t.a0);
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->e_ready[pb], c));
+        if (p > 0) GPTQ_CUDA_CHECK(cudaStreamWaitEvent(c, qs->far_done[pb ^ 1], 0));
+        GPTQ_TRY(update(e, e_col(p), t.a0, K, t.pe, std::min(t.f0, t.ne), 0, c, 0));
+        GPTQ_CUDA_CHECK(cudaStreamWaitEvent(sd, qs->e_ready[pb], 0));
+        if (t.f0 < t.ne) GPTQ_TRY(update(e, e_col(p), t.a0, K, t.f0, t.ne, far_ctas, sd, 1));
+        if (t.far) GPTQ_TRY(update(e, 0, t.g0, (int)(t.pe - t.g0), t.ne, d, far_ctas, sd, 1));
+        GPTQ_CUDA_CHECK(cudaEventRecord(qs->far_done[pb], sd));
       }
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->crit_done, c));
       GPTQ_CUDA_CHECK(cudaEventRecord(qs->side_done, sd));
