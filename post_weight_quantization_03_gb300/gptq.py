@@ -377,25 +377,28 @@ def quantize_shared(Ws, U, bits=4, block=128, dead_mask=None, want_w_hat=False, 
 
 
 def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, overlap=True,
-                   stage_events=None):
+                   stage_events=None, consumers=2):
     """GPTQ over a block of layers grouped by their shared inputs.
 
     ``groups`` is a list of ``(X, [W, ...])``: X the token-major inputs of the group (on the
     device) and the weights of every layer that reads them.  Per group: H from X, one
     prepare, then one shared sweep of all its layers per bit width.  With ``overlap`` the
     Hessians are accumulated (in chunks of ``chunk_tok`` tokens, or in one call when None) on
-    a producer stream, ahead of the prepares and sweeps, which run on a higher-priority
-    stream; every step is a call of this library.  Returns ``[{bits: [(qpacked, scale, zero, None) per layer]}, ...]`` and
+    a producer stream, ahead of the prepares and sweeps, which run on ``consumers``
+    higher-priority streams taken in turn by group (so one group's sweep can run beside the
+    next group's prepare); every step is a call of this library.  Returns ``[{bits: [(qpacked, scale, zero, None) per layer]}, ...]`` and
     the dead-column counts, in group order."""
     torch = _torch()
     dev = groups[0][1][0].device
     caller = torch.cuda.current_stream(dev)
     lo, hi = torch.cuda.Stream.priority_range()
-    cons = torch.cuda.Stream(dev, priority=hi) if overlap else caller
+    cons_all = ([torch.cuda.Stream(dev, priority=hi) for _ in range(max(1, consumers))]
+                if overlap else [caller])
     prod = torch.cuda.Stream(dev, priority=lo) if overlap else caller
     if overlap:
         prod.wait_stream(caller)
-        cons.wait_stream(caller)
+        for c in cons_all:
+            c.wait_stream(caller)
     Hs, ready = [], []
     for X, _ in groups:
         d = X.shape[1]
@@ -413,12 +416,15 @@ def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, over
         Hs.append(H)
         ready.append(e)
     results, n_dead, keep = [], [], []
-    for (X, Ws), H, e in zip(groups, Hs, ready):
+    for gi, ((X, Ws), H, e) in enumerate(zip(groups, Hs, ready)):
+        cons = cons_all[gi % len(cons_all)]
         cons.wait_event(e)
         d = X.shape[1]
         e0 = torch.cuda.Event(enable_timing=True)
         e0.record(cons)
-        U, dm, nd = prepare(H, damp, stream=cons)
+        # every buffer a stream uses stays referenced until the caller has joined the streams
+        pws = workspace(gptq_prepare_workspace_bytes(d), dev)
+        U, dm, nd = prepare(H, damp, ws=pws, stream=cons)
         e1 = torch.cuda.Event(enable_timing=True)
         e1.record(cons)
         m_rows = (ctypes.c_int64 * len(Ws))(*[W.shape[0] for W in Ws])
@@ -434,9 +440,10 @@ def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, over
             stage_events.append(("quantize", e1, e2))
         results.append(res)
         n_dead.append(nd)
-        keep += [U, dm, ws]     # in use on the consumer stream until the waits below
+        keep += [U, dm, ws, pws]   # in use on the consumer streams until the waits below
     if overlap:
-        caller.wait_stream(cons)
+        for c in cons_all:
+            caller.wait_stream(c)
         caller.wait_stream(prod)
     return results, n_dead
 
