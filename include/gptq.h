@@ -93,7 +93,8 @@ gptq_status gptq_hessian_accumulate(const void *X, int xdtype, int64_t n_tok, in
  * gptq_hessian_host_workspace_bytes: device staging workspace that
  * gptq_hessian_accumulate_host needs for inputs of d_in channels streamed in chunks of
  * chunk_tok tokens (0 = the default chunk: about 64 MiB of X, a multiple of 512 tokens, and
- * at least 8192 tokens, since every chunk's products read and write all of H).
+ * at least 8192 tokens, or 32768 from d_in = 16384 on, since every chunk's products read and
+ * write all of H).
  * Returns 0 for an unknown dtype, d_in < 1 or chunk_tok < 0.
  */
 size_t gptq_hessian_host_workspace_bytes(int xdtype, int64_t d_in, int64_t chunk_tok);

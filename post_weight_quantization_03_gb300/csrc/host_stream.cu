@@ -20,15 +20,22 @@ namespace {
 
 constexpr size_t kChunkBytes = (size_t)64 << 20;
 
-// Default chunk: about kChunkBytes of X, but at least kMinChunkTokens tokens: every chunk's
-// products read and write all of H, so wide layers need long chunks (at d_in = 28672, 64 MiB
-// would be 1024 tokens, and H's 6.6 GB of traffic per chunk would outweigh its products).
+// Default chunk: about kChunkBytes of X, but at least kMinChunkTokens tokens, and at least
+// kMinChunkTokensWide from d_in = kWideD on: every chunk's products read and write all of H
+// and end in a partial round of tiles, so wide layers need long chunks (at d_in = 28672,
+// 64 MiB would be 1024 tokens, and H's 6.6 GB of traffic per chunk would outweigh its
+// products; measured there over 65,536 tokens: 69.3 ms with 8192-token chunks, 56.2 with
+// 16384, 52.5 with 32768).  Narrower layers are bound by the copies, where a longer first
+// chunk only delays the first product (10.45 against 10.65 ms at d_in = 4096).
 constexpr int64_t kMinChunkTokens = 8192;
+constexpr int64_t kMinChunkTokensWide = 32768;
+constexpr int64_t kWideD = 16384;
 
-int64_t chunk_tokens(size_t row_bytes, int64_t chunk_tok) {
+int64_t chunk_tokens(int64_t d, size_t es, int64_t chunk_tok) {
   if (chunk_tok > 0) return chunk_tok;
-  const int64_t t = (int64_t)(kChunkBytes / row_bytes) / 512 * 512;
-  return t < kMinChunkTokens ? kMinChunkTokens : t;
+  const int64_t t = (int64_t)(kChunkBytes / ((size_t)d * es)) / 512 * 512;
+  const int64_t lo = d >= kWideD ? kMinChunkTokensWide : kMinChunkTokens;
+  return t < lo ? lo : t;
 }
 
 struct CopyStream {
@@ -61,7 +68,7 @@ gptq_status copy_stream(CopyStream **out) {
 }  // namespace
 
 size_t hessian_host_ws_bytes(int64_t d, size_t es, int64_t chunk_tok) {
-  const int64_t ct = chunk_tokens((size_t)d * es, chunk_tok);
+  const int64_t ct = chunk_tokens(d, es, chunk_tok);
   return 2 * round_up((size_t)ct * (size_t)d * es, 256);
 }
 
@@ -70,7 +77,7 @@ gptq_status launch_hessian_host(const void *X_host, int xdtype, size_t es, int64
                                 int64_t chunk_tok, void *ws, cudaStream_t s) {
   if (n_tok == 0) return launch_hessian(nullptr, xdtype, 0, d, d, H, accumulate, nullptr, s);
   const size_t row = (size_t)d * es;
-  const int64_t ct = chunk_tokens(row, chunk_tok);
+  const int64_t ct = chunk_tokens(d, es, chunk_tok);
   char *buf[2] = {(char *)ws, (char *)ws + round_up((size_t)ct * row, 256)};
   CopyStream *cs = nullptr;
   GPTQ_TRY(copy_stream(&cs));
