@@ -12,6 +12,7 @@
 // kind::tf32 products of TF32 head/tail splits (3xTF32); tiny shapes take a CUDA-core
 // kernel.
 #include <algorithm>
+#include <cstring>
 
 #include "tc.cuh"
 
@@ -140,11 +141,13 @@ struct HessTcParams {
   int full_tiles;     // units [0, full_tiles): whole tiles, written with plain stores
   int cut_tiles;      // then cut_tiles heads and cut_tiles tails (atomic adds)
   int cut_stage;      // first token stage of a tail
+  int tma_h;          // 1: off-diagonal tiles leave through the H tensor map
 };
 
 template <int FMT>  // 0 = fp16, 1 = bf16
 __global__ void __launch_bounds__(T_THREADS, 1)
-hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevStatus *st) {
+hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mh,
+                  HessTcParams p, DevStatus *st) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *full = (uint64_t *)(smem + T_STAGES * T_STAGE);   // even CTA's: both halves in
@@ -282,9 +285,64 @@ hessian_tc_kernel(const __grid_constant__ CUtensorMap mx, HessTcParams p, DevSta
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(tempty0 + (uint32_t)(buf * sizeof(uint64_t)));
     }
-    const int64_t r = m0 + q * 32 + lane;
+    const int64_t rl = q * 32 + lane;   // row within this CTA's 128
+    const int64_t r = m0 + rl;
     const int64_t d = p.d;
-    if (ok && r < d && add) {
+    if (p.tma_h && I != J) {
+      // Off-diagonal tile: the operand ring is free now (the last MMA has completed), so the
+      // tile goes out through it by TMA, first as it is (H rows m0.., columns n0..), then
+      // transposed (H rows n0.., columns m0..): eight boxes of 32 columns x 128 rows, with
+      // the 128-byte swizzle, each time.  A store overwrites H; an accumulating call or a cut
+      // tile's part adds in L2 instead.  All eight warps agree on `ok` first.
+      ok = tc::named_barrier_and(1, 32 * T_EPI_WARPS, ok);
+      const bool lead = warp == 2 && lane == 0;
+      const bool red = add || p.accumulate;
+      if (ok && m0 < d) {
+        uint8_t *stg = smem;
+        // as it is: column c of this thread's half -> box (h * 128 + c) / 32, row rl
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int c = 4 * u, b = h * 4 + c / 32, ch = (c % 32) / 4;
+          *reinterpret_cast<float4 *>(stg + b * 16384 + rl * 128 + ((ch ^ (rl & 7)) * 16)) =
+              make_float4(2.0f * acc[c], 2.0f * acc[c + 1], 2.0f * acc[c + 2], 2.0f * acc[c + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::named_barrier(2, 32 * T_EPI_WARPS);
+        if (lead) {
+          for (int b = 0; b < 8; ++b) {
+            const int32_t x = (int32_t)(n0 + 32 * b);
+            if (x >= d) continue;     // boxes wholly past the last column are not issued
+            if (red) tc::tma_reduce_add_2d(&mh, x, (int32_t)m0, stg + b * 16384);
+            else tc::tma_store_2d(&mh, x, (int32_t)m0, stg + b * 16384);
+          }
+          tc::bulk_commit();
+          tc::bulk_wait_read_all();   // the staging is rewritten next
+        }
+        tc::named_barrier(2, 32 * T_EPI_WARPS);
+        // transposed: tile column h * 128 + i -> H row n0 + h * 128 + i, this thread's row
+        // rl -> H column m0 + rl; box (rl / 32) + 4 h, row i, column rl % 32
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int b = (int)(rl / 32) + 4 * h, cc = (int)(rl % 32);
+          *reinterpret_cast<float *>(stg + b * 16384 + i * 128 + (((cc / 4) ^ (i & 7)) * 16) +
+                                     (cc % 4) * 4) = 2.0f * acc[i];
+        }
+        tc::fence_proxy_async_smem();
+        tc::named_barrier(2, 32 * T_EPI_WARPS);
+        if (lead) {
+          for (int hh = 0; hh < 2; ++hh)
+            for (int b = 0; b < 4; ++b) {
+              uint8_t *src = stg + (b + 4 * hh) * 16384;
+              const int32_t x = (int32_t)(m0 + 32 * b), y = (int32_t)(n0 + 128 * hh);
+              if (x >= d || y >= d) continue;
+              if (red) tc::tma_reduce_add_2d(&mh, x, y, src);
+              else tc::tma_store_2d(&mh, x, y, src);
+            }
+          tc::bulk_commit();
+          tc::bulk_wait_all();
+        }
+      }
+    } else if (ok && r < d && add) {
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
         const int64_t c = n0 + h * 128 + i;
@@ -569,6 +627,12 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
   p.lost_stage = lost_stage;
   const int64_t tiles = (int64_t)p.n_blocks * (p.n_blocks + 1) / 2;
   const int total = (int)ceil_div(n_tok, TB_K);
+  // H as a tensor map (32-column x 128-row boxes, 128-byte swizzle) when its rows start on
+  // 16-byte boundaries: off-diagonal tiles then leave through TMA stores
+  CUtensorMap mh;
+  memset(&mh, 0, sizeof(mh));
+  p.tma_h = (d % 4 == 0) &&
+            tc::make_tmap_2d(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, H, d, d, d * 4, 32, 128) ? 1 : 0;
   p.full_tiles = (int)tiles;
   p.cut_tiles = 0;
   p.cut_stage = total;
@@ -606,8 +670,9 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t e = xdtype == GPTQ_F16 ? cudaLaunchKernelEx(&cfg, hessian_tc_kernel<0>, mx, p, st)
-                                           : cudaLaunchKernelEx(&cfg, hessian_tc_kernel<1>, mx, p, st);
+  const cudaError_t e = xdtype == GPTQ_F16
+                            ? cudaLaunchKernelEx(&cfg, hessian_tc_kernel<0>, mx, mh, p, st)
+                            : cudaLaunchKernelEx(&cfg, hessian_tc_kernel<1>, mx, mh, p, st);
   count_launch();
   if (e != cudaSuccess) {
     (void)cudaGetLastError();

@@ -121,6 +121,18 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *m, int32_t 
       : "memory");
 }
 
+// global[box at (x, y)] = shared box, tracked by bulk groups.  x * elem_size must be a
+// multiple of 16 bytes and x, y must not be negative; elements outside the tensor are not
+// written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int32_t x, int32_t y,
+                                             const void *src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          (uint64_t)m),
+      "r"(x), "r"(y), "r"(smem_u32(src))
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
