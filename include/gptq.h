@@ -403,7 +403,7 @@ gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream);
  *
  * Runs the fp16/bf16 tensor-core Hessian exactly as gptq_hessian_accumulate with
  * accumulate = 0 would, except that its TMA producer issues nothing for token stage
- * `lost_stage` (stages are 64 tokens): no copy and no arrival, so the MMA issuer's wait for
+ * `lost_stage` (stages are 128 tokens): no copy and no arrival, so the MMA issuer's wait for
  * that stage can never complete.  Every wait of the launch gives up after `wait_ns`
  * nanoseconds of the GPU's global timer, records GPTQ_ERR_TIMEOUT in the status block and
  * returns; the CTA then leaves with no copy or tensor-core operation of its own in flight
@@ -412,7 +412,7 @@ gptq_status gptq_workspace_status(const void *ws, gptq_stream_t stream);
  *   X, xdtype, n_tok, d_in, ldx, H
  *              as gptq_hessian_accumulate; xdtype GPTQ_F16 or GPTQ_BF16 with d_in >= 64
  *              and n_tok >= 64 (else UNSUPPORTED).  H is left undefined.
- *   lost_stage 0 <= lost_stage < ceil(n_tok / 64).
+ *   lost_stage 0 <= lost_stage < ceil(n_tok / 128).
  *   wait_ns    1e3 .. 1e10: budget of every wait (the regular calls use 2 s).
  *   status_ws  DEVICE buffer of >= 256 bytes, 256-byte aligned, for the status block.
  * SYNCHRONIZES `stream` and returns the device status: GPTQ_ERR_TIMEOUT when the waits ran

@@ -98,10 +98,10 @@ hessian_simt_kernel(const T *__restrict__ X, int64_t n_tok, int64_t d, int64_t l
 // tcgen05 SYRK on CTA pairs: one cluster of two CTAs (two SMs) per 256 x 256 tile of H on
 // or below the diagonal, one cta_group::2 MMA stream for the pair.  CTA r of the pair holds
 // the tile's rows 128 r .. 128 r + 127 (its A half) and columns 128 r .. 128 r + 127 (its B
-// half) of each 64-token stage, and its half of the accumulator (128 rows x 256 columns) in
-// its own TMEM.  Per SM and stage that is 32 KB of X written into shared memory and 8 KB
-// read by the tensor core per 16 tokens, against 48 KB and 12 KB for a 128 x 256 tile on
-// one SM with the same output per SM.
+// half) of each 128-token stage, and its half of the accumulator (128 rows x 256 columns)
+// in its own TMEM.  Per SM and 16 tokens that is 8 KB of X written into shared memory and
+// 8 KB read by the tensor core, against 12 KB and 12 KB for a 128 x 256 tile on one SM
+// with the same output per SM.
 //   warp 0      : TMA producer of this CTA's halves; both CTAs' copies complete on the
 //                 even CTA's stage barrier
 //   warp 1      : TMEM allocator (2 x 256 columns, both SMs); in the even CTA the MMA
@@ -121,11 +121,14 @@ hessian_simt_kernel(const T *__restrict__ X, int64_t n_tok, int64_t d, int64_t l
 // shared through L2.  Head and tail add into H, which the launcher zeroes first (only
 // calls that overwrite H are cut, so the sum 0 + head + tail is the same in either order).
 // ---------------------------------------------------------------------------------------
-constexpr int TB_M = 128, TB_N = 256, TB_K = 64;      // per-CTA rows, tile columns, tokens
-constexpr int T_STAGES = 6;
-constexpr uint32_t T_BOX = 64 * TB_K * 2;                 // 8 KB: 64 channels x 64 tokens
-constexpr uint32_t T_HALF = 2 * T_BOX;                    // 16 KB: 128 channels
-constexpr uint32_t T_STAGE = 2 * T_HALF;                  // A half + B half: 32 KB
+// 128 tokens per stage (measured against 64: 2.64 against 2.99 ms at d_in = 4096, 42.5
+// against 45.6 ms at 28672, the same at 11008; the same bytes in flight, half the barrier
+// round trips per MMA)
+constexpr int TB_M = 128, TB_N = 256, TB_K = 128;     // per-CTA rows, tile columns, tokens
+constexpr int T_STAGES = 3;
+constexpr uint32_t T_BOX = 64 * TB_K * 2;                 // 16 KB: 64 channels x 128 tokens
+constexpr uint32_t T_HALF = 2 * T_BOX;                    // 32 KB: 128 channels
+constexpr uint32_t T_STAGE = 2 * T_HALF;                  // A half + B half: 64 KB
 constexpr int T_EPI_WARPS = 8;
 constexpr int T_THREADS = 64 + 32 * T_EPI_WARPS;          // 320
 constexpr size_t T_SMEM = 1024 + T_STAGES * T_STAGE + 256;
@@ -133,7 +136,7 @@ constexpr size_t T_SMEM = 1024 + T_STAGES * T_STAGE + 256;
 struct HessTcParams {
   int64_t d, n_tok;
   int n_blocks;       // ceil(d / 256)
-  int seg_stages;     // stages (of 64 tokens) per accumulation segment
+  int seg_stages;     // stages (of TB_K tokens) per accumulation segment
   float *H;
   int accumulate;
   uint64_t wait_ns;   // budget of every mbarrier wait
