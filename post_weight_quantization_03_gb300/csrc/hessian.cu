@@ -647,11 +647,11 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
     if (r > 0 && pairs > r) {
       const int64_t k = ceil_div(r, pairs - r);     // batches of tails per idle pair
       // heads and k batches of tails end together: head = k rho / (1 + k rho) of the tokens,
-      // in whole accumulation segments, where rho = 1.1 is the time of a tail's token stage
-      // relative to a head's (measured at d = 4096: 429 against 390 ns; the tails share
-      // their tokens through L2 with fewer tiles)
+      // in whole accumulation segments, where rho = 1.05 is the time of a tail's token stage
+      // relative to a head's (measured at d = 4096: 816 against 791 ns per 128 tokens; the
+      // tails share their tokens through L2 with fewer tiles)
       const int64_t nsegs = ceil_div(total, p.seg_stages);
-      const int64_t head_segs = (nsegs * 11 * k + (10 + 11 * k) / 2) / (10 + 11 * k);
+      const int64_t head_segs = (nsegs * 21 * k + (20 + 21 * k) / 2) / (20 + 21 * k);
       // worth it when the last round shrinks by at least 2 % of the whole call
       if (head_segs >= 1 && head_segs < nsegs && nsegs >= 8 && 50 * (nsegs - head_segs) >= rounds * nsegs) {
         p.full_tiles = (int)(tiles - r);

@@ -67,7 +67,7 @@ def _codes(qpacked, bits, d):
     (4000, 640, "f16", 2, 1),       # ragged channels: the last rows of a pair beyond d
     (3998, 512, "f16", 0, 0),       # rows of H not 16-byte aligned
     # the last round's tiles cut into a head and a tail that add onto a zeroed H
-    (4096, 4096, "f16", 0, 0),      # 60 cut tiles, heads of 7 of 8 segments, 4 tail batches
+    (4096, 4096, "f16", 0, 0),      # 60 cut tiles, heads of 6 of 8 segments, 4 tail batches
     (3000, 4100, "bf16", 3, 2),     # ragged channels and tokens: 2 cut tiles, tail ends ragged
 ])
 def test_hessian_parity(d, n, dtype, dead, outl):
