@@ -117,9 +117,10 @@ hessian_simt_kernel(const T *__restrict__ X, int64_t n_tok, int64_t d, int64_t l
 // The heads run beside the first batch of tails on the pairs the partial round leaves idle,
 // the later batches of tails follow on the same pairs, and the cut is placed so that the
 // heads and the k batches of tails end together: a round of about k/(k+1) tile-times
-// instead of one.  The heads walk the same tokens in step, and so does each batch of tails, so X stays
-// shared through L2.  Head and tail add into H, which the launcher zeroes first (only
-// calls that overwrite H are cut, so the sum 0 + head + tail is the same in either order).
+// instead of one.  The heads walk the same tokens in step, and so does each batch of tails,
+// so X stays shared through L2.  Head and tail add into H, which the launcher zeroes first
+// (only calls that overwrite H are cut, so the sum 0 + head + tail is the same in either
+// order).
 // ---------------------------------------------------------------------------------------
 // 128 tokens per stage (measured against 64: 2.64 against 2.99 ms at d_in = 4096, 42.5
 // against 45.6 ms at 28672, the same at 11008; the same bytes in flight, half the barrier
@@ -141,8 +142,8 @@ struct HessTcParams {
   int accumulate;
   uint64_t wait_ns;   // budget of every mbarrier wait
   int lost_stage;     // test hook: the producers issue nothing for this stage (-1: none)
-  int full_tiles;     // units [0, full_tiles): whole tiles, written with plain stores
-  int cut_tiles;      // then cut_tiles heads and cut_tiles tails (atomic adds)
+  int full_tiles;     // units [0, full_tiles): whole tiles, stored (added when accumulating)
+  int cut_tiles;      // then cut_tiles heads and cut_tiles tails, added onto a zeroed H
   int cut_stage;      // first token stage of a tail
   int tma_h;          // 1: off-diagonal tiles leave through the H tensor map
 };
@@ -653,7 +654,8 @@ gptq_status launch_hessian_tc(const void *X, int xdtype, int64_t n_tok, int64_t 
       const int64_t nsegs = ceil_div(total, p.seg_stages);
       const int64_t head_segs = (nsegs * 21 * k + (20 + 21 * k) / 2) / (20 + 21 * k);
       // worth it when the last round shrinks by at least 2 % of the whole call
-      if (head_segs >= 1 && head_segs < nsegs && nsegs >= 8 && 50 * (nsegs - head_segs) >= rounds * nsegs) {
+      if (head_segs >= 1 && head_segs < nsegs && nsegs >= 8 &&
+          50 * (nsegs - head_segs) >= rounds * nsegs) {
         p.full_tiles = (int)(tiles - r);
         p.cut_tiles = (int)r;
         p.cut_stage = (int)(head_segs * p.seg_stages);
