@@ -280,19 +280,21 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
         tc::tc_fence_before();
         __syncwarp();
       };
-      // each warp drains its lane quarter on its own; the four agree once per tile
-      for (int gi = 0; gi < ngroups && ok; ++gi, ++hg) {
-        const int hb = hg % kHeadBufs;
+      // each warp drains its lane quarter on its own; the four agree once per tile.  The
+      // cross sum is drained before the tile's last head sum (both are complete by then):
+      // the next tile's first MMAs wait for the cross sum only, so they start one drain
+      // earlier.
+      auto drain_head = [&](int gi) -> bool {
+        const int hb = (hg + gi) % kHeadBufs;
         int okl = 0;
-        if (lane == 0) okl = tc::mbar_wait(&hfull[hb], (hg / kHeadBufs) & 1, st) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, okl, 0)) {
-          ok = false;
-          break;
-        }
+        if (lane == 0) okl = tc::mbar_wait(&hfull[hb], ((hg + gi) / kHeadBufs) & 1, st) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, okl, 0)) return false;
         tc::tc_fence_after();
         drain((uint32_t)(hb * BN));
         if (lane == 0) tc::mbar_arrive(&hempty[hb]);
-      }
+        return true;
+      };
+      for (int gi = 0; gi < ngroups - 1 && ok; ++gi) ok = drain_head(gi);
       if (ok) {
         int okl = 0;
         if (lane == 0) okl = tc::mbar_wait(xfull, it & 1, st) ? 1 : 0;
@@ -304,6 +306,8 @@ tc_gemm_short_sums_kernel(const __grid_constant__ CUtensorMap ma_hi,
           ok = false;
         }
       }
+      if (ok) ok = drain_head(ngroups - 1);
+      hg += ngroups;
       ok = tc::named_barrier_and(1, 128, ok);   // uniform across the four warps
       if (!ok) break;
       int tm, tn;
