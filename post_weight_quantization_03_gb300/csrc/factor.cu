@@ -839,8 +839,12 @@ gptq_status enqueue_prepare(float *H, int64_t d, float damp, float *U, uint8_t *
   // than all SMs, than one CTA per tile, and the same as 32)
   const int side_ctas = overlap ? std::max(1, ss->num_sms - 16) : 0;
   // the far products are persistent too (measured: 95 against 116 ms for one CTA per tile
-  // on a 28672-wide layer, 8.3 against 9.0 ms at 11008)
-  const int far_ctas = side_ctas;
+  // on a 28672-wide layer, 8.3 against 9.0 ms at 11008).  On narrower layers they are a
+  // smaller part of the work and leave more SMs to the chain and the near products
+  // (measured, prepare: 1.221 against 1.248 ms at 4096 leaving 76, 7.53 against 7.74 ms at
+  // 11008 leaving 48; at 28672 leaving 32 or more costs 1.5 % to 50 %)
+  const int far_left = d <= 6144 ? 76 : d <= 16384 ? 48 : 16;
+  const int far_ctas = overlap ? std::max(1, ss->num_sms - far_left) : 0;
   GPTQ_CUDA_CHECK(cudaMemsetAsync(w.st, 0, sizeof(DevStatus), s));
   // vector path: rows of H, Yt and U start 16-byte aligned (the workspace is)
   const bool vec = (d % 4) == 0 && (((uintptr_t)H) % 16) == 0 && (((uintptr_t)U) % 16) == 0;
