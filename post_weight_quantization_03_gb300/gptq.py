@@ -386,8 +386,9 @@ def quantize_block(groups, bits=(4,), block=128, damp=0.01, chunk_tok=None, over
     Hessians are accumulated (in chunks of ``chunk_tok`` tokens, or in one call when None) on
     a producer stream, ahead of the prepares and sweeps, which run on ``consumers``
     higher-priority streams taken in turn by group (so one group's sweep can run beside the
-    next group's prepare); every step is a call of this library.  Returns ``[{bits: [(qpacked, scale, zero, None) per layer]}, ...]`` and
-    the dead-column counts, in group order."""
+    next group's prepare); every step is a call of this library.  Returns
+    ``[{bits: [(qpacked, scale, zero, None) per layer]}, ...]`` and the dead-column counts,
+    in group order."""
     torch = _torch()
     dev = groups[0][1][0].device
     caller = torch.cuda.current_stream(dev)
