@@ -197,8 +197,11 @@ def _oracle_h(d, n, dead, outl, seed, dtype="f16", relu=False):
     return O.hessian(X)
 
 
-@pytest.mark.parametrize("d,n,dead,outl", [(256, 512, 0, 0), (300, 900, 3, 2),
-                                           (777, 3000, 7, 4), (1024, 4096, 10, 8)])
+@pytest.mark.parametrize("d,n,dead,outl", [
+    (256, 512, 0, 0), (300, 900, 3, 2), (777, 3000, 7, 4), (1024, 4096, 10, 8),
+    # wide enough for deferred groups: the columns past the next group of four panels are
+    # updated once per group by the far products (one group, ragged; then three groups)
+    (1600, 4096, 6, 3), (2560, 4096, 0, 2)])
 def test_prepare_parity(d, n, dead, outl):
     H64 = _oracle_h(d, n, dead, outl, seed=d)
     H32 = H64.astype(np.float32)
